@@ -1,0 +1,50 @@
+"""Seeded input generators: determinism, and host (numpy) == device-style (torch) streams."""
+import numpy as np
+import torch
+
+from int4_grouped_expert_router_gb300 import synth
+
+
+def test_splitmix_reference_values():
+    # SplitMix64 from state 0: the published first outputs of the generator
+    # (state += golden gamma, then the mix) are 0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F.
+    assert [int(v) for v in synth.u64(0, 3)] == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+
+
+def test_numpy_and_torch_streams_agree():
+    for seed in (0, 1, synth.stream_seed(synth.BASE_SEED, "expert", 17, "gate")):
+        a = synth.u64(seed, 1001)
+        b = synth.u64_torch(seed, 1001).numpy().view(np.uint64)
+        assert np.array_equal(a, b)
+        assert np.array_equal(synth.random_bytes(seed, 777), synth.random_bytes_torch(seed, 777).numpy())
+        assert np.array_equal(synth.uniform(seed, 500, 0.005, 0.02), synth.uniform_torch(seed, 500, 0.005, 0.02).numpy())
+
+
+def test_expert_tensor_host_and_torch_agree():
+    p, s = synth.expert_tensor(123, 16, 40, 8)
+    pt, st = synth.expert_tensor_torch(123, 16, 40, 8, "cpu")
+    assert np.array_equal(p, pt.numpy()) and np.array_equal(s, st.numpy())
+    assert p.shape == (16, 20) and s.shape == (16 * 5,)
+    assert 0.005 <= s.min() and s.max() < 0.02
+
+
+def test_normal_moments_and_determinism():
+    z = synth.normal(5, 200001)
+    assert abs(float(z.mean())) < 0.01 and abs(float(z.std()) - 1.0) < 0.01
+    assert np.array_equal(z, synth.normal(5, 200001))
+
+
+def test_bf16_rounding():
+    v = np.array([1.0, 1.00390625, 1.005859375, -2.5, 3.0e38], np.float32)
+    bits = synth.to_bf16_bits(v)
+    back = synth.bf16_bits_to_f32(bits)
+    assert back[0] == 1.0 and back[1] == 1.0   # tie -> even
+    assert back[2] == np.float32(1.0078125)
+    assert back[3] == -2.5
+    t = torch.tensor(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(bits, t)
+
+
+def test_zipf_bias_is_skewed():
+    b = synth.zipf_bias(synth.BASE_SEED, 256)
+    assert b.shape == (256,) and float(b.max() - b.min()) > 1.0
