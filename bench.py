@@ -1,0 +1,382 @@
+#!/usr/bin/env python3
+"""Benchmark of one decode-time MoE layer (device router + grouped int4 expert FFN + reduce).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload decode]
+
+A step is one pass of the whole hot path for one token of the full-shape decode layer
+(D=6144, I=2048, E=256 resident experts, K=8, S=1, per-row int4): coli_router_select followed by
+coli_expert_group. Inputs are resident in HBM before the timed region. Each step is bracketed by
+CUDA events on the library's stream; a 256 MiB buffer is written between steps (outside the
+events) so every step starts with a cold L2. Rank 0 prints one JSON line.
+
+--impl reference times the CPU oracle (the plain float64 restatement in oracle/) on the host's
+cores for a bounded sample of the same workload and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs per MoE decode layer (S=1, E=256,K=8) and expert-weight HBM GB/s vs peak"
+UNIT = "us/layer"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--cpu-worker", type=int, default=0, help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def workload_desc(cfg):
+    return (f"MoE decode layer D={cfg.D} I={cfg.I} E={cfg.E} resident experts K={cfg.K} S={cfg.S}, "
+            f"int4 gs={cfg.gs}, {cfg.x_dtype} activations, top-p={cfg.topp}")
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle leg (reference arm and cpu_baseline): runs in a child process pinned to one thread.
+# ------------------------------------------------------------------------------------------------
+
+def cpu_worker(workload: str, tokens: int):
+    import oracle.moe as O
+    from int4_grouped_expert_router_gb300.workload import CONFIGS, host_expert, router_host_inputs
+
+    cfg = CONFIGS[workload]
+    t0 = time.perf_counter()
+    for tok in range(tokens):
+        x, Wr, bias, resid = router_host_inputs(cfg, tok)
+        idx, w, n, _ = O.router_select(x, Wr, bias, cfg.K, cfg.topp, cfg.norm_topk, cfg.routed_scale)
+        experts = {}
+        for e in set(int(v) for v in idx.reshape(-1) if v >= 0):
+            experts[e] = tuple(O.Tensor(p, s, r, c, gs) for (p, s, r, c, gs) in host_expert(cfg, e))
+        O.expert_group(x, experts, idx, w, n, resid)
+    dt = time.perf_counter() - t0
+    print(json.dumps({"us_per_layer": dt / tokens * 1e6, "tokens": tokens, "seconds": dt}))
+
+
+def run_cpu_leg(workload: str, tokens: int):
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", str(tokens), "--workload", workload],
+                       capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle timing failed: {r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return 0
+    from int4_grouped_expert_router_gb300.workload import CONFIGS
+    cfg = CONFIGS[args.workload]
+    per_step_tokens = 1
+    tokens = max(1, (args.steps + args.warmup) * per_step_tokens)
+    tokens = min(tokens, 6)  # bounded sample: a few seconds of single-threaded oracle per token
+    res = run_cpu_leg(args.workload, tokens)
+    v = res["us_per_layer"]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": res["tokens"],
+        "warmup": 0, "ms_per_step": v / 1000.0, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded SplitMix64; shapes of the pages' GLM-5.2 decode layer)",
+        "config": {"workload": workload_desc(cfg)},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{res['tokens']} tokens of the {args.workload} layer (router + 8 experts each)"},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index, enabled=True):
+        self.proc = None
+        self.device_index = device_index
+        if not enabled:
+            return
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={device_index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def load_traffic(kernel: str, src_hash: str):
+    """Per-launch DRAM bytes of ``kernel`` from the committed ncu summary, if taken on this source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        for line in f:
+            kv = dict(tok.split("=", 1) for tok in line.split() if "=" in tok)
+            if kv.get("kernel") == kernel and kv.get("source_sha") == src_hash:
+                try:
+                    return float(kv["dram_bytes_per_launch"])
+                except (KeyError, ValueError):
+                    return None
+    return None
+
+
+def source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("experts.cu", "coli_internal.h"):
+        with open(os.path.join(ROOT, "int4_grouped_expert_router_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def gpu_arm(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    from int4_grouped_expert_router_gb300 import binding as B
+    from int4_grouped_expert_router_gb300.build import build
+    from int4_grouped_expert_router_gb300.workload import CONFIGS, DeviceLayer, router_host_inputs
+
+    build()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    cfg = CONFIGS[args.workload]
+    stream = torch.cuda.current_stream()
+    ctx = B.coli_init(local, stream)
+    layer = DeviceLayer(ctx, cfg)
+    n_tok = args.warmup + args.steps
+    B.coli_reserve(ctx, cfg.S, cfg.E, cfg.K, cfg.D, cfg.I)
+
+    # per-step inputs, resident on the device before timing (each rank its own tokens)
+    xs, rs = [], []
+    for s in range(n_tok):
+        x, _, _, resid = router_host_inputs(cfg, rank * 100000 + s)
+        xs.append(layer.act_tensor(x))
+        rs.append(layer.act_tensor(resid))
+    outs = [layer.outputs() for _ in range(n_tok)]
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_tok)]
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- timed region: device-resident inputs ----
+    for s in range(args.warmup):
+        flush.zero_()
+        layer.step(xs[s], rs[s], outs[s])
+    barrier()
+    clocks = ClockSampler(local, enabled=not args.no_clocks and rank == 0)
+    time.sleep(0.3)
+    t_wall = time.perf_counter()
+    for s in range(args.warmup, n_tok):
+        flush.zero_()
+        ev[s][0].record(stream)
+        layer.step(xs[s], rs[s], outs[s])
+        ev[s][1].record(stream)
+    barrier()
+    wall = time.perf_counter() - t_wall
+    clock_info = clocks.stop()
+    assert B.coli_check_error(ctx) == 0, B.coli_last_error(ctx)
+    step_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.warmup, n_tok)]
+    total_ms = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    us_per_layer = total_ms * 1000.0 / (args.steps * world)
+
+    # bytes each step had to read: the kept experts' packed weights + scales
+    expert_bytes = []
+    gateup_bytes = []
+    for s in range(args.warmup, n_tok):
+        idx = outs[s]["idx"].cpu().numpy()
+        ids = [int(e) for e in idx.reshape(-1) if e >= 0]
+        uniq = sorted(set(ids))
+        expert_bytes.append(sum(cfg.expert_bytes(e) for e in uniq))
+        gu = 0
+        for e in uniq:
+            gs = cfg.gs_of(e)
+            from int4_grouped_expert_router_gb300 import synth
+            gu += 2 * (cfg.I * ((cfg.D + 1) // 2) + 4 * synth.scale_count(cfg.I, cfg.D, gs))
+        gateup_bytes.append(gu)
+    mean_expert_bytes = float(np.mean(expert_bytes))
+    hbm_peak, peak_kind = peaks()
+    layer_gbs = mean_expert_bytes / (us_per_layer * 1e-6) / 1e9 * (1 if world == 1 else world)
+
+    # ---- per-kernel durations: a second pass of the same steps with event pairs per launch ----
+    B.coli_profile_enable(ctx, True)
+    for k in (B.COLI_KERNEL_ROUTER, B.COLI_KERNEL_GATEUP, B.COLI_KERNEL_DOWN, B.COLI_KERNEL_COMBINE):
+        B.coli_profile_read(ctx, k)
+    for s in range(args.warmup, n_tok):
+        flush.zero_()
+        layer.step(xs[s], rs[s], outs[s])
+    kern = {}
+    for name, k in (("router", B.COLI_KERNEL_ROUTER), ("gateup", B.COLI_KERNEL_GATEUP), ("down", B.COLI_KERNEL_DOWN),
+                    ("combine", B.COLI_KERNEL_COMBINE)):
+        ms, n = B.coli_profile_read(ctx, k)
+        if n:
+            kern[name] = {"launches": n, "mean_us": ms * 1000.0 / n}
+    B.coli_profile_enable(ctx, False)
+    gu_us = kern["gateup"]["mean_us"]
+    achieved = float(np.mean(gateup_bytes)) / (gu_us * 1e-6) / 1e9
+    traffic = load_traffic("gateup_kernel", source_hash())
+
+    # ---- end to end through the C ABI with host buffers: H2D inputs, D2H result per step ----
+    hx = [torch.empty_like(xs[s], device="cpu").pin_memory() for s in range(n_tok)]
+    hr = [torch.empty_like(rs[s], device="cpu").pin_memory() for s in range(n_tok)]
+    hy = [torch.empty_like(outs[s]["y"], device="cpu").pin_memory() for s in range(n_tok)]
+    for s in range(n_tok):
+        hx[s].copy_(xs[s])
+        hr[s].copy_(rs[s])
+    dx = [torch.empty_like(xs[s]) for s in range(n_tok)]
+    dr = [torch.empty_like(rs[s]) for s in range(n_tok)]
+    for s in range(args.warmup):
+        flush.zero_()
+        dx[s].copy_(hx[s], non_blocking=True)
+        dr[s].copy_(hr[s], non_blocking=True)
+        layer.step(dx[s], dr[s], outs[s])
+        hy[s].copy_(outs[s]["y"], non_blocking=True)
+    barrier()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_tok)]
+    for s in range(args.warmup, n_tok):
+        flush.zero_()
+        e2e_ev[s][0].record(stream)
+        dx[s].copy_(hx[s], non_blocking=True)
+        dr[s].copy_(hr[s], non_blocking=True)
+        layer.step(dx[s], dr[s], outs[s])
+        hy[s].copy_(outs[s]["y"], non_blocking=True)
+        e2e_ev[s][1].record(stream)
+    barrier()
+    e2e_ms = sum(e2e_ev[s][0].elapsed_time(e2e_ev[s][1]) for s in range(args.warmup, n_tok))
+    if dist is not None:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_us = e2e_ms * 1000.0 / (args.steps * world)
+    h2d = xs[0].numel() * xs[0].element_size() + rs[0].numel() * rs[0].element_size()
+    d2h = outs[0]["y"].numel() * outs[0]["y"].element_size()
+
+    launches_per_step = 3 if cfg.S == 1 else 4
+    result = None
+    if rank == 0:
+        cpu = None
+        try:
+            cpu_tokens = 4
+            res = run_cpu_leg(args.workload, cpu_tokens)
+            cpu = {"value": res["us_per_layer"], "unit": UNIT, "cores": 1, "kind": "oracle",
+                   "sample": f"{res['tokens']} tokens of the {args.workload} layer (router + kept experts), "
+                             f"{res['seconds']:.1f} s single-threaded"}
+        except Exception as exc:  # the CPU leg must not hide the GPU number
+            cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": f"failed: {exc}"[:300]}
+        p50 = statistics.median(step_ms) * 1000.0
+        result = {
+            "metric": METRIC, "value": us_per_layer, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": us_per_layer / 1000.0 * world, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int4xf32",
+            "data": "synthetic (seeded SplitMix64; shapes of the pages' GLM-5.2 decode layer)",
+            "config": {"workload": workload_desc(cfg), "l2": "flushed between steps (256 MiB write, outside the events)",
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "expert_bytes_per_layer": mean_expert_bytes,
+                       "layer_hbm_gbs": layer_gbs, "layer_hbm_frac": layer_gbs / hbm_peak,
+                       "p50_us": p50, "p10_us": float(np.percentile(step_ms, 10)) * 1000.0,
+                       "p90_us": float(np.percentile(step_ms, 90)) * 1000.0,
+                       "kernels_us": kern, "wall_s": wall},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": traffic, "kernel": "gateup_kernel",
+                         "peak_kind": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": float(np.mean(gateup_bytes))},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clock_info,
+        }
+    layer.free()
+    B.coli_destroy(ctx)
+    if dist is not None:
+        dist.destroy_process_group()
+    if result is not None:
+        print(json.dumps(result))
+    return 0
+
+
+def main():
+    args = parse()
+    if args.cpu_worker:
+        cpu_worker(args.workload, args.cpu_worker)
+        return 0
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+    return gpu_arm(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

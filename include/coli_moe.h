@@ -1,0 +1,169 @@
+/*
+ * coli_moe.h -- C ABI of the GB300 (sm_103a) decode-time MoE block: a device router and a
+ * grouped int4 expert FFN with an on-device, fixed-order weighted reduce.
+ *
+ * Sources (web pages about the "colibri" int4 MoE engine), cited by page and section:
+ *   [g4]     c/backend_cuda.cu commit history, commit "grouped MoE kernels were per-row-only"
+ *   [router] c/backend_cuda.cu commit history, commit "First increment of the #431 plan"
+ *   [tcgate] c/backend_cuda.cu commit history, commit "The TC_W4A16 branch ..."
+ *   [fixes]  c/backend_cuda.cu commit history, commit "Three vendor-neutral fixes to backend_cuda.cu"
+ *   [pipe]   c/backend_cuda.cu commit history, commit "GPU resident pipeline ..."
+ *   [resid]  PR #434 "COLI_CUDA_RESID=1", section "What"
+ *
+ * Conventions shared by every call:
+ *  - Return value: COLI_OK (0) or a negative COLI_E_* code. A failed call leaves no CUDA error
+ *    pending for the next call (the runtime error is consumed on the failure path, [fixes] 2).
+ *    coli_last_error() gives a one-line description of the last failure on that context.
+ *  - Pointers to activations, routes and outputs are DEVICE pointers owned by the caller; the
+ *    library never frees them. Weights passed to coli_expert_upload may be host or device
+ *    pointers; the library copies them and owns the copy.
+ *  - Compute calls are asynchronous on the context's stream: they validate arguments on the host,
+ *    enqueue kernels and return. They never synchronise and never copy to the host.
+ *  - Errors found by kernels (an expert index outside the table or naming an unset entry, a
+ *    non-finite activation or router score) are recorded in a per-context device error word;
+ *    coli_check_error() synchronises the stream, returns that code and clears it. Kernels never
+ *    trap.
+ *  - Test hook: if the environment variable COLI_FAIL_AFTER=N is set when a context is created,
+ *    every compute call after the first N successful ones returns COLI_E_INJECTED without
+ *    launching anything ([fixes] 3). Uploads, frees, table updates and queries are never gated.
+ *  - A context is used by one host thread at a time.
+ */
+#ifndef COLI_MOE_H
+#define COLI_MOE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define COLI_API __attribute__((visibility("default")))
+#else
+#define COLI_API
+#endif
+
+#define COLI_OK 0
+#define COLI_E_INVAL -1      /* bad argument (NULL, size out of range, unknown dtype/handle) */
+#define COLI_E_OOM -2        /* device allocation failed */
+#define COLI_E_CUDA -3       /* a CUDA runtime call or kernel launch failed */
+#define COLI_E_INJECTED -4   /* COLI_FAIL_AFTER test hook fired; nothing was launched */
+#define COLI_E_FORMAT -5     /* weight format rejected: odd I, odd or negative gs, shape mismatch */
+#define COLI_E_NONFINITE -6  /* (device) non-finite activation or router score */
+#define COLI_E_ROUTE -7      /* (device) expert index outside the table or naming an unset entry */
+
+#define COLI_DTYPE_F32 0     /* IEEE binary32 */
+#define COLI_DTYPE_BF16 1    /* bfloat16 (upper half of a binary32) */
+
+/* Size limits of this build (checked on the host; beyond them a call returns COLI_E_INVAL). */
+#define COLI_MAX_EXPERTS 4096   /* router E and expert-table entries */
+#define COLI_MAX_K 32           /* experts per token */
+#define COLI_MAX_DIM 32768      /* D and I */
+#define COLI_MAX_TOKENS 65536   /* S for coli_router_select */
+#define COLI_MAX_GROUP_TOKENS 1024  /* S for coli_expert_group */
+
+typedef struct coli_ctx coli_ctx;
+
+/* Create a context on CUDA device `device` that enqueues work on `cuda_stream` (a cudaStream_t;
+ * NULL = the legacy default stream). Returns COLI_E_CUDA if the device is unusable.
+ * *out is set to NULL on failure. */
+COLI_API int coli_init(coli_ctx **out, int device, void *cuda_stream);
+
+/* Release every uploaded tensor, the expert table and the workspace. NULL is ignored. */
+COLI_API void coli_destroy(coli_ctx *ctx);
+
+/* Change the stream later calls enqueue on (e.g. a stream being captured into a CUDA graph). */
+COLI_API int coli_set_stream(coli_ctx *ctx, void *cuda_stream);
+
+/* Text of the last failure on this context ("" if none). Valid until the next call. */
+COLI_API const char *coli_last_error(coli_ctx *ctx);
+
+/* COLI_E_* code of the last failure on this context (COLI_OK if none), e.g. after an upload
+ * returned handle 0. */
+COLI_API int coli_last_code(coli_ctx *ctx);
+
+/* Synchronise the context's stream; return and clear the device error word (COLI_OK if clean). */
+COLI_API int coli_check_error(coli_ctx *ctx);
+
+/* Pre-size the workspace for calls up to these sizes so that no later compute call allocates.
+ * Without it, a compute call that needs more workspace than the last one allocates (once). */
+COLI_API int coli_reserve(coli_ctx *ctx, int max_S, int max_E, int max_K, int max_D, int max_I);
+
+/* Per-kernel timing: when on, every kernel launch of this context is bracketed by two CUDA events
+ * recorded on the context's stream (off by default). Kinds: COLI_KERNEL_ROUTER, _GATEUP, _DOWN,
+ * _COMBINE. coli_profile_read synchronises the stream and returns, for one kind, the summed event
+ * time in milliseconds and the number of launches since the previous read of that kind. */
+#define COLI_KERNEL_ROUTER 0
+#define COLI_KERNEL_GATEUP 1
+#define COLI_KERNEL_DOWN 2
+#define COLI_KERNEL_COMBINE 3
+COLI_API int coli_profile_enable(coli_ctx *ctx, int on);
+COLI_API int coli_profile_read(coli_ctx *ctx, int kind, double *total_ms, long long *launches);
+
+/*
+ * Device router, [router] (and the batched router of [pipe] for S > 1):
+ *   z[s,e] = sum_j Wr[e,j] * x[s,j]                 (f32 logits GEMV, f32 accumulation)
+ *   score[s,e]  = 1 / (1 + exp(-z[s,e]))           (sigmoid)
+ *   choice[s,e] = score[s,e] + bias[e]             (bias-augmented; bias NULL = 0)
+ *   idx[s,:] = K rounds of arg-max of choice over the not-yet-chosen experts with a strict '>'
+ *              comparison, so a tie goes to the lower index; slots keep the selection order
+ *   w[s,k]   = score[s, idx[s,k]]                  (weights from the raw, bias-free score)
+ *   top-p (0 < topp < 1): p_k = w_k / sum_{k<K} w_k; keep the shortest prefix of slots whose
+ *              running sum of p_k reaches topp (at least one slot); dropped slots get idx = -1
+ *              and w = 0. topp <= 0 or >= 1 disables it.
+ *   norm_topk != 0: w_k <- w_k / sum of the kept w; then w_k <- w_k * routed_scale.
+ *   All sums of the last three steps run in slot order in binary32.
+ * x: [S x D] row-major, dtype x_dtype. Wr: [E x D] row-major f32. bias: [E] f32 or NULL.
+ * Outputs (device, caller-owned): idx [S x K] int32, w [S x K] f32, n_sel [S] int32 (kept slots
+ * per token) or NULL. Limits: 1 <= K <= min(E, COLI_MAX_K), E <= COLI_MAX_EXPERTS.
+ * A non-finite score sets COLI_E_NONFINITE in the device error word.
+ */
+COLI_API int coli_router_select(coli_ctx *ctx, const void *x, int x_dtype, int S, int D,
+                       const float *Wr, const float *bias, int E, int K, float topp,
+                       int norm_topk, float routed_scale, int32_t *idx, float *w, int32_t *n_sel);
+
+/*
+ * Upload one int4 weight tensor W [O x I], [g4]:
+ *   packed: O rows of ceil(I/2) bytes; byte m of a row holds column 2m in its low nibble and
+ *           column 2m+1 in its high nibble; the stored nibble n means the value n - 8.
+ *   scales: gs == 0: O floats (one per row); gs > 0: O * ceil(I/gs) floats, row-major, one per
+ *           row and per run of gs columns, the last run of a row being the tail group.
+ *   W[o,i] = scale(o,i) * (n(o,i) - 8).
+ * gs must be 0 or even (a byte never straddles two groups); I must be even. Host or device
+ * pointers; the data are copied before the call returns, so the caller may free or overwrite
+ * its buffers afterwards ([fixes] 1). Returns a nonzero handle, or 0 on failure (reason in
+ * coli_last_error: COLI_E_FORMAT for a rejected format, COLI_E_OOM, COLI_E_CUDA).
+ */
+COLI_API uint64_t coli_expert_upload(coli_ctx *ctx, const uint8_t *packed, const float *scales, int O,
+                            int I, int gs);
+
+/* Free an uploaded tensor. It must not be referenced by the expert table (COLI_E_INVAL). */
+COLI_API int coli_expert_free(coli_ctx *ctx, uint64_t handle);
+
+/* Make expert e (0 <= e < COLI_MAX_EXPERTS) the triple (gate [I x D], up [I x D], down [D x I]).
+ * Shapes are checked against each other and against every other entry of the table (all
+ * experts share D and I): COLI_E_FORMAT on mismatch. Handles 0,0,0 clear the entry. */
+COLI_API int coli_expert_table_set(coli_ctx *ctx, int e, uint64_t gate, uint64_t up, uint64_t down);
+
+/*
+ * Grouped expert FFN with weighting and a fixed-order reduce, [tcgate] [g4] [resid]:
+ *   for each token s and kept slot k < n_sel[s] (all K if n_sel is NULL), with e = idx[s,k]:
+ *     g = W_gate[e] x[s],  u = W_up[e] x[s]         (int4 x activation, f32 results)
+ *     h = SiLU(g) * u = g / (1 + exp(-g)) * u       (f32)
+ *     y_k = W_down[e] h                            (f32)
+ *   y[s,:] = resid[s,:] + sum_{k < n_sel[s]} w[s,k] * y_k, the sum over slots formed in slot order
+ *   without atomics, then added to the residual (resid NULL: y = the sum).
+ * x_rows, resid, y: [S x D] row-major in x_dtype (f32 or bf16; bf16 values are widened exactly
+ * and y is rounded to bf16 once at the end). idx, w, n_sel: as produced by coli_router_select,
+ * device pointers. Slots with idx < 0 beyond n_sel are ignored. D and I come from the table.
+ * Every weight byte of an expert is read once per call however many of the S tokens chose it.
+ */
+COLI_API int coli_expert_group(coli_ctx *ctx, const void *x_rows, int x_dtype, int S,
+                      const int32_t *idx, const float *w, const int32_t *n_sel, int K,
+                      const void *resid, void *y);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* COLI_MOE_H */

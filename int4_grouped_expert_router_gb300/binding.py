@@ -1,0 +1,231 @@
+"""Thin ctypes binding of libcoli_moe.so with the same names as the C ABI (include/coli_moe.h).
+
+Argument marshalling only: torch tensors are checked for device, dtype and contiguity and passed
+as raw pointers; every step of the computation runs in the library's CUDA kernels. Importing this
+module loads the in-tree library and fails loudly if it has not been built (there is no CPU
+fallback): build it with ``python -m int4_grouped_expert_router_gb300.build``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libcoli_moe.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "coli_moe.h")
+
+_lib = None
+
+
+def _constants():
+    consts = {}
+    with open(HEADER) as f:
+        for m in re.finditer(r"^#define (COLI_\w+)\s+(-?\d+)", f.read(), re.M):
+            consts[m.group(1)] = int(m.group(2))
+    return consts
+
+
+_C = _constants()
+COLI_OK = _C["COLI_OK"]
+COLI_E_INVAL = _C["COLI_E_INVAL"]
+COLI_E_OOM = _C["COLI_E_OOM"]
+COLI_E_CUDA = _C["COLI_E_CUDA"]
+COLI_E_INJECTED = _C["COLI_E_INJECTED"]
+COLI_E_FORMAT = _C["COLI_E_FORMAT"]
+COLI_E_NONFINITE = _C["COLI_E_NONFINITE"]
+COLI_E_ROUTE = _C["COLI_E_ROUTE"]
+COLI_DTYPE_F32 = _C["COLI_DTYPE_F32"]
+COLI_DTYPE_BF16 = _C["COLI_DTYPE_BF16"]
+COLI_MAX_EXPERTS = _C["COLI_MAX_EXPERTS"]
+COLI_MAX_K = _C["COLI_MAX_K"]
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_U64 = ctypes.c_uint64
+
+SIGNATURES = {
+    "coli_init": (_I, [ctypes.POINTER(_P), _I, _P]),
+    "coli_destroy": (None, [_P]),
+    "coli_set_stream": (_I, [_P, _P]),
+    "coli_last_error": (ctypes.c_char_p, [_P]),
+    "coli_last_code": (_I, [_P]),
+    "coli_check_error": (_I, [_P]),
+    "coli_reserve": (_I, [_P, _I, _I, _I, _I, _I]),
+    "coli_router_select": (_I, [_P, _P, _I, _I, _I, _P, _P, _I, _I, _F, _I, _F, _P, _P, _P]),
+    "coli_expert_upload": (_U64, [_P, _P, _P, _I, _I, _I]),
+    "coli_expert_free": (_I, [_P, _U64]),
+    "coli_expert_table_set": (_I, [_P, _I, _U64, _U64, _U64]),
+    "coli_expert_group": (_I, [_P, _P, _I, _I, _P, _P, _P, _I, _P, _P]),
+    "coli_profile_enable": (_I, [_P, _I]),
+    "coli_profile_read": (_I, [_P, _I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong)]),
+}
+
+COLI_KERNEL_ROUTER = _C["COLI_KERNEL_ROUTER"]
+COLI_KERNEL_GATEUP = _C["COLI_KERNEL_GATEUP"]
+COLI_KERNEL_DOWN = _C["COLI_KERNEL_DOWN"]
+COLI_KERNEL_COMBINE = _C["COLI_KERNEL_COMBINE"]
+
+
+class ColiError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"{msg} (code {code})")
+        self.code = code
+
+
+def library():
+    """Load libcoli_moe.so (once). Raises if the library has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m int4_grouped_expert_router_gb300.build` (no CPU fallback exists)")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def act_dtype(t):
+    if t.dtype == torch.float32:
+        return COLI_DTYPE_F32
+    if t.dtype == torch.bfloat16:
+        return COLI_DTYPE_BF16
+    raise ValueError("activations must be float32 or bfloat16")
+
+
+def _check(ctx, rc, what):
+    if rc != COLI_OK:
+        raise ColiError(rc, f"{what}: {coli_last_error(ctx)}")
+    return rc
+
+
+def coli_init(device=0, stream=None):
+    """Create a context; ``stream`` is a torch.cuda.Stream (default: the current stream)."""
+    lib = library()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    out = ctypes.c_void_p()
+    rc = lib.coli_init(ctypes.byref(out), device, ctypes.c_void_p(stream.cuda_stream))
+    if rc != COLI_OK:
+        raise ColiError(rc, "coli_init failed")
+    return out
+
+
+def coli_destroy(ctx):
+    library().coli_destroy(ctx)
+
+
+def coli_set_stream(ctx, stream):
+    return _check(ctx, library().coli_set_stream(ctx, ctypes.c_void_p(stream.cuda_stream)), "coli_set_stream")
+
+
+def coli_last_error(ctx):
+    s = library().coli_last_error(ctx)
+    return s.decode() if s else ""
+
+
+def coli_last_code(ctx):
+    return library().coli_last_code(ctx)
+
+
+def coli_check_error(ctx):
+    """Synchronise and return (and clear) the device error word: 0 when clean."""
+    return library().coli_check_error(ctx)
+
+
+def coli_reserve(ctx, max_S, max_E, max_K, max_D, max_I):
+    return _check(ctx, library().coli_reserve(ctx, max_S, max_E, max_K, max_D, max_I), "coli_reserve")
+
+
+def coli_router_select(ctx, x, Wr, bias, K, topp, norm_topk, routed_scale, idx, w, n_sel=None):
+    S, D = x.shape
+    E = Wr.shape[0]
+    _dev(x, name="x")
+    _dev(Wr, torch.float32, "Wr")
+    _dev(bias, torch.float32, "bias")
+    _dev(idx, torch.int32, "idx")
+    _dev(w, torch.float32, "w")
+    _dev(n_sel, torch.int32, "n_sel")
+    if Wr.shape[1] != D or idx.numel() != S * K or w.numel() != S * K or (n_sel is not None and n_sel.numel() != S):
+        raise ValueError("router_select: inconsistent shapes")
+    if bias is not None and bias.numel() != E:
+        raise ValueError("router_select: bias must have E entries")
+    rc = library().coli_router_select(ctx, _ptr(x), act_dtype(x), S, D, _ptr(Wr), _ptr(bias), E, K, float(topp),
+                                      int(bool(norm_topk)), float(routed_scale), _ptr(idx), _ptr(w), _ptr(n_sel))
+    return _check(ctx, rc, "coli_router_select")
+
+
+def coli_expert_upload(ctx, packed, scales, O, I, gs):
+    """Upload one int4 tensor from host or device tensors; returns the handle (raises on failure)."""
+    if packed.dtype != torch.uint8 or scales.dtype != torch.float32:
+        raise ValueError("packed must be uint8 and scales float32")
+    if not (packed.is_contiguous() and scales.is_contiguous()):
+        raise ValueError("packed and scales must be contiguous")
+    if packed.numel() != O * ((I + 1) // 2):
+        raise ValueError("packed must hold O * ceil(I/2) bytes")
+    nsc = O if gs == 0 else O * ((I + gs - 1) // gs) if gs > 0 else -1
+    if scales.numel() != nsc:
+        raise ValueError("scale count must be O (gs=0) or O*ceil(I/gs)")
+    h = library().coli_expert_upload(ctx, _ptr(packed), _ptr(scales), O, I, gs)
+    if h == 0:
+        raise ColiError(library().coli_last_code(ctx), f"coli_expert_upload: {coli_last_error(ctx)}")
+    return h
+
+
+def coli_expert_free(ctx, handle):
+    return _check(ctx, library().coli_expert_free(ctx, handle), "coli_expert_free")
+
+
+def coli_expert_table_set(ctx, e, gate, up, down):
+    return _check(ctx, library().coli_expert_table_set(ctx, e, gate, up, down), "coli_expert_table_set")
+
+
+def coli_expert_group(ctx, x_rows, idx, w, n_sel, K, resid, y):
+    S = x_rows.shape[0]
+    _dev(x_rows, name="x_rows")
+    _dev(idx, torch.int32, "idx")
+    _dev(w, torch.float32, "w")
+    _dev(n_sel, torch.int32, "n_sel")
+    _dev(resid, x_rows.dtype, "resid")
+    _dev(y, x_rows.dtype, "y")
+    if idx.numel() != S * K or w.numel() != S * K or y.shape != x_rows.shape or \
+            (resid is not None and resid.shape != x_rows.shape) or (n_sel is not None and n_sel.numel() != S):
+        raise ValueError("expert_group: inconsistent shapes")
+    rc = library().coli_expert_group(ctx, _ptr(x_rows), act_dtype(x_rows), S, _ptr(idx), _ptr(w), _ptr(n_sel), K,
+                                     _ptr(resid), _ptr(y))
+    return _check(ctx, rc, "coli_expert_group")
+
+
+def coli_profile_enable(ctx, on):
+    return _check(ctx, library().coli_profile_enable(ctx, int(bool(on))), "coli_profile_enable")
+
+
+def coli_profile_read(ctx, kind):
+    """(total_ms, launches) of one kernel kind since its previous read (synchronises)."""
+    ms = ctypes.c_double()
+    n = ctypes.c_longlong()
+    _check(ctx, library().coli_profile_read(ctx, kind, ctypes.byref(ms), ctypes.byref(n)), "coli_profile_read")
+    return ms.value, n.value

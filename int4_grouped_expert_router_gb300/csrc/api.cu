@@ -1,0 +1,378 @@
+// C ABI of libcoli_moe.so: contexts, weight upload, the expert table, error reporting and the
+// argument checks of the compute calls. The kernels live in router.cu and experts.cu.
+#include <stdlib.h>
+#include <string.h>
+
+#include <string>
+
+#include "coli_internal.h"
+
+namespace coli {
+
+int fail(coli_ctx* ctx, int code, const std::string& msg) {
+  if (ctx) {
+    ctx->last_error = msg;
+    ctx->last_code = code;
+  }
+  return code;
+}
+
+// Record a failed runtime call and consume the runtime's error state so that the next healthy
+// call does not report it (a failed allocation must not poison later launches).
+int cuda_fail(coli_ctx* ctx, cudaError_t e, const char* what) {
+  (void)cudaGetLastError();
+  std::string m = std::string(what) + ": " + cudaGetErrorString(e);
+  return fail(ctx, e == cudaErrorMemoryAllocation ? COLI_E_OOM : COLI_E_CUDA, m);
+}
+
+bool injected(coli_ctx* ctx) {
+  if (ctx->fail_after < 0) return false;
+  if (ctx->compute_calls >= ctx->fail_after) {
+    ctx->last_error = "COLI_FAIL_AFTER test hook";
+    ctx->last_code = COLI_E_INJECTED;
+    return true;
+  }
+  return false;
+}
+
+int ensure_workspace(coli_ctx* ctx, size_t bytes) {
+  bytes = align_up(bytes < 256 ? 256 : bytes, 256);
+  if (bytes <= ctx->ws.bytes) return COLI_OK;
+  if (ctx->ws.base) {
+    cudaError_t e = cudaStreamSynchronize(ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "workspace grow: stream sync");
+    cudaFree(ctx->ws.base);
+    ctx->ws.base = nullptr;
+    ctx->ws.bytes = 0;
+  }
+  void* p = nullptr;
+  cudaError_t e = cudaMalloc(&p, bytes);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "workspace cudaMalloc");
+  ctx->ws.base = static_cast<char*>(p);
+  ctx->ws.bytes = bytes;
+  return COLI_OK;
+}
+
+static cudaEvent_t prof_event(coli_ctx* ctx) {
+  if (!ctx->prof_free.empty()) {
+    cudaEvent_t e = ctx->prof_free.back();
+    ctx->prof_free.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return e;
+}
+
+ProfScope::ProfScope(coli_ctx* c, int k) : ctx(c), kind(k) {
+  if (!ctx->prof) return;
+  a = prof_event(ctx);
+  b = prof_event(ctx);
+  if (a) cudaEventRecord(a, ctx->stream);
+}
+
+ProfScope::~ProfScope() {
+  if (!ctx->prof) return;
+  if (a && b && cudaEventRecord(b, ctx->stream) == cudaSuccess) {
+    ctx->prof_pending.push_back({kind, a, b});
+  } else {
+    (void)cudaGetLastError();
+    if (a) ctx->prof_free.push_back(a);
+    if (b) ctx->prof_free.push_back(b);
+  }
+}
+
+static bool valid_handle(coli_ctx* ctx, uint64_t h) {
+  return h >= 1 && h <= ctx->tensors.size() && ctx->tensors[h - 1].live;
+}
+
+static TensorDesc make_desc(const HostTensor& t) {
+  TensorDesc d;
+  d.w = t.w;
+  d.s = t.s;
+  d.pitch = t.pitch;
+  d.gs = t.gs;
+  d.G = t.G;
+  d.rows = t.O;
+  d.cols = t.I;
+  d.mode = t.gs == 0 ? SCALE_ROW : (t.gs % 32 == 0 ? SCALE_CHUNK : SCALE_GENERIC);
+  return d;
+}
+
+}  // namespace coli
+
+using namespace coli;
+
+extern "C" {
+
+int coli_init(coli_ctx** out, int device, void* cuda_stream) {
+  if (!out) return COLI_E_INVAL;
+  *out = nullptr;
+  int n = 0;
+  cudaError_t e = cudaGetDeviceCount(&n);
+  if (e != cudaSuccess || device < 0 || device >= n) {
+    (void)cudaGetLastError();
+    return COLI_E_CUDA;
+  }
+  if ((e = cudaSetDevice(device)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return COLI_E_CUDA;
+  }
+  coli_ctx* ctx = new coli_ctx();
+  ctx->device = device;
+  ctx->stream = static_cast<cudaStream_t>(cuda_stream);
+  cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, device);
+  const char* fa = getenv("COLI_FAIL_AFTER");
+  if (fa && *fa) ctx->fail_after = atoll(fa);
+  ctx->h_table.assign(COLI_MAX_EXPERTS, ExpertDesc{});
+  ctx->table_handles.assign(3 * COLI_MAX_EXPERTS, 0);
+  void* p = nullptr;
+  if ((e = cudaMalloc(&p, sizeof(ExpertDesc) * COLI_MAX_EXPERTS)) != cudaSuccess) goto fail;
+  ctx->d_table = static_cast<ExpertDesc*>(p);
+  if ((e = cudaMemset(ctx->d_table, 0, sizeof(ExpertDesc) * COLI_MAX_EXPERTS)) != cudaSuccess) goto fail;
+  if ((e = cudaMalloc(&p, 256)) != cudaSuccess) goto fail;
+  ctx->d_status = static_cast<int*>(p);
+  if ((e = cudaMemset(ctx->d_status, 0, 256)) != cudaSuccess) goto fail;
+  *out = ctx;
+  return COLI_OK;
+fail:
+  (void)cudaGetLastError();
+  coli_destroy(ctx);
+  return e == cudaErrorMemoryAllocation ? COLI_E_OOM : COLI_E_CUDA;
+}
+
+void coli_destroy(coli_ctx* ctx) {
+  if (!ctx) return;
+  cudaSetDevice(ctx->device);
+  cudaStreamSynchronize(ctx->stream);
+  for (auto& t : ctx->tensors) {
+    if (t.w) cudaFree(t.w);
+    if (t.s) cudaFree(t.s);
+  }
+  if (ctx->d_table) cudaFree(ctx->d_table);
+  if (ctx->d_status) cudaFree(ctx->d_status);
+  if (ctx->ws.base) cudaFree(ctx->ws.base);
+  for (auto& r : ctx->prof_pending) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (auto ev : ctx->prof_free) cudaEventDestroy(ev);
+  (void)cudaGetLastError();
+  delete ctx;
+}
+
+int coli_set_stream(coli_ctx* ctx, void* cuda_stream) {
+  if (!ctx) return COLI_E_INVAL;
+  ctx->stream = static_cast<cudaStream_t>(cuda_stream);
+  return COLI_OK;
+}
+
+const char* coli_last_error(coli_ctx* ctx) { return ctx ? ctx->last_error.c_str() : "null context"; }
+
+int coli_last_code(coli_ctx* ctx) { return ctx ? ctx->last_code : COLI_E_INVAL; }
+
+int coli_check_error(coli_ctx* ctx) {
+  if (!ctx) return COLI_E_INVAL;
+  cudaSetDevice(ctx->device);
+  cudaError_t e = cudaStreamSynchronize(ctx->stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "coli_check_error: stream sync");
+  int code = 0;
+  e = cudaMemcpy(&code, ctx->d_status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "coli_check_error: read error word");
+  if (code != 0) {
+    e = cudaMemset(ctx->d_status, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "coli_check_error: clear error word");
+    ctx->last_error = code == COLI_E_ROUTE ? "device: expert index out of range or unset table entry"
+                      : code == COLI_E_NONFINITE ? "device: non-finite activation or router score"
+                                                 : "device error";
+  }
+  return code;
+}
+
+int coli_profile_enable(coli_ctx* ctx, int on) {
+  if (!ctx) return COLI_E_INVAL;
+  ctx->prof = on != 0;
+  return COLI_OK;
+}
+
+int coli_profile_read(coli_ctx* ctx, int kind, double* total_ms, long long* launches) {
+  if (!ctx || kind < 0 || kind > 3 || !total_ms || !launches) return COLI_E_INVAL;
+  cudaSetDevice(ctx->device);
+  cudaError_t e = cudaStreamSynchronize(ctx->stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "coli_profile_read: stream sync");
+  for (auto& r : ctx->prof_pending) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) {
+      ctx->prof_ms[r.kind] += ms;
+      ctx->prof_n[r.kind] += 1;
+    } else {
+      (void)cudaGetLastError();
+    }
+    ctx->prof_free.push_back(r.a);
+    ctx->prof_free.push_back(r.b);
+  }
+  ctx->prof_pending.clear();
+  *total_ms = ctx->prof_ms[kind];
+  *launches = ctx->prof_n[kind];
+  ctx->prof_ms[kind] = 0;
+  ctx->prof_n[kind] = 0;
+  return COLI_OK;
+}
+
+int coli_reserve(coli_ctx* ctx, int max_S, int max_E, int max_K, int max_D, int max_I) {
+  if (!ctx || max_S < 1 || max_E < 1 || max_K < 1 || max_D < 1 || max_I < 1) return COLI_E_INVAL;
+  size_t router = align_up((size_t)max_S * max_E * 2 * sizeof(float), 256);
+  size_t experts = align_up((size_t)max_S * max_K * max_I * sizeof(float), 256) +
+                   align_up((size_t)max_S * max_K * max_D * sizeof(float), 256) + 4096 +
+                   align_up((size_t)(max_S + 1) * sizeof(int) * 4, 256);
+  cudaSetDevice(ctx->device);
+  return ensure_workspace(ctx, router > experts ? router : experts);
+}
+
+uint64_t coli_expert_upload(coli_ctx* ctx, const uint8_t* packed, const float* scales, int O, int I,
+                            int gs) {
+  if (!ctx) return 0;
+  if (!packed || !scales || O < 1 || I < 2 || O > COLI_MAX_DIM || I > COLI_MAX_DIM) {
+    fail(ctx, COLI_E_INVAL, "upload: NULL pointer or shape out of range");
+    return 0;
+  }
+  if (I % 2 != 0 || gs < 0 || gs % 2 != 0) {
+    fail(ctx, COLI_E_FORMAT, "upload: I must be even and gs must be 0 or a positive even number");
+    return 0;
+  }
+  cudaSetDevice(ctx->device);
+  HostTensor t;
+  t.O = O;
+  t.I = I;
+  t.gs = gs;
+  t.G = gs == 0 ? 1 : (I + gs - 1) / gs;
+  t.pitch = (uint32_t)(((I + 31) / 32) * 16);
+  size_t nscales = gs == 0 ? (size_t)O : (size_t)O * t.G;
+  size_t row_bytes = (size_t)I / 2;
+  void* pw = nullptr;
+  void* ps = nullptr;
+  cudaError_t e;
+  if ((e = cudaMalloc(&pw, (size_t)O * t.pitch)) != cudaSuccess) {
+    cuda_fail(ctx, e, "upload: cudaMalloc weights");
+    return 0;
+  }
+  if ((e = cudaMalloc(&ps, nscales * sizeof(float))) != cudaSuccess) {
+    cudaFree(pw);
+    cuda_fail(ctx, e, "upload: cudaMalloc scales");
+    return 0;
+  }
+  // pad nibbles hold 8 (the value 0); then copy the caller's rows into the padded pitch
+  if ((e = cudaMemsetAsync(pw, 0x88, (size_t)O * t.pitch, ctx->stream)) != cudaSuccess ||
+      (e = cudaMemcpy2DAsync(pw, t.pitch, packed, row_bytes, row_bytes, O, cudaMemcpyDefault,
+                             ctx->stream)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(ps, scales, nscales * sizeof(float), cudaMemcpyDefault, ctx->stream)) !=
+          cudaSuccess ||
+      (e = cudaStreamSynchronize(ctx->stream)) != cudaSuccess) {
+    cudaFree(pw);
+    cudaFree(ps);
+    cuda_fail(ctx, e, "upload: copy");
+    return 0;
+  }
+  t.w = static_cast<uint8_t*>(pw);
+  t.s = static_cast<float*>(ps);
+  t.live = true;
+  ctx->tensors.push_back(t);
+  return (uint64_t)ctx->tensors.size();
+}
+
+int coli_expert_free(coli_ctx* ctx, uint64_t handle) {
+  if (!ctx) return COLI_E_INVAL;
+  if (!valid_handle(ctx, handle)) return fail(ctx, COLI_E_INVAL, "free: unknown handle");
+  HostTensor& t = ctx->tensors[handle - 1];
+  if (t.table_refs > 0) return fail(ctx, COLI_E_INVAL, "free: tensor is still in the expert table");
+  cudaSetDevice(ctx->device);
+  cudaError_t e = cudaStreamSynchronize(ctx->stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "free: stream sync");
+  cudaFree(t.w);
+  cudaFree(t.s);
+  t = HostTensor{};
+  return COLI_OK;
+}
+
+int coli_expert_table_set(coli_ctx* ctx, int e, uint64_t gate, uint64_t up, uint64_t down) {
+  if (!ctx) return COLI_E_INVAL;
+  if (e < 0 || e >= COLI_MAX_EXPERTS) return fail(ctx, COLI_E_INVAL, "table_set: expert id out of range");
+  cudaSetDevice(ctx->device);
+  uint64_t* cur = &ctx->table_handles[3 * (size_t)e];
+  ExpertDesc d{};
+  if (gate == 0 && up == 0 && down == 0) {
+    if (cur[0]) {
+      for (int i = 0; i < 3; i++) ctx->tensors[cur[i] - 1].table_refs--;
+      ctx->table_count--;
+      if (ctx->table_count == 0) ctx->table_D = ctx->table_I = 0;
+    }
+    for (int i = 0; i < 3; i++) cur[i] = 0;
+  } else {
+    if (!valid_handle(ctx, gate) || !valid_handle(ctx, up) || !valid_handle(ctx, down))
+      return fail(ctx, COLI_E_INVAL, "table_set: unknown handle");
+    const HostTensor &g = ctx->tensors[gate - 1], &u = ctx->tensors[up - 1], &dn = ctx->tensors[down - 1];
+    int I = g.O, D = g.I;
+    if (u.O != I || u.I != D || dn.O != D || dn.I != I)
+      return fail(ctx, COLI_E_FORMAT, "table_set: need gate [I x D], up [I x D], down [D x I]");
+    bool replacing = cur[0] != 0;
+    if (ctx->table_count - (replacing ? 1 : 0) > 0 && (ctx->table_D != D || ctx->table_I != I))
+      return fail(ctx, COLI_E_FORMAT, "table_set: every expert must share D and I");
+    if (replacing)
+      for (int i = 0; i < 3; i++) ctx->tensors[cur[i] - 1].table_refs--;
+    else
+      ctx->table_count++;
+    ctx->table_D = D;
+    ctx->table_I = I;
+    cur[0] = gate;
+    cur[1] = up;
+    cur[2] = down;
+    for (int i = 0; i < 3; i++) ctx->tensors[cur[i] - 1].table_refs++;
+    d.t[T_GATE] = make_desc(g);
+    d.t[T_UP] = make_desc(u);
+    d.t[T_DOWN] = make_desc(dn);
+    d.valid = 1;
+  }
+  ctx->h_table[e] = d;
+  cudaError_t ce = cudaMemcpyAsync(ctx->d_table + e, &ctx->h_table[e], sizeof(ExpertDesc),
+                                   cudaMemcpyHostToDevice, ctx->stream);
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(ctx->stream);
+  if (ce != cudaSuccess) return cuda_fail(ctx, ce, "table_set: copy descriptor");
+  return COLI_OK;
+}
+
+int coli_router_select(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr,
+                       const float* bias, int E, int K, float topp, int norm_topk, float routed_scale,
+                       int32_t* idx, float* w, int32_t* n_sel) {
+  if (!ctx) return COLI_E_INVAL;
+  if (!x || !Wr || !idx || !w) return fail(ctx, COLI_E_INVAL, "router: NULL pointer");
+  if (x_dtype != COLI_DTYPE_F32 && x_dtype != COLI_DTYPE_BF16) return fail(ctx, COLI_E_INVAL, "router: dtype");
+  if (S < 1 || S > COLI_MAX_TOKENS || D < 1 || D > COLI_MAX_DIM || E < 1 || E > COLI_MAX_EXPERTS || K < 1 ||
+      K > COLI_MAX_K || K > E)
+    return fail(ctx, COLI_E_INVAL, "router: size out of range");
+  if (injected(ctx)) return COLI_E_INJECTED;
+  cudaSetDevice(ctx->device);
+  int rc = launch_router(ctx, x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk, routed_scale, idx, w, n_sel);
+  if (rc == COLI_OK) ctx->compute_calls++;
+  return rc;
+}
+
+int coli_expert_group(coli_ctx* ctx, const void* x_rows, int x_dtype, int S, const int32_t* idx,
+                      const float* w, const int32_t* n_sel, int K, const void* resid, void* y) {
+  if (!ctx) return COLI_E_INVAL;
+  if (!x_rows || !idx || !w || !y) return fail(ctx, COLI_E_INVAL, "expert_group: NULL pointer");
+  if (x_dtype != COLI_DTYPE_F32 && x_dtype != COLI_DTYPE_BF16)
+    return fail(ctx, COLI_E_INVAL, "expert_group: dtype");
+  if (S < 1 || S > COLI_MAX_TOKENS || K < 1 || K > COLI_MAX_K)
+    return fail(ctx, COLI_E_INVAL, "expert_group: size out of range");
+  if (ctx->table_count == 0) return fail(ctx, COLI_E_INVAL, "expert_group: expert table is empty");
+  if (injected(ctx)) return COLI_E_INJECTED;
+  cudaSetDevice(ctx->device);
+  int rc = launch_expert_group(ctx, x_rows, x_dtype, S, idx, w, n_sel, K, resid, y);
+  if (rc == COLI_OK) ctx->compute_calls++;
+  return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,149 @@
+// Internal declarations shared by the translation units of libcoli_moe.so (not installed).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "coli_moe.h"
+
+namespace coli {
+
+// ---------------------------------------------------------------------------------------------
+// Device-side tensor and expert descriptors
+// ---------------------------------------------------------------------------------------------
+
+// One uploaded int4 tensor as the kernels see it. Rows are padded to a whole number of 16-byte
+// chunks (32 columns each); padding nibbles hold 8, i.e. the value 0.
+struct TensorDesc {
+  const uint8_t* w;    // rows x pitch bytes
+  const float* s;      // scales: rows (gs == 0) or rows * G (gs > 0)
+  uint32_t pitch;      // bytes per row, multiple of 16
+  int32_t gs;          // 0 or even
+  int32_t G;           // groups per row (1 when gs == 0)
+  int32_t rows, cols;
+  int32_t mode;        // SCALE_ROW, SCALE_CHUNK (gs % 32 == 0) or SCALE_GENERIC
+};
+
+enum { SCALE_ROW = 0, SCALE_CHUNK = 1, SCALE_GENERIC = 2 };
+enum { T_GATE = 0, T_UP = 1, T_DOWN = 2 };
+
+struct ExpertDesc {
+  TensorDesc t[3];
+  int32_t valid;
+  int32_t pad_[3];
+};
+
+// ---------------------------------------------------------------------------------------------
+// Host-side context
+// ---------------------------------------------------------------------------------------------
+
+struct HostTensor {
+  uint8_t* w = nullptr;
+  float* s = nullptr;
+  int O = 0, I = 0, gs = 0, G = 1;
+  uint32_t pitch = 0;
+  int table_refs = 0;
+  bool live = false;
+};
+
+struct Workspace {
+  char* base = nullptr;
+  size_t bytes = 0;
+};
+
+}  // namespace coli
+
+struct coli_ctx {
+  int device = 0;
+  cudaStream_t stream = nullptr;
+  int num_sms = 0;
+  std::string last_error;
+  int last_code = 0;
+  std::vector<coli::HostTensor> tensors;  // handle = index + 1
+  // expert table
+  coli::ExpertDesc* d_table = nullptr;       // COLI_MAX_EXPERTS entries
+  std::vector<coli::ExpertDesc> h_table;
+  std::vector<uint64_t> table_handles;       // 3 per entry
+  int table_D = 0, table_I = 0, table_count = 0;
+  // device status words: [0] error code, [1] router completion counter
+  int* d_status = nullptr;
+  coli::Workspace ws;
+  // COLI_FAIL_AFTER test hook
+  long long fail_after = -1;
+  long long compute_calls = 0;
+  // per-kernel event profiling (coli_profile_enable)
+  bool prof = false;
+  struct ProfRec {
+    int kind;
+    cudaEvent_t a, b;
+  };
+  std::vector<ProfRec> prof_pending;
+  std::vector<cudaEvent_t> prof_free;
+  double prof_ms[4] = {0, 0, 0, 0};
+  long long prof_n[4] = {0, 0, 0, 0};
+};
+
+namespace coli {
+
+int fail(coli_ctx* ctx, int code, const std::string& msg);
+int cuda_fail(coli_ctx* ctx, cudaError_t e, const char* what);
+bool injected(coli_ctx* ctx);  // COLI_FAIL_AFTER: true if this compute call must fail
+int ensure_workspace(coli_ctx* ctx, size_t bytes);
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Brackets one kernel launch with profiling events when profiling is on.
+struct ProfScope {
+  coli_ctx* ctx;
+  int kind;
+  cudaEvent_t a = nullptr, b = nullptr;
+  ProfScope(coli_ctx* c, int k);
+  ~ProfScope();
+};
+
+// Launchers (defined in router.cu / experts.cu). Arguments already validated.
+int launch_router(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr,
+                  const float* bias, int E, int K, float topp, int norm_topk, float routed_scale,
+                  int32_t* idx, float* w, int32_t* n_sel);
+int launch_expert_group(coli_ctx* ctx, const void* x, int x_dtype, int S, const int32_t* idx,
+                        const float* w, const int32_t* n_sel, int K, const void* resid, void* y);
+
+}  // namespace coli
+
+// ---------------------------------------------------------------------------------------------
+// Small device helpers
+// ---------------------------------------------------------------------------------------------
+#ifdef __CUDACC__
+namespace coli {
+
+__device__ __forceinline__ void set_error(int* err, int code) { atomicCAS(err, 0, code); }
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return 0x7fc0;  // NaN
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+__device__ __forceinline__ float load_act(const void* p, int dtype, size_t i) {
+  return dtype == COLI_DTYPE_F32 ? __ldg(reinterpret_cast<const float*>(p) + i)
+                                 : bf16_to_f32(__ldg(reinterpret_cast<const unsigned short*>(p) + i));
+}
+
+// Streaming 16-byte load of packed weights: read-only, no L1 allocation, 256-byte L2 sector
+// prefetch (weights are read once per call).
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+}  // namespace coli
+#endif

@@ -1,0 +1,197 @@
+// Device router: f32 logits GEMV + sigmoid + bias (every CTA), then bias-augmented top-K
+// selection, raw-score weights, top-p, norm_topk and routed_scale (the CTA that finishes last).
+//
+// c/backend_cuda.cu commit history, commit "First increment of the #431 plan": an E x D f32
+// logits GEMV + sigmoid, then a selection step that does bias-augmented top-K by choice with a
+// strict '>' tie-break, weights from the raw score, route-level TOPP truncation, norm_topk and
+// routed_scale. For S > 1 the logits of all tokens come from one launch (the batched router of
+// the "GPU resident pipeline" commit).
+#include "coli_internal.h"
+
+namespace coli {
+
+constexpr int kRouterThreads = 256;
+constexpr int kRowsPerCta = 2;
+
+// One warp selects for one token. Lane l owns experts e = l + 32 * i (i < EPL), so each lane's
+// own scan runs in increasing e and a strict '>' keeps the first (lowest) index of a tie; the
+// cross-lane arg-max breaks equal scores by the lower index as well.
+template <int EPL>
+__device__ void select_token(const float* __restrict__ c_row, const float* __restrict__ s_row, int E,
+                             int K, float topp, int norm_topk, float routed_scale,
+                             int32_t* __restrict__ idx_out, float* __restrict__ w_out,
+                             int32_t* __restrict__ nsel_out, int* err) {
+  const int lane = threadIdx.x & 31;
+  float cv[EPL];
+  unsigned taken = 0;  // bit i: expert lane + 32 i already chosen (or absent)
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < EPL; i++) {
+    int e = lane + 32 * i;
+    if (e < E) {
+      cv[i] = __ldcg(c_row + e);
+      if (!isfinite(cv[i])) bad = true;
+    } else {
+      cv[i] = 0.f;
+      taken |= 1u << i;
+    }
+  }
+  if (__any_sync(0xffffffffu, bad)) {
+    if (lane == 0) set_error(err, COLI_E_NONFINITE);
+  }
+  int chosen[COLI_MAX_K];
+  for (int k = 0; k < K; k++) {
+    float best = 0.f;
+    int besti = -1;
+#pragma unroll
+    for (int i = 0; i < EPL; i++) {
+      if (!(taken & (1u << i)) && (besti < 0 || cv[i] > best)) {
+        best = cv[i];
+        besti = lane + 32 * i;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      float ob = __shfl_xor_sync(0xffffffffu, best, off);
+      int oi = __shfl_xor_sync(0xffffffffu, besti, off);
+      bool take = oi >= 0 && (besti < 0 || ob > best || (ob == best && oi < besti));
+      if (take) {
+        best = ob;
+        besti = oi;
+      }
+    }
+    if (besti >= 0 && (besti & 31) == lane) taken |= 1u << (besti >> 5);
+    chosen[k] = besti;
+  }
+  if (lane != 0) return;
+  // weights from the raw (bias-free) score; slot-order binary32 sums, no contraction
+  float wv[COLI_MAX_K];
+  for (int k = 0; k < K; k++) wv[k] = __ldcg(s_row + chosen[k]);
+  int m = K;
+  if (topp > 0.f && topp < 1.f) {
+    float total = 0.f;
+    for (int k = 0; k < K; k++) total = __fadd_rn(total, wv[k]);
+    float cum = 0.f;
+    for (int k = 0; k < K; k++) {
+      cum = __fadd_rn(cum, __fdiv_rn(wv[k], total));
+      if (cum >= topp) {
+        m = k + 1;
+        break;
+      }
+    }
+  }
+  if (norm_topk) {
+    float denom = 0.f;
+    for (int k = 0; k < m; k++) denom = __fadd_rn(denom, wv[k]);
+    for (int k = 0; k < m; k++) wv[k] = __fdiv_rn(wv[k], denom);
+  }
+  for (int k = 0; k < K; k++) {
+    idx_out[k] = k < m ? chosen[k] : -1;
+    w_out[k] = k < m ? __fmul_rn(wv[k], routed_scale) : 0.f;
+  }
+  if (nsel_out) *nsel_out = m;
+}
+
+template <int EPL>
+__device__ void select_all(const float* s, const float* c, int S, int E, int K, float topp, int norm_topk,
+                           float routed_scale, int32_t* idx, float* w, int32_t* n_sel, int* err) {
+  const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  for (int t = warp; t < S; t += nwarps)
+    select_token<EPL>(c + (size_t)t * E, s + (size_t)t * E, E, K, topp, norm_topk, routed_scale,
+                      idx + (size_t)t * K, w + (size_t)t * K, n_sel ? n_sel + t : nullptr, err);
+}
+
+template <bool VEC4>
+__global__ void __launch_bounds__(kRouterThreads) router_kernel(
+    const void* __restrict__ x, int x_dtype, int S, int D, const float* __restrict__ Wr,
+    const float* __restrict__ bias, int E, int K, float topp, int norm_topk, float routed_scale,
+    float* __restrict__ s_ws, float* __restrict__ c_ws, int32_t* __restrict__ idx, float* __restrict__ w,
+    int32_t* __restrict__ n_sel, int* __restrict__ status, int epl) {
+  __shared__ float red[kRouterThreads / 32];
+  __shared__ int am_last;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int e0 = blockIdx.x * kRowsPerCta;
+  for (int t = 0; t < S; t++) {
+    for (int r = 0; r < kRowsPerCta; r++) {
+      const int e = e0 + r;
+      if (e >= E) break;  // uniform across the CTA
+      const float* wrow = Wr + (size_t)e * D;
+      float acc = 0.f;
+      if (VEC4 && x_dtype == COLI_DTYPE_F32) {
+        const float4* w4 = reinterpret_cast<const float4*>(wrow);
+        const float4* x4 = reinterpret_cast<const float4*>(static_cast<const float*>(x) + (size_t)t * D);
+        for (int j = tid; j < D / 4; j += kRouterThreads) {
+          float4 a = __ldg(w4 + j), b = __ldg(x4 + j);
+          acc = fmaf(a.x, b.x, acc);
+          acc = fmaf(a.y, b.y, acc);
+          acc = fmaf(a.z, b.z, acc);
+          acc = fmaf(a.w, b.w, acc);
+        }
+      } else {
+        for (int j = tid; j < D; j += kRouterThreads)
+          acc = fmaf(__ldg(wrow + j), load_act(x, x_dtype, (size_t)t * D + j), acc);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (lane == 0) red[warp] = acc;
+      __syncthreads();
+      if (tid == 0) {
+        float z = 0.f;
+        for (int i = 0; i < kRouterThreads / 32; i++) z += red[i];
+        float sc = 1.0f / (1.0f + expf(-z));
+        float ch = bias ? __fadd_rn(sc, __ldg(bias + e)) : sc;
+        s_ws[(size_t)t * E + e] = sc;
+        c_ws[(size_t)t * E + e] = ch;
+      }
+      __syncthreads();
+    }
+  }
+  // The CTA that finishes last runs the selection over every token's complete score row.
+  if (tid == 0) {
+    __threadfence();
+    unsigned prev = atomicAdd(reinterpret_cast<unsigned*>(status + 1), 1u);
+    am_last = prev == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!am_last) return;
+  __threadfence();
+  switch (epl) {
+    case 1: select_all<1>(s_ws, c_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
+    case 2: select_all<2>(s_ws, c_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
+    case 4: select_all<4>(s_ws, c_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
+    case 8: select_all<8>(s_ws, c_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
+    case 16: select_all<16>(s_ws, c_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
+    default: select_all<32>(s_ws, c_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
+  }
+  __syncthreads();
+  if (tid == 0) atomicExch(reinterpret_cast<unsigned*>(status + 1), 0u);
+}
+
+int launch_router(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr, const float* bias,
+                  int E, int K, float topp, int norm_topk, float routed_scale, int32_t* idx, float* w,
+                  int32_t* n_sel) {
+  size_t half = align_up((size_t)S * E * sizeof(float), 256);
+  int rc = ensure_workspace(ctx, 2 * half);
+  if (rc != COLI_OK) return rc;
+  float* s_ws = reinterpret_cast<float*>(ctx->ws.base);
+  float* c_ws = reinterpret_cast<float*>(ctx->ws.base + half);
+  int epl = 1;
+  while (32 * epl < E) epl *= 2;
+  bool vec4 = (D % 4 == 0) && ((reinterpret_cast<uintptr_t>(Wr) & 15) == 0) &&
+              ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
+  int grid = (E + kRowsPerCta - 1) / kRowsPerCta;
+  ProfScope prof(ctx, COLI_KERNEL_ROUTER);
+  if (vec4)
+    router_kernel<true><<<grid, kRouterThreads, 0, ctx->stream>>>(x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk,
+                                                                  routed_scale, s_ws, c_ws, idx, w, n_sel,
+                                                                  ctx->d_status, epl);
+  else
+    router_kernel<false><<<grid, kRouterThreads, 0, ctx->stream>>>(x, x_dtype, S, D, Wr, bias, E, K, topp,
+                                                                   norm_topk, routed_scale, s_ws, c_ws, idx, w,
+                                                                   n_sel, ctx->d_status, epl);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "router launch");
+  return COLI_OK;
+}
+
+}  // namespace coli

@@ -1,0 +1,41 @@
+"""Full-shape decode layers (D=6144, I=2048 or 2000, E=256, K=8) against the oracle on sampled tokens,
+in the launch configuration the benchmark times."""
+import numpy as np
+import pytest
+
+from int4_grouped_expert_router_gb300 import binding as B
+from int4_grouped_expert_router_gb300.workload import CONFIGS, DeviceLayer, router_host_inputs
+from gpu_util import BF16_RTOL, F32_ATOL, F32_RTOL, Ctx, assert_close, check_router, ffn_reference, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    c = Ctx()
+    yield c.ctx
+    c.close()
+
+
+@pytest.mark.parametrize("name,tokens", [("decode", (0, 1, 2)), ("decode_g64", (0, 1)), ("decode_g64_tail", (0,)),
+                                         ("decode_s4_bf16", (0,))])
+def test_full_shape_layer(ctx, name, tokens):
+    cfg = CONFIGS[name]
+    layer = DeviceLayer(ctx, cfg)
+    try:
+        for tok in tokens:
+            x, Wr, bias, resid = router_host_inputs(cfg, tok)
+            out = layer.outputs()
+            layer.step(layer.act_tensor(x), layer.act_tensor(resid), out)
+            assert B.coli_check_error(ctx) == 0
+            idx, w, n, y = (to_np(out[k]) for k in ("idx", "w", "n_sel", "y"))
+            near, werr = check_router(idx, w, n, x, Wr, bias, cfg.K, cfg.topp, cfg.norm_topk, cfg.routed_scale)
+            ref = ffn_reference(cfg, x, idx, w, n, resid)
+            if cfg.x_dtype == "bf16":
+                stats = assert_close(y, ref, BF16_RTOL, BF16_RTOL * 1e-2, name)
+            else:
+                stats = assert_close(y, ref, F32_RTOL, F32_ATOL, name)
+            print(name, tok, "near-ties", near, "distinct", len(set(idx[idx >= 0].tolist())), stats)
+            assert near <= 1
+    finally:
+        layer.free()
