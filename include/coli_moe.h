@@ -51,6 +51,7 @@ extern "C" {
 #define COLI_E_FORMAT -5     /* weight format rejected: odd I, odd or negative gs, shape mismatch */
 #define COLI_E_NONFINITE -6  /* (device) non-finite activation or router score */
 #define COLI_E_ROUTE -7      /* (device) expert index outside the table or naming an unset entry */
+#define COLI_E_TIMEOUT -8    /* (device) a bounded wait inside a kernel gave up (never expected) */
 
 #define COLI_DTYPE_F32 0     /* IEEE binary32 */
 #define COLI_DTYPE_BF16 1    /* bfloat16 (upper half of a binary32) */

@@ -130,9 +130,11 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
   return (uint16_t)(u >> 16);
 }
 
+// Activations may be the output of the kernel just before (programmatic dependent launch), so
+// they are read through L2 (ld.global.cg), never through the non-coherent read-only path.
 __device__ __forceinline__ float load_act(const void* p, int dtype, size_t i) {
-  return dtype == COLI_DTYPE_F32 ? __ldg(reinterpret_cast<const float*>(p) + i)
-                                 : bf16_to_f32(__ldg(reinterpret_cast<const unsigned short*>(p) + i));
+  return dtype == COLI_DTYPE_F32 ? __ldcg(reinterpret_cast<const float*>(p) + i)
+                                 : bf16_to_f32(__ldcg(reinterpret_cast<const unsigned short*>(p) + i));
 }
 
 // Streaming 16-byte load of packed weights: read-only, no L1 allocation, 256-byte L2 sector

@@ -19,6 +19,7 @@
 // plus the activation quantisation (below 2^-30 of the chunk's largest activation, per column).
 // Chunk results are summed across the warp by a butterfly and across warps in a fixed order.
 #include "coli_internal.h"
+#include "pipe.h"
 
 namespace coli {
 
@@ -190,7 +191,7 @@ __device__ int build_plan(const int32_t* __restrict__ n_sel, int S, int K, int* 
     const int t = base + tid;
     int v = 0;
     if (t < S) {
-      v = n_sel ? __ldg(n_sel + t) : K;
+      v = n_sel ? ld_cg_i32(n_sel + t) : K;
       v = v < 0 ? 0 : (v > K ? K : v);
     }
     int incl = v;
@@ -242,191 +243,375 @@ struct GroupParams {
 };
 
 // ------------------------------------------------------------------------------------------
-// Gate + up dual GEMV with SiLU(g) * u epilogue. Thread c of the CTA owns column chunk c.
-// Work = kept routes x I row pairs, split into equal contiguous ranges over the grid.
+// Batches of the gate/up work: kept routes x I row pairs, split into equal contiguous ranges over
+// the grid; a batch is up to RB consecutive row pairs of one route. Producer and consumers walk
+// the same sequence.
 // ------------------------------------------------------------------------------------------
 
-constexpr int kGU = 4;  // row pairs per batch (8 weight rows in flight per thread)
+struct RouteInfo {
+  int j = -1, t = -1, k = 0, e = -1;
+  bool ok = false;
+};
 
-template <int MAXT>
-__global__ void __launch_bounds__(MAXT) gateup_kernel(GroupParams P) {
-  extern __shared__ int smem_plan[];        // S + 1
+__device__ __forceinline__ void resolve_route(const GroupParams& P, const int* pre, int j, RouteInfo& r) {
+  r.j = j;
+  r.t = route_token(pre, P.S, j);
+  r.k = j - pre[r.t];
+  r.e = ld_cg_i32(P.idx + (size_t)r.t * P.K + r.k);
+  r.ok = r.e >= 0 && r.e < COLI_MAX_EXPERTS && P.table[r.e].valid;
+}
+
+// ------------------------------------------------------------------------------------------
+// Gate + up dual GEMV with the SiLU(g) * u epilogue (warp-specialised, TMA-fed).
+// Warps 0..W-1 are consumers: thread c owns column chunk c of every row and keeps that chunk of
+// the activation in registers. Warp W is the producer: one lane streams each batch's gate and up
+// rows (contiguous in memory) into a ring of NST shared-memory stages with bulk copies.
+// ------------------------------------------------------------------------------------------
+
+constexpr int kMaxStages = 8;
+
+template <int RB>
+struct GateUpSmem {
+  static constexpr int kRows = 2 * RB;
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  float red[2][32][kRows];
+  int abort_flag;
+};
+
+template <int RB, int MAXT>
+__global__ void __launch_bounds__(MAXT) gateup_kernel(GroupParams P, uint32_t pitch, uint32_t NST) {
+  using SM = GateUpSmem<RB>;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  const uint32_t stage_bytes = 2u * RB * pitch;
+  uint8_t* stages = smem_raw;
+  SM& sm = *reinterpret_cast<SM*>(smem_raw + (size_t)NST * stage_bytes);
+  int* pre = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(&sm) + sizeof(SM));
   __shared__ int scratch32[32];
-  __shared__ float red[2][32][2 * kGU];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-  const int C = (P.D + 31) >> 5;
-  const int c = tid;
-  const bool has_chunk = c < C;
-  const int R = build_plan(P.n_sel, P.S, P.K, smem_plan, scratch32);
-  if (blockIdx.x == 0)
-    for (int t = tid; t <= P.S; t += blockDim.x) P.plan[t] = smem_plan[t];
-  const long long T = (long long)R * P.I;
-  long long p = (long long)blockIdx.x * T / gridDim.x;
-  const long long pend = (long long)(blockIdx.x + 1) * T / gridDim.x;
 
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int C = (P.D + 31) >> 5;
+  const int W = (C + 31) >> 5;            // consumer warps
+  const bool producer = warp == W;
+  const int c = tid;
+  const bool has_chunk = !producer && c < C;
+
+  if (tid == 0) {
+    for (int s = 0; s < NST; s++) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], W);
+    }
+    sm.abort_flag = 0;
+    mbar_fence_init();
+  }
+  // prologue overlapping the router's tail: activation limbs of token 0
   Limbs L;
   float xv[32];
-  int cur_tok = -1, cur_route = -1;
-  bool route_ok = false;
+  int cur_tok = 0;
+  load_chunk_f32(P.x, P.x_dtype, 0, 32 * c, has_chunk ? P.D : 0, xv);
+  bool finite = make_limbs(xv, L);
+  griddep_wait();
+  const int R = build_plan(P.n_sel, P.S, P.K, pre, scratch32);  // contains __syncthreads
+  if (blockIdx.x == 0)
+    for (int t = tid; t <= P.S; t += blockDim.x) P.plan[t] = pre[t];
+  griddep_launch_dependents();
+  if (!finite && has_chunk) set_error(P.err, COLI_E_NONFINITE);
+
+  const long long T = (long long)R * P.I;
+  const long long pbeg = (long long)blockIdx.x * T / gridDim.x;
+  const long long pend = (long long)(blockIdx.x + 1) * T / gridDim.x;
+
+  if (producer) {
+    if (lane == 0) {
+      const uint64_t policy = l2_evict_first_policy();
+      RouteInfo r;
+      const uint8_t *wg = nullptr, *wu = nullptr;
+      uint32_t b = 0;
+      bool aborted = false;
+      for (long long p = pbeg; p < pend && !aborted;) {
+        const int j = (int)(p / P.I), i0 = (int)(p - (long long)j * P.I);
+        const int nb = (int)min((long long)min(RB, P.I - i0), pend - p);
+        p += nb;
+        if (j != r.j) {
+          resolve_route(P, pre, j, r);
+          if (r.ok) {
+            wg = P.table[r.e].t[T_GATE].w;
+            wu = P.table[r.e].t[T_UP].w;
+          }
+        }
+        if (!r.ok) continue;
+        const uint32_t slot = b % NST;
+        if (b >= NST) {
+          const uint32_t par = ((b / NST) - 1) & 1;
+          uint32_t spins = 0;
+          while (!mbar_test_parity(&sm.empty[slot], par)) {
+            if (++spins > kSpinLimit || *(volatile int*)&sm.abort_flag) {
+              aborted = true;
+              break;
+            }
+          }
+          if (aborted) break;
+        }
+        uint8_t* st = stages + (size_t)slot * stage_bytes;
+        mbar_arrive_expect_tx(&sm.full[slot], 2u * nb * pitch);
+        bulk_g2s_stream(st, wg + (size_t)i0 * pitch, nb * pitch, &sm.full[slot], policy);
+        bulk_g2s_stream(st + (size_t)RB * pitch, wu + (size_t)i0 * pitch, nb * pitch, &sm.full[slot], policy);
+        b++;
+      }
+      if (aborted) set_error(P.err, COLI_E_TIMEOUT);
+      // never leave the CTA with bulk copies in flight: wait for the last fill of every slot
+      for (uint32_t q = b > NST ? b - NST : 0; q < b; q++) (void)mbar_wait(&sm.full[q % NST], (q / NST) & 1);
+    }
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  RouteInfo r;
   TensorDesc Tg, Tu;
+  uint32_t b = 0;
   int buf = 0;
-  while (p < pend) {
-    const int j = (int)(p / P.I);
-    const int i0 = (int)(p - (long long)j * P.I);
-    int nb = kGU;
-    if (nb > P.I - i0) nb = P.I - i0;
-    if (nb > pend - p) nb = (int)(pend - p);
-    if (j != cur_route) {
-      cur_route = j;
-      const int t = route_token(smem_plan, P.S, j);
-      const int k = j - smem_plan[t];
-      const int e = __ldg(P.idx + (size_t)t * P.K + k);
-      route_ok = e >= 0 && e < COLI_MAX_EXPERTS && P.table[e].valid;
-      if (!route_ok) {
-        if (tid == 0) set_error(P.err, COLI_E_ROUTE);
-      } else {
-        Tg = load_desc(&P.table[e].t[T_GATE]);
-        Tu = load_desc(&P.table[e].t[T_UP]);
-      }
-      if (t != cur_tok) {
-        cur_tok = t;
-        load_chunk_f32(P.x, P.x_dtype, (size_t)t * P.D, 32 * c, has_chunk ? P.D : 0, xv);
-        if (!make_limbs(xv, L)) set_error(P.err, COLI_E_NONFINITE);
+  for (long long p = pbeg; p < pend;) {
+    const int j = (int)(p / P.I), i0 = (int)(p - (long long)j * P.I);
+    const int nb = (int)min((long long)min(RB, P.I - i0), pend - p);
+    p += nb;
+    if (j != r.j) {
+      resolve_route(P, pre, j, r);
+      if (r.ok) {
+        Tg = load_desc(&P.table[r.e].t[T_GATE]);
+        Tu = load_desc(&P.table[r.e].t[T_UP]);
+        if (r.t != cur_tok) {
+          cur_tok = r.t;
+          load_chunk_f32(P.x, P.x_dtype, (size_t)cur_tok * P.D, 32 * c, has_chunk ? P.D : 0, xv);
+          if (!make_limbs(xv, L) && has_chunk) set_error(P.err, COLI_E_NONFINITE);
+        }
+      } else if (tid == 0) {
+        set_error(P.err, COLI_E_ROUTE);
       }
     }
-    float part[2 * kGU];
-    if (route_ok && has_chunk) {
-      uint4 wv[2 * kGU];
+    if (!r.ok) continue;
+    // scales needed after the wait, fetched before it
+    float scg[RB], scu[RB];
 #pragma unroll
-      for (int u = 0; u < kGU; u++) {
-        if (u < nb) {
-          wv[u] = ldg_stream(Tg.w + (size_t)(i0 + u) * Tg.pitch + 16 * c);
-          wv[kGU + u] = ldg_stream(Tu.w + (size_t)(i0 + u) * Tu.pitch + 16 * c);
-        } else {
-          wv[u] = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
-          wv[kGU + u] = wv[u];
-        }
+    for (int u = 0; u < RB; u++) {
+      scg[u] = 1.f;
+      scu[u] = 1.f;
+      if (u < nb && has_chunk) {
+        if (Tg.mode == SCALE_CHUNK) scg[u] = __ldg(Tg.s + (size_t)(i0 + u) * Tg.G + (32 * c) / Tg.gs);
+        if (Tu.mode == SCALE_CHUNK) scu[u] = __ldg(Tu.s + (size_t)(i0 + u) * Tu.G + (32 * c) / Tu.gs);
       }
-#pragma unroll
-      for (int u = 0; u < 2 * kGU; u++) {
-        const TensorDesc& T = u < kGU ? Tg : Tu;
-        const int row = i0 + (u % kGU);
-        float d;
-        if (T.mode == SCALE_GENERIC) {
-          d = (u % kGU) < nb ? chunk_dot_generic(wv[u], P.x, P.x_dtype, (size_t)cur_tok * P.D, T, row, c) : 0.f;
-        } else {
-          d = chunk_dot(wv[u], L);
-          if (T.mode == SCALE_CHUNK && (u % kGU) < nb) d *= __ldg(T.s + (size_t)row * T.G + (32 * c) / T.gs);
-        }
-        part[u] = d;
-      }
-    } else {
-#pragma unroll
-      for (int u = 0; u < 2 * kGU; u++) part[u] = 0.f;
     }
-    warp_transpose_reduce<2 * kGU>(part, lane);
-    if ((lane & (32 / (2 * kGU) - 1)) == 0) red[buf][warp][lane / (32 / (2 * kGU))] = part[0];
-    __syncthreads();
-    if (tid < nb && route_ok) {
-      float g = 0.f, uu = 0.f;
-      for (int wi = 0; wi < nwarps; wi++) {
-        g += red[buf][wi][tid];
-        uu += red[buf][wi][kGU + tid];
+    float fg = 1.f, fu = 1.f;
+    if (tid < nb) {
+      if (Tg.mode == SCALE_ROW) fg = __ldg(Tg.s + i0 + tid);
+      if (Tu.mode == SCALE_ROW) fu = __ldg(Tu.s + i0 + tid);
+    }
+    const uint32_t slot = b % NST;
+    const bool ok = mbar_wait(&sm.full[slot], (b / NST) & 1);
+    const uint8_t* st = stages + (size_t)slot * stage_bytes;
+    float part[2 * RB];
+#pragma unroll
+    for (int u = 0; u < 2 * RB; u++) {
+      const int uu = u % RB;
+      const TensorDesc& T = u < RB ? Tg : Tu;
+      float d = 0.f;
+      if (ok && has_chunk && uu < nb) {
+        const uint4 wv = lds128(st + (size_t)(u < RB ? 0 : RB) * pitch + (size_t)uu * pitch + 16 * c);
+        if (T.mode == SCALE_GENERIC)
+          d = chunk_dot_generic(wv, P.x, P.x_dtype, (size_t)cur_tok * P.D, T, i0 + uu, c);
+        else
+          d = chunk_dot(wv, L) * (u < RB ? scg[uu] : scu[uu]);
       }
-      const int i = i0 + tid;
-      if (Tg.mode == SCALE_ROW) g *= __ldg(Tg.s + i);
-      if (Tu.mode == SCALE_ROW) uu *= __ldg(Tu.s + i);
-      P.h[(size_t)j * P.I + i] = silu_mul(g, uu);
+      part[u] = d;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[slot]);
+    warp_transpose_reduce<2 * RB>(part, lane);
+    if ((lane & (32 / (2 * RB) - 1)) == 0) sm.red[buf][warp][lane / (32 / (2 * RB))] = part[0];
+    if (named_sync_or(1, W * 32, !ok)) {  // uniform decision across the consumer warps
+      if (tid == 0) {
+        set_error(P.err, COLI_E_TIMEOUT);
+        *(volatile int*)&sm.abort_flag = 1;
+      }
+      break;
+    }
+    if (tid < nb) {
+      float g = 0.f, u = 0.f;
+      for (int wi = 0; wi < W; wi++) {
+        g += sm.red[buf][wi][tid];
+        u += sm.red[buf][wi][RB + tid];
+      }
+      P.h[(size_t)j * P.I + i0 + tid] = silu_mul(g * fg, u * fu);
     }
     buf ^= 1;
-    p += nb;
+    b++;
   }
 }
 
 // ------------------------------------------------------------------------------------------
-// S == 1: down GEMV of every kept slot, weighting and the slot-ordered reduce in one kernel.
-// Threads (k, c): slot k = tid / TPE owns column chunk c = tid % TPE of its expert's down rows.
+// S == 1: down GEMV of every kept slot, weighting and the slot-ordered reduce in one kernel
+// (warp-specialised, TMA-fed). Consumer threads (k, c): slot k = tid / TPE owns column chunk
+// c = tid % TPE of its expert's down rows, with that chunk of h_k in registers. The producer warp
+// streams, per batch of RB output rows, the RB rows of every kept expert (one bulk copy each).
+// The weight stream does not depend on the gate/up kernel, so it starts before that kernel ends.
 // ------------------------------------------------------------------------------------------
 
-constexpr int kDU = 4;  // down rows per batch
+template <int RB>
+struct DownSmem {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  float red[2][32][RB];
+  float rscale[2][COLI_MAX_K][RB];
+  float wk[COLI_MAX_K];
+  int ok[COLI_MAX_K];
+  int mode_row[COLI_MAX_K];
+  int abort_flag;
+};
 
-template <int MAXT>
-__global__ void __launch_bounds__(MAXT) down_fused_kernel(GroupParams P, int TPE) {
-  __shared__ float red[2][32][kDU];
-  __shared__ float wk_s[COLI_MAX_K];
-  __shared__ const float* srow_s[COLI_MAX_K];   // per-row scales of slot k (ROW mode) or null
-  __shared__ int ok_s[COLI_MAX_K];
+template <int RB, int MAXT>
+__global__ void __launch_bounds__(MAXT) down_fused_kernel(GroupParams P, int TPE, uint32_t pitch, uint32_t NST) {
+  using SM = DownSmem<RB>;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  const uint32_t slot_bytes = (uint32_t)P.K * RB * pitch;  // per stage: K experts x RB rows
+  uint8_t* stages = smem_raw;
+  SM& sm = *reinterpret_cast<SM*>(smem_raw + (size_t)NST * slot_bytes);
+
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int NC = P.K * TPE;               // consumer threads
+  const int WC = NC >> 5;
+  const bool producer = tid >= NC;
   const int k = tid / TPE, c = tid % TPE;
   const int CI = (P.I + 31) >> 5;
-  int m = P.n_sel ? __ldg(P.n_sel) : P.K;
+  const int wpe = TPE >> 5;
+
+  // routes of token 0 (written by the router, complete before the gate/up kernel started)
+  int m = P.n_sel ? ld_cg_i32(P.n_sel) : P.K;
   m = m < 0 ? 0 : (m > P.K ? P.K : m);
-  const int wpe = TPE >> 5;  // warps per slot
-  bool active = k < m && c < CI;
-  TensorDesc Td;
-  int e = -1;
-  if (k < m) {
-    e = __ldg(P.idx + k);
-    if (e < 0 || e >= COLI_MAX_EXPERTS || !P.table[e].valid) {
-      e = -1;
-      active = false;
-    } else {
-      Td = load_desc(&P.table[e].t[T_DOWN]);
+  if (tid == 0) {
+    for (int s = 0; s < NST; s++) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], WC);
     }
+    sm.abort_flag = 0;
+    mbar_fence_init();
   }
-  if (c == 0 && k < P.K) {
-    ok_s[k] = (k < m && e >= 0);
-    wk_s[k] = k < m ? __ldg(P.w + k) : 0.f;
-    srow_s[k] = (e >= 0 && Td.mode == SCALE_ROW) ? Td.s : nullptr;
-    if (k < m && e < 0) set_error(P.err, COLI_E_ROUTE);
+  if (!producer && c == 0) {
+    int e = k < m ? ld_cg_i32(P.idx + k) : -1;
+    bool ok = k < m && e >= 0 && e < COLI_MAX_EXPERTS && P.table[e].valid;
+    if (k < m && !ok) set_error(P.err, COLI_E_ROUTE);
+    sm.ok[k] = ok;
+    sm.wk[k] = ok ? ld_cg_f32(P.w + k) : 0.f;
+    sm.mode_row[k] = ok ? (P.table[e].t[T_DOWN].mode == SCALE_ROW) : 0;
   }
+  __syncthreads();
+  const int d_begin = (int)((long long)blockIdx.x * P.D / gridDim.x);
+  const int d_end = (int)((long long)(blockIdx.x + 1) * P.D / gridDim.x);
+
+  if (producer) {
+    if (lane == 0) {
+      const uint64_t policy = l2_evict_first_policy();
+      const uint8_t* wsrc[COLI_MAX_K];
+      for (int kk = 0; kk < m; kk++) wsrc[kk] = sm.ok[kk] ? P.table[ld_cg_i32(P.idx + kk)].t[T_DOWN].w : nullptr;
+      uint32_t b = 0;
+      bool aborted = false;
+      for (int d0 = d_begin; d0 < d_end; d0 += RB, b++) {
+        const int nb = min(RB, d_end - d0);
+        const uint32_t slot = b % NST;
+        if (b >= NST) {
+          const uint32_t par = ((b / NST) - 1) & 1;
+          uint32_t spins = 0;
+          while (!mbar_test_parity(&sm.empty[slot], par)) {
+            if (++spins > kSpinLimit || *(volatile int*)&sm.abort_flag) {
+              aborted = true;
+              break;
+            }
+          }
+          if (aborted) break;
+        }
+        uint32_t bytes = 0;
+        for (int kk = 0; kk < m; kk++)
+          if (wsrc[kk]) bytes += nb * pitch;
+        uint8_t* st = stages + (size_t)slot * slot_bytes;
+        mbar_arrive_expect_tx(&sm.full[slot], bytes);
+        for (int kk = 0; kk < m; kk++)
+          if (wsrc[kk])
+            bulk_g2s_stream(st + (size_t)kk * RB * pitch, wsrc[kk] + (size_t)d0 * pitch, nb * pitch, &sm.full[slot],
+                            policy);
+      }
+      if (aborted) set_error(P.err, COLI_E_TIMEOUT);
+      for (uint32_t q = b > NST ? b - NST : 0; q < b; q++) (void)mbar_wait(&sm.full[q % NST], (q / NST) & 1);
+    }
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  const bool active = k < m && sm.ok[k] && c < CI;
+  TensorDesc Td;
+  if (active) Td = load_desc(&P.table[ld_cg_i32(P.idx + k)].t[T_DOWN]);
+  griddep_wait();  // h is written by the gate/up kernel
   float hv[32];
   Limbs L;
   load_chunk_f32(P.h, COLI_DTYPE_F32, (size_t)k * P.I, 32 * c, active ? P.I : 0, hv);
-  if (!make_limbs(hv, L)) set_error(P.err, COLI_E_NONFINITE);
-  __syncthreads();
+  if (!make_limbs(hv, L) && active) set_error(P.err, COLI_E_NONFINITE);
 
-  const int d_begin = (int)((long long)blockIdx.x * P.D / gridDim.x);
-  const int d_end = (int)((long long)(blockIdx.x + 1) * P.D / gridDim.x);
+  uint32_t b = 0;
   int buf = 0;
-  for (int d0 = d_begin; d0 < d_end; d0 += kDU) {
-    const int nb = min(kDU, d_end - d0);
-    float part[kDU];
-    if (active) {
-      uint4 wv[kDU];
+  for (int d0 = d_begin; d0 < d_end; d0 += RB, b++) {
+    const int nb = min(RB, d_end - d0);
+    float sc[RB];
+    float rs[RB];
 #pragma unroll
-      for (int u = 0; u < kDU; u++)
-        wv[u] = u < nb ? ldg_stream(Td.w + (size_t)(d0 + u) * Td.pitch + 16 * c)
-                       : make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
-#pragma unroll
-      for (int u = 0; u < kDU; u++) {
-        float d;
-        if (Td.mode == SCALE_GENERIC) {
-          d = u < nb ? chunk_dot_generic(wv[u], P.h, COLI_DTYPE_F32, (size_t)k * P.I, Td, d0 + u, c) : 0.f;
-        } else {
-          d = chunk_dot(wv[u], L);
-          if (Td.mode == SCALE_CHUNK && u < nb) d *= __ldg(Td.s + (size_t)(d0 + u) * Td.G + (32 * c) / Td.gs);
-        }
-        part[u] = d;
+    for (int u = 0; u < RB; u++) {
+      sc[u] = 1.f;
+      rs[u] = 1.f;
+      if (active && u < nb) {
+        if (Td.mode == SCALE_CHUNK) sc[u] = __ldg(Td.s + (size_t)(d0 + u) * Td.G + (32 * c) / Td.gs);
+        if (Td.mode == SCALE_ROW && c == 0) rs[u] = __ldg(Td.s + d0 + u);
       }
-    } else {
-#pragma unroll
-      for (int u = 0; u < kDU; u++) part[u] = 0.f;
     }
-    warp_transpose_reduce<kDU>(part, lane);
-    if ((lane & (32 / kDU - 1)) == 0) red[buf][warp][lane / (32 / kDU)] = part[0];
-    __syncthreads();
+    float res = 0.f;
+    if (tid < nb && P.resid) res = load_act(P.resid, P.x_dtype, d0 + tid);
+    const uint32_t slot = b % NST;
+    const bool ok = mbar_wait(&sm.full[slot], (b / NST) & 1);
+    const uint8_t* st = stages + (size_t)slot * slot_bytes + (size_t)k * RB * pitch;
+    float part[RB];
+#pragma unroll
+    for (int u = 0; u < RB; u++) {
+      float d = 0.f;
+      if (ok && active && u < nb) {
+        const uint4 wv = lds128(st + (size_t)u * pitch + 16 * c);
+        if (Td.mode == SCALE_GENERIC)
+          d = chunk_dot_generic(wv, P.h, COLI_DTYPE_F32, (size_t)k * P.I, Td, d0 + u, c);
+        else
+          d = chunk_dot(wv, L) * sc[u];
+      }
+      part[u] = d;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[slot]);
+    if (c == 0 && k < m) {
+#pragma unroll
+      for (int u = 0; u < RB; u++) sm.rscale[buf][k][u] = rs[u];
+    }
+    warp_transpose_reduce<RB>(part, lane);
+    if ((lane & (32 / RB - 1)) == 0) sm.red[buf][warp][lane / (32 / RB)] = part[0];
+    if (named_sync_or(1, NC, !ok)) {
+      if (tid == 0) {
+        set_error(P.err, COLI_E_TIMEOUT);
+        *(volatile int*)&sm.abort_flag = 1;
+      }
+      break;
+    }
     if (tid < nb) {
       const int d = d0 + tid;
       float acc = 0.f;
       for (int kk = 0; kk < m; kk++) {
-        if (!ok_s[kk]) continue;
+        if (!sm.ok[kk]) continue;
         float yk = 0.f;
-        for (int wi = kk * wpe; wi < (kk + 1) * wpe; wi++) yk += red[buf][wi][tid];
-        if (srow_s[kk]) yk *= __ldg(srow_s[kk] + d);
-        acc = fmaf(wk_s[kk], yk, acc);
+        for (int wi = kk * wpe; wi < (kk + 1) * wpe; wi++) yk += sm.red[buf][wi][tid];
+        if (sm.mode_row[kk]) yk *= sm.rscale[buf][kk][tid];
+        acc = fmaf(sm.wk[kk], yk, acc);
       }
-      if (P.resid) acc = load_act(P.resid, P.x_dtype, d) + acc;
+      if (P.resid) acc = res + acc;
       if (P.x_dtype == COLI_DTYPE_F32)
         static_cast<float*>(P.y)[d] = acc;
       else
@@ -438,6 +623,11 @@ __global__ void __launch_bounds__(MAXT) down_fused_kernel(GroupParams P, int TPE
 
 // ------------------------------------------------------------------------------------------
 // S > 1: down GEMV per kept route into yr, then a slot-ordered combine per token.
+// ------------------------------------------------------------------------------------------
+
+constexpr int kDU = 4;  // rows per batch of the route-parallel down kernel
+
+// ------------------------------------------------------------------------------------------
 // ------------------------------------------------------------------------------------------
 
 template <int MAXT>
@@ -534,6 +724,28 @@ __global__ void combine_kernel(GroupParams P) {
 // ------------------------------------------------------------------------------------------
 
 
+constexpr int kGateUpRows = 2;            // row pairs per gate/up stage
+constexpr int kDownRows = 2;              // output rows per down stage
+constexpr uint32_t kStageBudget = 96 * 1024;  // shared memory for the stage ring of one CTA
+
+// Launch with programmatic stream serialisation (the kernel may start while its predecessor in
+// the stream finishes; it calls griddepcontrol.wait before reading that predecessor's output).
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_k(void (*kern)(KArgs...), int grid, int block, size_t smem, cudaStream_t st, bool pdl,
+                            Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 int launch_expert_group(coli_ctx* ctx, const void* x, int x_dtype, int S, const int32_t* idx, const float* w,
                         const int32_t* n_sel, int K, const void* resid, void* y) {
   if (S > COLI_MAX_GROUP_TOKENS) return fail(ctx, COLI_E_INVAL, "expert_group: S above COLI_MAX_GROUP_TOKENS");
@@ -563,25 +775,41 @@ int launch_expert_group(coli_ctx* ctx, const void* x, int x_dtype, int S, const 
   P.err = ctx->d_status;
 
   const int CD = (D + 31) / 32, CI = (I + 31) / 32;
-  const int nt_gu = (CD + 31) / 32 * 32;
-  const size_t smem_gu = (size_t)(S + 1) * sizeof(int);
+  const uint32_t pitch_d = (uint32_t)CD * 16, pitch_i = (uint32_t)CI * 16;
   cudaError_t e;
   {
-    auto kern = nt_gu <= 256 ? gateup_kernel<256> : (nt_gu <= 512 ? gateup_kernel<512> : gateup_kernel<1024>);
+    constexpr int RB = kGateUpRows;
+    const int nt = ((CD + 31) / 32 + 1) * 32;  // consumer warps + producer warp
+    const uint32_t stage = 2u * RB * pitch_d;
+    uint32_t nst = kStageBudget / stage;
+    nst = nst < 2 ? 2 : (nst > kMaxStages ? kMaxStages : nst);
+    const size_t smem = (size_t)nst * stage + sizeof(GateUpSmem<RB>) + (size_t)(S + 1) * sizeof(int);
+    auto kern = nt <= 256 ? gateup_kernel<RB, 256> : (nt <= 512 ? gateup_kernel<RB, 512> : gateup_kernel<RB, 1024>);
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+      return cuda_fail(ctx, e, "gate/up smem attribute");
     int occ = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, nt_gu, smem_gu);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, nt, smem);
     ProfScope prof(ctx, COLI_KERNEL_GATEUP);
-    kern<<<ctx->num_sms * (occ > 0 ? occ : 1), nt_gu, smem_gu, ctx->stream>>>(P);
-    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(ctx, e, "gate/up launch");
+    e = launch_k(kern, ctx->num_sms * (occ > 0 ? occ : 1), nt, smem, ctx->stream, true, P, pitch_d, nst);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "gate/up launch");
   }
   const int TPE = (CI + 31) / 32 * 32;
-  if (S == 1 && K * TPE <= 1024) {
-    const int nt = K * TPE;
-    auto kern = nt <= 256 ? down_fused_kernel<256> : (nt <= 512 ? down_fused_kernel<512> : down_fused_kernel<1024>);
+  constexpr int RBD = kDownRows;
+  const uint32_t down_stage = (uint32_t)K * RBD * pitch_i;
+  if (S == 1 && K * TPE + 32 <= 1024 && 2 * down_stage <= 2 * kStageBudget) {
+    const int nt = K * TPE + 32;
+    uint32_t nst = kStageBudget / down_stage;
+    nst = nst < 2 ? 2 : (nst > kMaxStages ? kMaxStages : nst);
+    const size_t smem = (size_t)nst * down_stage + sizeof(DownSmem<RBD>);
+    auto kern = nt <= 256 ? down_fused_kernel<RBD, 256>
+                          : (nt <= 544 ? down_fused_kernel<RBD, 544> : down_fused_kernel<RBD, 1024>);
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+      return cuda_fail(ctx, e, "down smem attribute");
     int grid = ctx->num_sms;
     if (grid > D) grid = D;
     ProfScope prof(ctx, COLI_KERNEL_DOWN);
-    kern<<<grid, nt, 0, ctx->stream>>>(P, TPE);
+    e = launch_k(kern, grid, nt, smem, ctx->stream, true, P, TPE, pitch_i, nst);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "down launch");
   } else {
     auto kern = TPE <= 256 ? down_routes_kernel<256> : (TPE <= 512 ? down_routes_kernel<512> : down_routes_kernel<1024>);
     int occ = 0;

@@ -7,11 +7,12 @@
 // routed_scale. For S > 1 the logits of all tokens come from one launch (the batched router of
 // the "GPU resident pipeline" commit).
 #include "coli_internal.h"
+#include "pipe.h"
 
 namespace coli {
 
 constexpr int kRouterThreads = 256;
-constexpr int kRowsPerCta = 2;
+constexpr int kRowsPerCta = 2;  // E = 256 -> 128 CTAs, every row group in flight at once
 
 // One warp selects for one token. Lane l owns experts e = l + 32 * i (i < EPL), so each lane's
 // own scan runs in increasing e and a strict '>' keeps the first (lowest) index of a tie; the
@@ -29,17 +30,15 @@ __device__ void select_token(const float* __restrict__ c_row, const float* __res
   for (int i = 0; i < EPL; i++) {
     int e = lane + 32 * i;
     if (e < E) {
-      cv[i] = __ldcg(c_row + e);
+      cv[i] = ld_cg_f32(c_row + e);
       if (!isfinite(cv[i])) bad = true;
     } else {
       cv[i] = 0.f;
       taken |= 1u << i;
     }
   }
-  if (__any_sync(0xffffffffu, bad)) {
-    if (lane == 0) set_error(err, COLI_E_NONFINITE);
-  }
-  int chosen[COLI_MAX_K];
+  if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(err, COLI_E_NONFINITE);
+  int mine = -1;  // lane k keeps the expert chosen in round k
   for (int k = 0; k < K; k++) {
     float best = 0.f;
     int besti = -1;
@@ -61,19 +60,18 @@ __device__ void select_token(const float* __restrict__ c_row, const float* __res
       }
     }
     if (besti >= 0 && (besti & 31) == lane) taken |= 1u << (besti >> 5);
-    chosen[k] = besti;
+    if (lane == k) mine = besti;
   }
-  if (lane != 0) return;
-  // weights from the raw (bias-free) score; slot-order binary32 sums, no contraction
-  float wv[COLI_MAX_K];
-  for (int k = 0; k < K; k++) wv[k] = __ldcg(s_row + chosen[k]);
+  // weights from the raw (bias-free) score; every sum in slot order in binary32, no contraction
+  const float wmine = (lane < K && mine >= 0) ? ld_cg_f32(s_row + mine) : 0.f;
   int m = K;
+  float denom = 1.f;
+  float total = 0.f;
+  for (int k = 0; k < K; k++) total = __fadd_rn(total, __shfl_sync(0xffffffffu, wmine, k));
   if (topp > 0.f && topp < 1.f) {
-    float total = 0.f;
-    for (int k = 0; k < K; k++) total = __fadd_rn(total, wv[k]);
     float cum = 0.f;
     for (int k = 0; k < K; k++) {
-      cum = __fadd_rn(cum, __fdiv_rn(wv[k], total));
+      cum = __fadd_rn(cum, __fdiv_rn(__shfl_sync(0xffffffffu, wmine, k), total));
       if (cum >= topp) {
         m = k + 1;
         break;
@@ -81,15 +79,16 @@ __device__ void select_token(const float* __restrict__ c_row, const float* __res
     }
   }
   if (norm_topk) {
-    float denom = 0.f;
-    for (int k = 0; k < m; k++) denom = __fadd_rn(denom, wv[k]);
-    for (int k = 0; k < m; k++) wv[k] = __fdiv_rn(wv[k], denom);
+    denom = 0.f;
+    for (int k = 0; k < m; k++) denom = __fadd_rn(denom, __shfl_sync(0xffffffffu, wmine, k));
   }
-  for (int k = 0; k < K; k++) {
-    idx_out[k] = k < m ? chosen[k] : -1;
-    w_out[k] = k < m ? __fmul_rn(wv[k], routed_scale) : 0.f;
+  if (lane < K) {
+    const bool kept = lane < m;
+    float wv = norm_topk ? __fdiv_rn(wmine, denom) : wmine;
+    idx_out[lane] = kept ? mine : -1;
+    w_out[lane] = kept ? __fmul_rn(wv, routed_scale) : 0.f;
   }
-  if (nsel_out) *nsel_out = m;
+  if (lane == 0 && nsel_out) *nsel_out = m;
 }
 
 template <int EPL>
@@ -101,50 +100,68 @@ __device__ void select_all(const float* s, const float* c, int S, int E, int K, 
                       idx + (size_t)t * K, w + (size_t)t * K, n_sel ? n_sel + t : nullptr, err);
 }
 
+// Logits GEMV: CTA b computes rows e = b * kRowsPerCta + r (r < kRowsPerCta) for every token;
+// thread t accumulates columns t, t + kRouterThreads, ... (float4 when aligned) for all rows at
+// once, so all of a row group's loads are in flight together.
 template <bool VEC4>
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(
     const void* __restrict__ x, int x_dtype, int S, int D, const float* __restrict__ Wr,
     const float* __restrict__ bias, int E, int K, float topp, int norm_topk, float routed_scale,
     float* __restrict__ s_ws, float* __restrict__ c_ws, int32_t* __restrict__ idx, float* __restrict__ w,
     int32_t* __restrict__ n_sel, int* __restrict__ status, int epl) {
-  __shared__ float red[kRouterThreads / 32];
+  __shared__ float red[kRouterThreads / 32][kRowsPerCta];
   __shared__ int am_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int e0 = blockIdx.x * kRowsPerCta;
+  const int nrows = min(kRowsPerCta, E - e0);
+  griddep_wait();               // x may be the previous kernel's output
+  griddep_launch_dependents();  // the gate/up kernel may start its prologue
   for (int t = 0; t < S; t++) {
-    for (int r = 0; r < kRowsPerCta; r++) {
-      const int e = e0 + r;
-      if (e >= E) break;  // uniform across the CTA
-      const float* wrow = Wr + (size_t)e * D;
-      float acc = 0.f;
-      if (VEC4 && x_dtype == COLI_DTYPE_F32) {
-        const float4* w4 = reinterpret_cast<const float4*>(wrow);
-        const float4* x4 = reinterpret_cast<const float4*>(static_cast<const float*>(x) + (size_t)t * D);
-        for (int j = tid; j < D / 4; j += kRouterThreads) {
-          float4 a = __ldg(w4 + j), b = __ldg(x4 + j);
-          acc = fmaf(a.x, b.x, acc);
-          acc = fmaf(a.y, b.y, acc);
-          acc = fmaf(a.z, b.z, acc);
-          acc = fmaf(a.w, b.w, acc);
-        }
-      } else {
-        for (int j = tid; j < D; j += kRouterThreads)
-          acc = fmaf(__ldg(wrow + j), load_act(x, x_dtype, (size_t)t * D + j), acc);
-      }
+    float acc[kRowsPerCta];
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      if (lane == 0) red[warp] = acc;
-      __syncthreads();
-      if (tid == 0) {
-        float z = 0.f;
-        for (int i = 0; i < kRouterThreads / 32; i++) z += red[i];
-        float sc = 1.0f / (1.0f + expf(-z));
-        float ch = bias ? __fadd_rn(sc, __ldg(bias + e)) : sc;
-        s_ws[(size_t)t * E + e] = sc;
-        c_ws[(size_t)t * E + e] = ch;
+    for (int r = 0; r < kRowsPerCta; r++) acc[r] = 0.f;
+    if (VEC4 && x_dtype == COLI_DTYPE_F32) {
+      const float4* x4 = reinterpret_cast<const float4*>(static_cast<const float*>(x) + (size_t)t * D);
+#pragma unroll 4
+      for (int j = tid; j < D / 4; j += kRouterThreads) {
+        const float4 b = __ldg(x4 + j);
+#pragma unroll
+        for (int r = 0; r < kRowsPerCta; r++) {
+          if (r < nrows) {
+            const float4 a = __ldg(reinterpret_cast<const float4*>(Wr + (size_t)(e0 + r) * D) + j);
+            acc[r] = fmaf(a.x, b.x, acc[r]);
+            acc[r] = fmaf(a.y, b.y, acc[r]);
+            acc[r] = fmaf(a.z, b.z, acc[r]);
+            acc[r] = fmaf(a.w, b.w, acc[r]);
+          }
+        }
       }
-      __syncthreads();
+    } else {
+#pragma unroll 4
+      for (int j = tid; j < D; j += kRouterThreads) {
+        const float b = load_act(x, x_dtype, (size_t)t * D + j);
+#pragma unroll
+        for (int r = 0; r < kRowsPerCta; r++)
+          if (r < nrows) acc[r] = fmaf(__ldg(Wr + (size_t)(e0 + r) * D + j), b, acc[r]);
+      }
     }
+#pragma unroll
+    for (int r = 0; r < kRowsPerCta; r++) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], off);
+      if (lane == 0) red[warp][r] = acc[r];
+    }
+    __syncthreads();
+    if (tid < nrows) {
+      float z = 0.f;
+      for (int i = 0; i < kRouterThreads / 32; i++) z += red[i][tid];
+      const int e = e0 + tid;
+      const float sc = 1.0f / (1.0f + expf(-z));
+      const float ch = bias ? __fadd_rn(sc, __ldg(bias + e)) : sc;
+      s_ws[(size_t)t * E + e] = sc;
+      c_ws[(size_t)t * E + e] = ch;
+    }
+    __syncthreads();
   }
   // The CTA that finishes last runs the selection over every token's complete score row.
   if (tid == 0) {
@@ -181,14 +198,21 @@ int launch_router(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const
               ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
   int grid = (E + kRowsPerCta - 1) / kRowsPerCta;
   ProfScope prof(ctx, COLI_KERNEL_ROUTER);
-  if (vec4)
-    router_kernel<true><<<grid, kRouterThreads, 0, ctx->stream>>>(x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk,
-                                                                  routed_scale, s_ws, c_ws, idx, w, n_sel,
-                                                                  ctx->d_status, epl);
-  else
-    router_kernel<false><<<grid, kRouterThreads, 0, ctx->stream>>>(x, x_dtype, S, D, Wr, bias, E, K, topp,
-                                                                   norm_topk, routed_scale, s_ws, c_ws, idx, w,
-                                                                   n_sel, ctx->d_status, epl);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kRouterThreads);
+  cfg.stream = ctx->stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const void* xp = x;
+  cudaError_t le = vec4 ? cudaLaunchKernelEx(&cfg, router_kernel<true>, xp, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk,
+                                             routed_scale, s_ws, c_ws, idx, w, n_sel, ctx->d_status, epl)
+                        : cudaLaunchKernelEx(&cfg, router_kernel<false>, xp, x_dtype, S, D, Wr, bias, E, K, topp,
+                                             norm_topk, routed_scale, s_ws, c_ws, idx, w, n_sel, ctx->d_status, epl);
+  if (le != cudaSuccess) return cuda_fail(ctx, le, "router launch");
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(ctx, e, "router launch");
   return COLI_OK;
