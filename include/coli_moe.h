@@ -62,6 +62,7 @@ extern "C" {
 #define COLI_MAX_DIM 32768      /* D and I */
 #define COLI_MAX_TOKENS 65536   /* S for coli_router_select */
 #define COLI_MAX_GROUP_TOKENS 1024  /* S for coli_expert_group */
+#define COLI_MAX_GROUP_DIM 8192     /* D (model width) for coli_expert_group */
 
 typedef struct coli_ctx coli_ctx;
 

@@ -89,8 +89,29 @@ static bool valid_handle(coli_ctx* ctx, uint64_t h) {
   return h >= 1 && h <= ctx->tensors.size() && ctx->tensors[h - 1].live;
 }
 
-static TensorDesc make_desc(const HostTensor& t) {
-  TensorDesc d;
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link-time libcuda dependency).
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    (void)cudaGetLastError();
+  }
+  return fn;
+}
+
+// Device descriptor of an uploaded tensor, with its TMA maps: the weights as a uint32 matrix
+// [O x pitch/4] read in boxes of [min(kBoxRows, O) rows x one warp's 128-word column slice], and,
+// when the group size lets a warp's chunk-group scales form a 16-byte-multiple box, the scales.
+static int make_desc(coli_ctx* ctx, HostTensor& t) {
+  TensorDesc d{};
   d.w = t.w;
   d.s = t.s;
   d.pitch = t.pitch;
@@ -99,7 +120,34 @@ static TensorDesc make_desc(const HostTensor& t) {
   d.rows = t.O;
   d.cols = t.I;
   d.mode = t.gs == 0 ? SCALE_ROW : (t.gs % 32 == 0 ? SCALE_CHUNK : SCALE_GENERIC);
-  return d;
+  const uint32_t words = t.pitch / 4;
+  d.box_rows = t.O < kBoxRows ? (uint32_t)t.O : (uint32_t)kBoxRows;
+  d.box_w = words < (uint32_t)kSliceWords ? words : (uint32_t)kSliceWords;
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(ctx, COLI_E_CUDA, "upload: cuTensorMapEncodeTiled unavailable");
+  {
+    cuuint64_t dims[2] = {words, (cuuint64_t)t.O};
+    cuuint64_t strides[1] = {t.pitch};
+    cuuint32_t box[2] = {d.box_w, d.box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(&d.map_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, t.w, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ctx, COLI_E_CUDA, "upload: weight tensor map encoding failed");
+  }
+  d.box_s = 0;
+  if (d.mode == SCALE_CHUNK && t.gs >= 64 && t.gs <= 256 && t.G % 4 == 0) {
+    uint32_t per_warp = (uint32_t)(32 * 32 / t.gs);  // chunk groups under one warp's 32 chunks
+    uint32_t bs = per_warp < (uint32_t)t.G ? per_warp : (uint32_t)t.G;
+    cuuint64_t dims[2] = {(cuuint64_t)t.G, (cuuint64_t)t.O};
+    cuuint64_t strides[1] = {(cuuint64_t)t.G * 4};
+    cuuint32_t box[2] = {bs, d.box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(&d.map_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, t.s, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS) d.box_s = bs;
+  }
+  t.desc = d;
+  return COLI_OK;
 }
 
 }  // namespace coli
@@ -278,6 +326,11 @@ uint64_t coli_expert_upload(coli_ctx* ctx, const uint8_t* packed, const float* s
   }
   t.w = static_cast<uint8_t*>(pw);
   t.s = static_cast<float*>(ps);
+  if (make_desc(ctx, t) != COLI_OK) {
+    cudaFree(pw);
+    cudaFree(ps);
+    return 0;
+  }
   t.live = true;
   ctx->tensors.push_back(t);
   return (uint64_t)ctx->tensors.size();
@@ -330,9 +383,9 @@ int coli_expert_table_set(coli_ctx* ctx, int e, uint64_t gate, uint64_t up, uint
     cur[1] = up;
     cur[2] = down;
     for (int i = 0; i < 3; i++) ctx->tensors[cur[i] - 1].table_refs++;
-    d.t[T_GATE] = make_desc(g);
-    d.t[T_UP] = make_desc(u);
-    d.t[T_DOWN] = make_desc(dn);
+    d.t[T_GATE] = g.desc;
+    d.t[T_UP] = u.desc;
+    d.t[T_DOWN] = dn.desc;
     d.valid = 1;
   }
   ctx->h_table[e] = d;

@@ -1,6 +1,7 @@
 // Internal declarations shared by the translation units of libcoli_moe.so (not installed).
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (types only; the driver entry point is fetched at run time)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -15,9 +16,18 @@ namespace coli {
 // Device-side tensor and expert descriptors
 // ---------------------------------------------------------------------------------------------
 
+// Rows per TMA box: one pipeline stage of one warp covers kBoxRows rows of its column slice.
+constexpr int kBoxRows = 8;
+// Words (uint32) of a row one warp owns: 32 lanes x 16 bytes.
+constexpr int kSliceWords = 128;
+// Chunk-group scales of one warp's slice that travel by TMA (group sizes 64..256).
+constexpr int kScaleBox = 16;
+
 // One uploaded int4 tensor as the kernels see it. Rows are padded to a whole number of 16-byte
 // chunks (32 columns each); padding nibbles hold 8, i.e. the value 0.
 struct TensorDesc {
+  CUtensorMap map_w;   // 2-D map over the weights as uint32 [rows x pitch/4], box [box_rows x box_w]
+  CUtensorMap map_s;   // 2-D map over chunk-group scales f32 [rows x G], box [box_rows x box_s]
   const uint8_t* w;    // rows x pitch bytes
   const float* s;      // scales: rows (gs == 0) or rows * G (gs > 0)
   uint32_t pitch;      // bytes per row, multiple of 16
@@ -25,6 +35,10 @@ struct TensorDesc {
   int32_t G;           // groups per row (1 when gs == 0)
   int32_t rows, cols;
   int32_t mode;        // SCALE_ROW, SCALE_CHUNK (gs % 32 == 0) or SCALE_GENERIC
+  uint32_t box_rows;   // rows of a weight box (min(kBoxRows, rows))
+  uint32_t box_w;      // words of a weight box row (min(kSliceWords, pitch / 4))
+  uint32_t box_s;      // floats of a scale box row (0: scales are not staged by TMA)
+  uint32_t pad_;
 };
 
 enum { SCALE_ROW = 0, SCALE_CHUNK = 1, SCALE_GENERIC = 2 };
@@ -33,7 +47,7 @@ enum { T_GATE = 0, T_UP = 1, T_DOWN = 2 };
 struct ExpertDesc {
   TensorDesc t[3];
   int32_t valid;
-  int32_t pad_[3];
+  int32_t pad_[15];
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -47,6 +61,7 @@ struct HostTensor {
   uint32_t pitch = 0;
   int table_refs = 0;
   bool live = false;
+  TensorDesc desc{};  // device view, tensor maps included
 };
 
 struct Workspace {

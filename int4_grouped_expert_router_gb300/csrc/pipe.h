@@ -110,6 +110,12 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
   return v;
 }
 
+__device__ __forceinline__ float lds32f(const void* p) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ int ld_cg_i32(const int* p) {
   int v;
   asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(v) : "l"(p));
