@@ -17,7 +17,7 @@ namespace coli {
 // ---------------------------------------------------------------------------------------------
 
 // Rows per TMA box: one pipeline stage of one warp covers kBoxRows rows of its column slice.
-constexpr int kBoxRows = 8;
+constexpr int kBoxRows = 4;
 // Words (uint32) of a row one warp owns: 32 lanes x 16 bytes.
 constexpr int kSliceWords = 128;
 // Chunk-group scales of one warp's slice that travel by TMA (group sizes 64..256).

@@ -28,9 +28,10 @@ namespace coli {
 // ------------------------------------------------------------------------------------------
 
 struct Limbs {
-  uint32_t r[4][2][4];  // [16-bit word of the chunk][even/odd columns][limb]: 4 bytes each
-  int32_t off[4];       // -8 * sum over the chunk of limb l
-  float kf[4];          // 2^(8 l - q)
+  uint32_t r[4][2][4];  // [32-bit word of the chunk][even/odd columns][limb]: 4 bytes each
+  int32_t a0[4];        // even-column accumulator start: -8 * sum over the even columns of limb l
+  int32_t b0[4];        // odd-column accumulator start: -128 * sum over the odd columns of limb l
+  float k01, k23;       // 2^(-q-4) and 2^(16-q-4)
 };
 
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
@@ -55,19 +56,20 @@ __device__ __forceinline__ bool make_limbs(const float (&v)[32], Limbs& L) {
     for (int p = 0; p < 2; p++)
 #pragma unroll
       for (int l = 0; l < 4; l++) L.r[w][p][l] = 0u;
-  if (!finite || M == 0.f) {
 #pragma unroll
-    for (int l = 0; l < 4; l++) {
-      L.off[l] = 0;
-      L.kf[l] = 0.f;
-    }
+  for (int l = 0; l < 4; l++) {
+    L.a0[l] = 0;
+    L.b0[l] = 0;
+  }
+  if (!finite || M == 0.f) {
+    L.k01 = 0.f;
+    L.k23 = 0.f;
     return finite;
   }
   int e;
   frexpf(M, &e);            // M < 2^e
   int q = 30 - e;           // M 2^q in [2^29, 2^30)
-  if (q > 126) q = 126;     // keep 2^-q a normal float (only for |x| < 2^-96)
-  int sum[4] = {0, 0, 0, 0};
+  if (q > 122) q = 122;     // keep 2^(-q-4) a normal float (only for |x| < 2^-92)
 #pragma unroll
   for (int j = 0; j < 32; j++) {
     int xi = __float2int_rn(ldexpf(v[j], q));
@@ -82,34 +84,37 @@ __device__ __forceinline__ bool make_limbs(const float (&v)[32], Limbs& L) {
     L.r[w][p][1] |= ((uint32_t)l1 & 0xffu) << (8 * b);
     L.r[w][p][2] |= ((uint32_t)l2 & 0xffu) << (8 * b);
     L.r[w][p][3] |= ((uint32_t)l3 & 0xffu) << (8 * b);
-    sum[0] += l0;
-    sum[1] += l1;
-    sum[2] += l2;
-    sum[3] += l3;
+    if (p == 0) {
+      L.a0[0] -= 8 * l0;
+      L.a0[1] -= 8 * l1;
+      L.a0[2] -= 8 * l2;
+      L.a0[3] -= 8 * l3;
+    } else {
+      L.b0[0] -= 128 * l0;
+      L.b0[1] -= 128 * l1;
+      L.b0[2] -= 128 * l2;
+      L.b0[3] -= 128 * l3;
+    }
   }
-#pragma unroll
-  for (int l = 0; l < 4; l++) {
-    L.off[l] = -8 * sum[l];
-    L.kf[l] = ldexpf(1.0f, 8 * l - q);
-  }
+  L.k01 = ldexpf(1.0f, -q - 4);
+  L.k23 = ldexpf(1.0f, 16 - q - 4);
   return true;
 }
 
-// Exact int -> float for |a| < 2^22 with an integer add and a float subtract (both on the fast
-// pipes): the integer is placed in the mantissa of 1.5 * 2^23.
-__device__ __forceinline__ float exact_i2f(int a) { return __int_as_float(a + 0x4B400000) - 12582912.0f; }
-
-// sum_j (n_j - 8) x_j over the 32 columns of one chunk, n_j the stored nibbles in wv. Even and odd
-// columns accumulate in separate chains (8 independent dp4a chains of 4); every partial sum is an
-// exact integer below 2^17 in magnitude.
+// sum_j (n_j - 8) x_j over the 32 columns of one chunk, n_j the stored nibbles in wv.
+// Even columns (low nibbles, w & 0x0f0f0f0f) and odd columns (high nibbles kept in place,
+// w & 0xf0f0f0f0 = 16 n) accumulate in separate dp4a chains; t_l = 16 a_l + b_l is then 16 times
+// the exact limb sum sum_j (n_j - 8) l_j (|t_l| <= 2^19). Limb pairs are joined exactly in 32-bit
+// integers, t_0 + 256 t_1 and t_2 + 256 t_3 (below 2^28), converted once each and scaled by
+// powers of two: the result is the dot product with the quantised activations, rounded twice.
 __device__ __forceinline__ float chunk_dot(const uint4 wv, const Limbs& L) {
-  int a0 = L.off[0], a1 = L.off[1], a2 = L.off[2], a3 = L.off[3];
-  int b0 = 0, b1 = 0, b2 = 0, b3 = 0;
+  int a0 = L.a0[0], a1 = L.a0[1], a2 = L.a0[2], a3 = L.a0[3];
+  int b0 = L.b0[0], b1 = L.b0[1], b2 = L.b0[2], b3 = L.b0[3];
   const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
   for (int w = 0; w < 4; w++) {
-    const uint32_t lo = words[w] & 0x0f0f0f0fu;          // even columns, one per byte
-    const uint32_t hi = (words[w] >> 4) & 0x0f0f0f0fu;   // odd columns
+    const uint32_t lo = words[w] & 0x0f0f0f0fu;  // even columns: n
+    const uint32_t hi = words[w] & 0xf0f0f0f0u;  // odd columns: 16 n
     a0 = dp4a_us(lo, L.r[w][0][0], a0);
     a1 = dp4a_us(lo, L.r[w][0][1], a1);
     a2 = dp4a_us(lo, L.r[w][0][2], a2);
@@ -119,8 +124,9 @@ __device__ __forceinline__ float chunk_dot(const uint4 wv, const Limbs& L) {
     b2 = dp4a_us(hi, L.r[w][1][2], b2);
     b3 = dp4a_us(hi, L.r[w][1][3], b3);
   }
-  return fmaf(exact_i2f(a3 + b3), L.kf[3],
-              fmaf(exact_i2f(a2 + b2), L.kf[2], fmaf(exact_i2f(a1 + b1), L.kf[1], exact_i2f(a0 + b0) * L.kf[0])));
+  const int t0 = 16 * a0 + b0, t1 = 16 * a1 + b1, t2 = 16 * a2 + b2, t3 = 16 * a3 + b3;
+  const int p01 = t0 + 256 * t1, p23 = t2 + 256 * t3;
+  return fmaf(__int2float_rn(p23), L.k23, __int2float_rn(p01) * L.k01);
 }
 
 // Any even gs that is not a multiple of 32: a chunk may cross group boundaries, so each column
@@ -280,12 +286,12 @@ struct GroupParams {
 //
 // Every consumer warp owns one 512-byte column slice (32 chunks of 16 bytes) of the weight rows
 // and streams it by itself: its lane 0 issues 2-D TMA loads of [kBoxRows rows x slice] boxes into
-// the warp's own ring of kWarpStages shared-memory stages, kWarpStages boxes ahead of the
-// warp's compute. Warps never wait for each other while streaming; they meet only at the end of a
+// the warp's own ring of shared-memory stages, a ring's depth of boxes ahead of the warp's
+// compute. Warps never wait for each other while streaming; they meet only at the end of a
 // segment of rows to add their slices' partial sums in a fixed order.
 // ------------------------------------------------------------------------------------------
 
-constexpr int kWarpStages = 2;
+constexpr int kDStages = 4;  // stages per warp ring of the down kernel
 constexpr int kSeg = 64;          // rows (down) or row pairs (gate/up) finished together
 constexpr int kRouteCache = 16;   // routes resolved once into shared memory
 
@@ -351,62 +357,53 @@ __device__ __forceinline__ void lane_tensor(LaneTensor& lt, const SlotTensor& st
   lt.fast = st.mode == SCALE_ROW || (st.mode == SCALE_CHUNK && st.box_s > 0);
 }
 
-// Dot product of one staged chunk with the activation limbs, scaled by its chunk-group scale
-// (per-row scales are applied after the row is complete). `sc` points at the staged scale box.
-__device__ __noinline__ float chunk_dot_slow(const uint4 wv, const Limbs& L, const LaneTensor& lt, const void* act,
-                                             int dtype, size_t base, int row, int c) {
+// The slow paths (any even group size that is not a multiple of 32, or chunk scales that do not
+// travel by TMA): the activation limbs stay in registers -- they are never passed by reference to
+// an out-of-line function, which would move them to local memory for the whole kernel.
+__device__ __forceinline__ float chunk_dot_slow(const uint4 wv, const Limbs& L, const LaneTensor& lt, const void* act,
+                                                int dtype, size_t base, int row, int c) {
   if (lt.mode == SCALE_GENERIC) return chunk_dot_generic(wv, act, dtype, base, lt.d, row, c);
   return chunk_dot(wv, L) * __ldg(lt.s + (size_t)row * lt.G + lt.cg);
 }
 
-// Walks [beg, end) over (route, row) items, `rows` rows per route, in batches of up to kBoxRows
-// items that never cross a route or a segment (kSeg items from beg).
-struct BatchWalk {
-  int j, i, left, done, rows;
-  __device__ BatchWalk(long long beg, long long end, int rows_) : rows(rows_) {
-    j = (int)(beg / rows_);
-    i = (int)(beg - (long long)j * rows_);
-    left = (int)(end - beg);
-    done = 0;
-  }
-  __device__ int next() const {
-    int n = kBoxRows < rows - i ? kBoxRows : rows - i;
-    n = n < left ? n : left;
-    const int to_seg = kSeg - done % kSeg;
-    return n < to_seg ? n : to_seg;
-  }
-  __device__ void advance(int n) {
-    i += n;
-    left -= n;
-    done += n;
-    if (i == rows) {
-      i = 0;
-      j++;
-    }
-  }
-};
 
 // ------------------------------------------------------------------------------------------
 // Gate + up dual GEMV with the SiLU(g) * u epilogue.
 // Thread c of the CTA owns column chunk c (warp c / 32 owns slice c / 32) of every row and keeps
 // that chunk of the activation in registers. A stage of a warp holds kBoxRows gate rows and
 // kBoxRows up rows of its slice (and their chunk scales when those travel by TMA).
+// Work items are batches of kBoxRows row pairs: route j owns batches covering its rows padded to
+// a multiple of kBoxRows, so batch q is (route q / Bpr, first row kBoxRows (q % Bpr)) in closed
+// form and a CTA owns a contiguous run of batches; segB batches (one row pair per thread of the
+// CTA, at most kSeg) form a finishing segment.
 // ------------------------------------------------------------------------------------------
+
+constexpr int kGUStages = 3;                 // stages per warp ring
+
+__device__ const float kOneF = 1.0f;         // stand-in scale for unconditional loads
 
 struct GateUpSmem {
   RouteSlot routes[kRouteCache];
-  uint64_t bars[8][kWarpStages];  // gate/up CTAs have at most 8 warps (D <= 8192)
+  uint64_t bars[8][kGUStages];     // gate/up CTAs have at most 8 warps (D <= 8192)
+  int e_spec[COLI_MAX_K];          // S == 1: the expert of each slot, read with n_sel
 };
 // followed in dynamic shared memory by the warps' rings, pg[W][kSeg], pu[W][kSeg], pre[S + 1]
 
-__host__ __device__ inline uint32_t gateup_stage_bytes() {
+__host__ __device__ constexpr uint32_t gateup_stage_bytes() {
   // gate box + up box (kBoxRows x 512 B each) + two scale boxes (kBoxRows x kScaleBox floats)
   return 2u * kBoxRows * kSliceWords * 4 + 2u * kBoxRows * kScaleBox * 4;
 }
 
+// 2-D TMA writes need 128-byte-aligned shared-memory destinations: the rings start on a 128-byte
+// boundary after the control block and every stage, box and scale box is a multiple of 128 bytes.
+constexpr size_t kGUCtrlBytes = (sizeof(GateUpSmem) + 127) / 128 * 128;
+static_assert(gateup_stage_bytes() % 128 == 0, "gate/up stage must keep 128-byte alignment");
+static_assert((kBoxRows * kSliceWords * 4) % 128 == 0 && (kBoxRows * kScaleBox * 4) % 128 == 0,
+              "TMA boxes must keep 128-byte alignment");
+
 inline size_t gateup_smem_bytes(int W, int S) {
-  return 128 + sizeof(GateUpSmem) + (size_t)W * kWarpStages * gateup_stage_bytes() +
-         2 * (size_t)W * kSeg * sizeof(float) + (size_t)(S + 1) * sizeof(int);
+  return 128 + kGUCtrlBytes + (size_t)W * kGUStages * gateup_stage_bytes() + 2 * (size_t)W * kSeg * sizeof(float) +
+         (size_t)(S + 1) * sizeof(int);
 }
 
 template <int MAXT>
@@ -417,8 +414,8 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 192 ? 2 : 1) gateup_kernel(Group
   const int W = (C + 31) >> 5;
   const uint32_t SB = gateup_stage_bytes();
   GateUpSmem& sm = *reinterpret_cast<GateUpSmem*>(smem_raw);
-  uint8_t* rings = smem_raw + sizeof(GateUpSmem);
-  float* pg = reinterpret_cast<float*>(rings + (size_t)W * kWarpStages * SB);
+  uint8_t* rings = smem_raw + kGUCtrlBytes;
+  float* pg = reinterpret_cast<float*>(rings + (size_t)W * kGUStages * SB);
   float* pu = pg + (size_t)W * kSeg;
   int* pre = reinterpret_cast<int*>(pu + (size_t)W * kSeg);
   __shared__ int scratch32[32];
@@ -426,160 +423,182 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 192 ? 2 : 1) gateup_kernel(Group
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = tid;
   const bool has_chunk = c < C;
-  uint8_t* ring = rings + (size_t)warp * kWarpStages * SB;
+  uint8_t* ring = rings + (size_t)warp * kGUStages * SB;
   uint64_t* bars = sm.bars[warp];
   if (lane == 0) {
-    for (int s = 0; s < kWarpStages; s++) mbar_init(&bars[s], 1);
+    for (int s = 0; s < kGUStages; s++) mbar_init(&bars[s], 1);
     mbar_fence_init();
   }
   // prologue overlapping the router's tail: activation limbs of token 0
   Limbs L;
-  float xv[32];
   int cur_tok = 0;
-  load_chunk_f32(P.x, P.x_dtype, 0, 32 * c, has_chunk ? P.D : 0, xv);
-  const bool finite0 = make_limbs(xv, L);
+  {
+    float xv[32];
+    load_chunk_f32(P.x, P.x_dtype, 0, 32 * c, has_chunk ? P.D : 0, xv);
+    if (!make_limbs(xv, L) && has_chunk) set_error(P.err, COLI_E_NONFINITE);
+  }
   griddep_wait();
-  const int R = build_plan(P.n_sel, P.S, P.K, pre, scratch32);  // contains __syncthreads
+  if (P.S == 1 && tid < P.K) sm.e_spec[tid] = ld_cg_i32(P.idx + tid);  // same round trip as n_sel
+  const int R = build_plan(P.n_sel, P.S, P.K, pre, scratch32);       // contains __syncthreads
   if (blockIdx.x == 0)
     for (int t = tid; t <= P.S; t += blockDim.x) P.plan[t] = pre[t];
   griddep_launch_dependents();
-  if (!finite0 && has_chunk) set_error(P.err, COLI_E_NONFINITE);
 
-  const long long T = (long long)R * P.I;
-  const long long pbeg = (long long)blockIdx.x * T / gridDim.x;
-  const long long pend = (long long)(blockIdx.x + 1) * T / gridDim.x;
-  if (pbeg >= pend) return;  // uniform across the CTA
-  const int j_first = (int)(pbeg / P.I);
-  const int n_routes = (int)((pend - 1) / P.I) - j_first + 1;  // <= kRouteCache (launch sizing)
-  if (tid < n_routes) resolve_slot(P, pre, j_first + tid, T_GATE, T_UP, sm.routes[tid]);
+  const int Bpr = (P.I + kBoxRows - 1) / kBoxRows;  // batches per route
+  const int segB = min(kSeg, W * 32) / kBoxRows;    // batches per finishing segment
+  const long long NB = (long long)R * Bpr;
+  const int qbeg = (int)((long long)blockIdx.x * NB / gridDim.x);
+  const int qend = (int)((long long)(blockIdx.x + 1) * NB / gridDim.x);
+  if (qbeg >= qend) return;  // uniform across the CTA
+  const int j_first = qbeg / Bpr;
+  const int n_routes = (qend - 1) / Bpr - j_first + 1;  // <= kRouteCache (launch sizing)
+  if (n_routes > kRouteCache) {  // uniform across the CTA; the launcher's grid rules this out
+    if (tid == 0) set_error(P.err, COLI_E_INVAL);
+    return;
+  }
+  if (tid < n_routes) {
+    const int j = j_first + tid;
+    RouteSlot& rs = sm.routes[tid];
+    if (P.S == 1) {
+      const int e = sm.e_spec[j];
+      rs.t = 0;
+      rs.ok = e >= 0 && e < COLI_MAX_EXPERTS && P.table[e].valid;
+      if (rs.ok) {
+        fill_slot_tensor(rs.ts[0], &P.table[e].t[T_GATE]);
+        fill_slot_tensor(rs.ts[1], &P.table[e].t[T_UP]);
+      }
+    } else {
+      resolve_slot(P, pre, j, T_GATE, T_UP, rs);
+    }
+    if (!rs.ok) set_error(P.err, COLI_E_ROUTE);
+  }
   __syncthreads();
 
-  // issue side of this warp's ring: kWarpStages batches ahead of the compute
-  BatchWalk iw(pbeg, pend, P.I);
-  uint32_t issued = 0;
+  // issue side of this warp's ring: kGUStages batches ahead of the compute (lane 0)
+  int iq = qbeg, ij = j_first, ii = (qbeg - j_first * Bpr) * kBoxRows, issued = 0;
   auto issue_next = [&]() {
-    while (iw.left > 0) {
-      const int n = iw.next(), j = iw.j, i0 = iw.i;
-      iw.advance(n);
+    for (; iq < qend; iq++) {
+      const int j = ij, i0 = ii;
+      ii += kBoxRows;
+      if (ii >= Bpr * kBoxRows) {
+        ii = 0;
+        ij++;
+      }
       const RouteSlot& rs = sm.routes[j - j_first];
       if (!rs.ok) continue;
-      const uint32_t s = issued % kWarpStages;
-      uint8_t* st = ring + (size_t)s * SB;
       const SlotTensor& g = rs.ts[0];
       const SlotTensor& u = rs.ts[1];
+      uint64_t* bar = &bars[issued % kGUStages];
+      uint8_t* st = ring + (size_t)(issued % kGUStages) * SB;
       uint32_t bytes = 2u * g.box_rows * g.box_w * 4;
       if (g.box_s) bytes += g.box_rows * g.box_s * 4;
       if (u.box_s) bytes += u.box_rows * u.box_s * 4;
-      mbar_arrive_expect_tx(&bars[s], bytes);
+      mbar_arrive_expect_tx(bar, bytes);
       const int x = kSliceWords * warp;
-      tma_load_2d(st, &g.d->map_w, x, i0, &bars[s]);
-      tma_load_2d(st + kBoxRows * kSliceWords * 4, &u.d->map_w, x, i0, &bars[s]);
-      if (g.box_s) tma_load_2d(st + 2 * kBoxRows * kSliceWords * 4, &g.d->map_s, g.box_s * warp, i0, &bars[s]);
+      tma_load_2d(st, &g.d->map_w, x, i0, bar);
+      tma_load_2d(st + kBoxRows * kSliceWords * 4, &u.d->map_w, x, i0, bar);
+      if (g.box_s) tma_load_2d(st + 2 * kBoxRows * kSliceWords * 4, &g.d->map_s, g.box_s * warp, i0, bar);
       if (u.box_s)
-        tma_load_2d(st + 2 * kBoxRows * kSliceWords * 4 + kBoxRows * kScaleBox * 4, &u.d->map_s, u.box_s * warp, i0,
-                    &bars[s]);
+        tma_load_2d(st + 2 * kBoxRows * kSliceWords * 4 + kBoxRows * kScaleBox * 4, &u.d->map_s, u.box_s * warp, i0, bar);
       issued++;
+      iq++;
       return;
     }
   };
   if (lane == 0)
-    for (int s = 0; s < kWarpStages; s++) issue_next();
+    for (int s = 0; s < kGUStages; s++) issue_next();
 
-  // ---------------- compute ----------------
-  int rj = -1;
-  const RouteSlot* rs = nullptr;
-  LaneTensor tg, tu;
-  uint32_t b = 0;
-  bool stop = false;
-  int seg_n = 0;
-  float fg = 1.f, fu = 1.f;  // finaliser thread `tid`: row scales of its segment row pair
+  // finaliser thread `tid` (< kSeg) of a segment: where its row pair goes and its row scales,
+  // loaded unconditionally when the segment starts and consumed when it ends
+  float fg = 1.f, fu = 1.f;
   size_t hdst = 0;
   bool fin_ok = false;
-  for (BatchWalk cw(pbeg, pend, P.I); cw.left > 0;) {
-    const int n = cw.next(), j = cw.j, i0 = cw.i;
-    cw.advance(n);
-    if (j != rj) {
-      rj = j;
-      rs = &sm.routes[j - j_first];
-      if (rs->ok) {
-        lane_tensor(tg, rs->ts[0], c);
-        lane_tensor(tu, rs->ts[1], c);
-        if (rs->t != cur_tok) {
-          cur_tok = rs->t;
+  auto prefetch_finaliser = [&](int q0) {
+    const int qq = q0 + tid / kBoxRows;
+    const int jj = qq / Bpr, i = (qq - jj * Bpr) * kBoxRows + tid % kBoxRows;
+    fin_ok = tid < segB * kBoxRows && qq < qend && i < P.I && sm.routes[jj - j_first].ok;
+    const RouteSlot& r = sm.routes[fin_ok ? jj - j_first : 0];
+    hdst = (size_t)jj * P.I + i;
+    fg = __ldg((fin_ok && r.ts[0].mode == SCALE_ROW) ? r.ts[0].s + i : &kOneF);
+    fu = __ldg((fin_ok && r.ts[1].mode == SCALE_ROW) ? r.ts[1].s + i : &kOneF);
+  };
+
+  // ---------------- compute ----------------
+  int cur_slot = -1;
+  LaneTensor tg, tu;
+  bool stop = false;
+  int cq = 0;  // batches consumed by this warp
+  for (int q = qbeg, j = j_first, i0 = (qbeg - j_first * Bpr) * kBoxRows; q < qend; q++) {
+    if ((q - qbeg) % segB == 0) prefetch_finaliser(q);
+    const int slot = j - j_first;
+    const int n = min(kBoxRows, P.I - i0);
+    const bool rok = sm.routes[slot].ok;
+    if (rok) {
+      if (slot != cur_slot) {
+        cur_slot = slot;
+        const RouteSlot& rs = sm.routes[slot];
+        lane_tensor(tg, rs.ts[0], c);
+        lane_tensor(tu, rs.ts[1], c);
+        if (rs.t != cur_tok) {
+          cur_tok = rs.t;
+          float xv[32];
           load_chunk_f32(P.x, P.x_dtype, (size_t)cur_tok * P.D, 32 * c, has_chunk ? P.D : 0, xv);
           if (!make_limbs(xv, L) && has_chunk) set_error(P.err, COLI_E_NONFINITE);
         }
-      } else if (tid == 0) {
-        set_error(P.err, COLI_E_ROUTE);
       }
-    }
-    const bool rok = rs->ok;
-    if (tid >= seg_n && tid < seg_n + n) {  // finaliser of each row pair of this batch
-      const int ii = i0 + (tid - seg_n);
-      fin_ok = rok;
-      hdst = (size_t)j * P.I + ii;
-      fg = (rok && tg.mode == SCALE_ROW) ? __ldg(tg.s + ii) : 1.f;
-      fu = (rok && tu.mode == SCALE_ROW) ? __ldg(tu.s + ii) : 1.f;
-    }
-    if (rok && !stop) {
-      const uint32_t s = b % kWarpStages;
-      const bool ok = mbar_wait(&bars[s], (b / kWarpStages) & 1);
-      const uint8_t* st = ring + (size_t)s * SB;
-      const uint8_t* sg = st + 2 * kBoxRows * kSliceWords * 4;
-      const uint8_t* su = sg + kBoxRows * kScaleBox * 4;
-      float acc[2 * kBoxRows];
-      const int sgo = tg.cg - tg.box_s * warp, suo = tu.cg - tu.box_s * warp;  // lane's scale in the box
+      const bool ok = !stop && mbar_wait(&bars[cq % kGUStages], (cq / kGUStages) & 1);
+      const uint8_t* st = ring + (size_t)(cq % kGUStages) * SB;
+      const uint8_t* sgb = st + 2 * kBoxRows * kSliceWords * 4;
+      float acc[2 * kBoxRows];  // gate rows 0..3, then up rows 0..3
       if (ok && has_chunk && tg.fast && tu.fast) {
 #pragma unroll
         for (int u = 0; u < kBoxRows; u++) {
-          float dg = 0.f, du = 0.f;
-          if (u < n) {
-            dg = chunk_dot(lds128(st + u * tg.rowB + 16 * lane), L);
-            du = chunk_dot(lds128(st + kBoxRows * kSliceWords * 4 + u * tu.rowB + 16 * lane), L);
-            if (tg.box_s) dg *= lds32f(sg + (u * tg.box_s + sgo) * 4);
-            if (tu.box_s) du *= lds32f(su + (u * tu.box_s + suo) * 4);
-          }
-          acc[2 * u] = dg;
-          acc[2 * u + 1] = du;
+          float dg = chunk_dot(lds128(st + u * tg.rowB + 16 * lane), L);
+          float du = chunk_dot(lds128(st + kBoxRows * kSliceWords * 4 + u * tu.rowB + 16 * lane), L);
+          if (tg.box_s) dg *= lds32f(sgb + (u * tg.box_s + tg.cg - tg.box_s * warp) * 4);
+          if (tu.box_s) du *= lds32f(sgb + kBoxRows * kScaleBox * 4 + (u * tu.box_s + tu.cg - tu.box_s * warp) * 4);
+          acc[u] = dg;
+          acc[kBoxRows + u] = du;
         }
       } else {
-        float tmp[2 * kBoxRows];  // local memory: the rarely used slow path keeps code small
+        float tmp[2 * kBoxRows];  // local memory: the rarely used slow path keeps the code small
 #pragma unroll 1
-        for (int u = 0; u < kBoxRows; u++) {
-          float dg = 0.f, du = 0.f;
+        for (int v = 0; v < 2 * kBoxRows; v++) {
+          const int u = v % kBoxRows;
+          const LaneTensor& lt = v < kBoxRows ? tg : tu;
+          float d = 0.f;
           if (ok && has_chunk && u < n) {
-            const uint4 wg = lds128(st + u * tg.rowB + 16 * lane);
-            const uint4 wu = lds128(st + kBoxRows * kSliceWords * 4 + u * tu.rowB + 16 * lane);
-            const size_t xb = (size_t)cur_tok * P.D;
-            dg = tg.fast ? chunk_dot(wg, L) * (tg.box_s ? lds32f(sg + (u * tg.box_s + sgo) * 4) : 1.f)
-                         : chunk_dot_slow(wg, L, tg, P.x, P.x_dtype, xb, i0 + u, c);
-            du = tu.fast ? chunk_dot(wu, L) * (tu.box_s ? lds32f(su + (u * tu.box_s + suo) * 4) : 1.f)
-                         : chunk_dot_slow(wu, L, tu, P.x, P.x_dtype, xb, i0 + u, c);
+            const uint4 wv = lds128(st + (v / kBoxRows) * (kBoxRows * kSliceWords * 4) + u * lt.rowB + 16 * lane);
+            if (lt.fast)
+              d = chunk_dot(wv, L) *
+                  (lt.box_s ? lds32f(sgb + (v / kBoxRows) * (kBoxRows * kScaleBox * 4) +
+                                     (u * lt.box_s + lt.cg - lt.box_s * warp) * 4)
+                            : 1.f);
+            else
+              d = chunk_dot_slow(wv, L, lt, P.x, P.x_dtype, (size_t)cur_tok * P.D, i0 + u, c);
           }
-          tmp[2 * u] = dg;
-          tmp[2 * u + 1] = du;
+          tmp[v] = d;
         }
 #pragma unroll
         for (int v = 0; v < 2 * kBoxRows; v++) acc[v] = tmp[v];
       }
       __syncwarp();
-      if (lane == 0) issue_next();  // refill the stage just consumed
-      if (!ok) {
+      if (lane == 0 && ok) issue_next();  // refill the stage just consumed
+      if (!ok && !stop) {
         stop = true;
         set_error(P.err, COLI_E_TIMEOUT);
       }
-      // lane l ends with the warp total of value l / 2: row pair v / 2, gate (even v) or up (odd v)
+      cq++;
+      // lane l ends with the warp total of value l / 4: gate row v (v < 4) or up row v - 4
       warp_transpose_reduce<2 * kBoxRows>(acc, lane);
-      if ((lane & 1) == 0) {
-        const int v = lane >> 1;
-        if ((v >> 1) < n) ((v & 1) ? pu : pg)[warp * kSeg + seg_n + (v >> 1)] = acc[0];
+      if ((lane & 3) == 0) {
+        const int v = lane >> 2, u = v % kBoxRows;
+        if (u < n) (v < kBoxRows ? pg : pu)[warp * kSeg + ((q - qbeg) % segB) * kBoxRows + u] = acc[0];
       }
-      b++;
     }
-    seg_n += n;
-    if (seg_n == kSeg || cw.left == 0) {
+    if ((q - qbeg) % segB == segB - 1 || q + 1 == qend) {  // segment end: finish its rows
       const bool any_stop = named_sync_or(1, W * 32, stop);
-      if (!any_stop && tid < seg_n && fin_ok) {
+      if (!any_stop && fin_ok) {
         float g = 0.f, u = 0.f;
         for (int wi = 0; wi < W; wi++) {
           g += pg[wi * kSeg + tid];
@@ -588,15 +607,18 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 192 ? 2 : 1) gateup_kernel(Group
         P.h[hdst] = silu_mul(g * fg, u * fu);
       }
       named_sync(1, W * 32);  // the partial buffers are reused by the next segment
-      seg_n = 0;
-      fin_ok = false;
       if (any_stop) stop = true;
     }
+    i0 += kBoxRows;
+    if (i0 >= Bpr * kBoxRows) {
+      i0 = 0;
+      j++;
+    }
   }
-  // never leave with TMA loads in flight into this warp's ring
+  // never leave with TMA loads in flight into this warp's ring (the last issued phases)
   if (lane == 0)
-    for (uint32_t q = issued > kWarpStages ? issued - kWarpStages : 0; q < issued; q++)
-      if (q >= b) (void)mbar_wait(&bars[q % kWarpStages], (q / kWarpStages) & 1);
+    for (int q = issued > kGUStages ? issued - kGUStages : 0; q < issued; q++)
+      (void)mbar_wait(&bars[q % kGUStages], (q / kGUStages) & 1);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -607,7 +629,7 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 192 ? 2 : 1) gateup_kernel(Group
 // ------------------------------------------------------------------------------------------
 
 struct DownSmem {
-  uint64_t bars[32][kWarpStages];
+  uint64_t bars[32][kDStages];
   float part[32][kSeg];
   float rscale[COLI_MAX_K][kSeg];
   float wk[COLI_MAX_K];
@@ -615,10 +637,12 @@ struct DownSmem {
   int ok[COLI_MAX_K];
 };
 
-__host__ __device__ inline uint32_t down_stage_bytes() { return kBoxRows * kSliceWords * 4 + kBoxRows * kScaleBox * 4; }
+__host__ __device__ constexpr uint32_t down_stage_bytes() { return kBoxRows * kSliceWords * 4 + kBoxRows * kScaleBox * 4; }
+constexpr size_t kDCtrlBytes = (sizeof(DownSmem) + 127) / 128 * 128;
+static_assert(down_stage_bytes() % 128 == 0, "down stage must keep 128-byte alignment");
 
 inline size_t down_smem_bytes(int nwarps) {
-  return 128 + sizeof(DownSmem) + (size_t)nwarps * kWarpStages * down_stage_bytes();
+  return 128 + kDCtrlBytes + (size_t)nwarps * kDStages * down_stage_bytes();
 }
 
 template <int MAXT>
@@ -633,14 +657,14 @@ __global__ void __launch_bounds__(MAXT, 1) down_fused_kernel(GroupParams P, int 
   const int CI = (P.I + 31) >> 5;
   const int wpe = TPE >> 5;
   const int slice = warp % wpe;  // this warp's column slice of its expert's rows
-  uint8_t* ring = smem_raw + sizeof(DownSmem) + (size_t)warp * kWarpStages * SB;
+  uint8_t* ring = smem_raw + kDCtrlBytes + (size_t)warp * kDStages * SB;
   uint64_t* bars = sm.bars[warp];
 
   // routes of token 0 (written by the router, complete before the gate/up kernel started)
   int m = P.n_sel ? ld_cg_i32(P.n_sel) : P.K;
   m = m < 0 ? 0 : (m > P.K ? P.K : m);
   if (lane == 0) {
-    for (int s = 0; s < kWarpStages; s++) mbar_init(&bars[s], 1);
+    for (int s = 0; s < kDStages; s++) mbar_init(&bars[s], 1);
     mbar_fence_init();
   }
   if (tid < P.K) {
@@ -665,7 +689,7 @@ __global__ void __launch_bounds__(MAXT, 1) down_fused_kernel(GroupParams P, int 
   const uint32_t nbat = (uint32_t)((d_end - d_begin + kBoxRows - 1) / kBoxRows);
   auto issue_next = [&]() {
     if (issued >= nbat) return;
-    const uint32_t s = issued % kWarpStages;
+    const uint32_t s = issued % kDStages;
     uint8_t* st = ring + (size_t)s * SB;
     const int d0 = d_begin + (int)issued * kBoxRows;
     uint32_t bytes = sl->box_rows * sl->box_w * 4 + (sl->box_s ? sl->box_rows * sl->box_s * 4 : 0);
@@ -675,7 +699,7 @@ __global__ void __launch_bounds__(MAXT, 1) down_fused_kernel(GroupParams P, int 
     issued++;
   };
   if (warp_on && lane == 0)
-    for (int s = 0; s < kWarpStages; s++) issue_next();  // the weight stream starts before h is ready
+    for (int s = 0; s < kDStages; s++) issue_next();  // the weight stream starts before h is ready
 
   LaneTensor lt;
   lane_tensor(lt, *sl, c);
@@ -703,8 +727,8 @@ __global__ void __launch_bounds__(MAXT, 1) down_fused_kernel(GroupParams P, int 
     for (int d0 = s0; d0 < s0 + nseg; d0 += kBoxRows) {
       const int n = min(kBoxRows, s0 + nseg - d0);
       if (!warp_on || stop) continue;
-      const uint32_t s = b % kWarpStages;
-      const bool ok = mbar_wait(&bars[s], (b / kWarpStages) & 1);
+      const uint32_t s = b % kDStages;
+      const bool ok = mbar_wait(&bars[s], (b / kDStages) & 1);
       const uint8_t* st = ring + (size_t)s * SB;
       float acc[kBoxRows];
       if (ok && active && lt.fast) {
@@ -729,14 +753,15 @@ __global__ void __launch_bounds__(MAXT, 1) down_fused_kernel(GroupParams P, int 
         for (int u = 0; u < kBoxRows; u++) acc[u] = tmp[u];
       }
       __syncwarp();
-      if (lane == 0) issue_next();
+      if (lane == 0 && ok) issue_next();
       if (!ok) {
         stop = true;
         set_error(P.err, COLI_E_TIMEOUT);
       }
-      // lane l ends with the warp total of row l / 4 of the batch
+      // lane l ends with the warp total of row l / (32 / kBoxRows) of the batch
       warp_transpose_reduce<kBoxRows>(acc, lane);
-      if ((lane & 3) == 0 && (lane >> 2) < n) sm.part[warp][d0 - s0 + (lane >> 2)] = acc[0];
+      constexpr int kSpread = 32 / kBoxRows;
+      if ((lane & (kSpread - 1)) == 0 && (lane / kSpread) < n) sm.part[warp][d0 - s0 + lane / kSpread] = acc[0];
       b++;
     }
     if (rsk >= 0) sm.rscale[rsk][rsr] = rsv;
@@ -760,8 +785,8 @@ __global__ void __launch_bounds__(MAXT, 1) down_fused_kernel(GroupParams P, int 
     if (any_stop) stop = true;
   }
   if (warp_on && lane == 0)  // never leave with TMA loads in flight into this warp's ring
-    for (uint32_t q = issued > kWarpStages ? issued - kWarpStages : 0; q < issued; q++)
-      if (q >= b) (void)mbar_wait(&bars[q % kWarpStages], (q / kWarpStages) & 1);
+    for (uint32_t q = issued > kDStages ? issued - kDStages : 0; q < issued; q++)
+      (void)mbar_wait(&bars[q % kDStages], (q / kDStages) & 1);
 }
 
 // ------------------------------------------------------------------------------------------

@@ -1,14 +1,23 @@
 // Device helpers for streaming kernels on sm_100-family GPUs: mbarriers, bulk asynchronous copies
-// (TMA, non-tensor form) global -> shared memory, and programmatic dependent launch controls.
-// Every wait is bounded: after kSpinLimit unsuccessful polls it reports failure to the caller,
-// which records COLI_E_TIMEOUT in the context's error word instead of hanging.
+// (TMA) global -> shared memory, and programmatic dependent launch controls.
+// Every wait is bounded: a waiting thread sleeps in mbarrier.try_wait (woken when the phase
+// completes) and gives up after kWaitLimitNs of wall-clock time; the caller then records
+// COLI_E_TIMEOUT in the context's error word instead of hanging.
 #pragma once
 
 #include <stdint.h>
 
 namespace coli {
 
-constexpr uint32_t kSpinLimit = 1u << 24;
+constexpr uint32_t kSpinLimit = 1u << 24;          // polls of a non-sleeping test loop
+constexpr uint64_t kWaitLimitNs = 2000000000ull;     // 2 s
+constexpr uint32_t kSuspendHintNs = 20000;           // longest single sleep inside try_wait
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -44,11 +53,23 @@ __device__ __forceinline__ bool mbar_test_parity(uint64_t* bar, uint32_t parity)
   return ok != 0;
 }
 
-// Wait until the phase with the given parity has completed; false after kSpinLimit polls.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait until the phase with the given parity has completed; false after kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; i++)
-    if (mbar_test_parity(bar, parity)) return true;
-  return false;
+  if (mbar_try_wait_sleep(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait_sleep(bar, parity))
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  return true;
 }
 
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from global to shared

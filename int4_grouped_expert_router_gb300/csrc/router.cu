@@ -14,56 +14,67 @@ namespace coli {
 constexpr int kRouterThreads = 256;
 constexpr int kRowsPerCta = 2;  // E = 256 -> 128 CTAs, every row group in flight at once
 
-// One warp selects for one token. Lane l owns experts e = l + 32 * i (i < EPL), so each lane's
-// own scan runs in increasing e and a strict '>' keeps the first (lowest) index of a tie; the
-// cross-lane arg-max breaks equal scores by the lower index as well.
+// Order-preserving map of a finite binary32 value to uint32 (larger float -> larger integer;
+// -0 is folded onto +0 so that the two compare equal, as floats do).
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f == 0.f ? 0.f : f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// One warp selects for one token. Lane l owns experts e = l + 32 * i (i < EPL). Each round, every
+// lane finds its best not-yet-chosen expert by a strict '>' scan in increasing e (so its first,
+// lowest index wins a local tie); the warp maximum of the order keys and then the minimum index
+// among the lanes holding that maximum are taken with warp reductions, so a tie across lanes also
+// goes to the lower index. The chosen expert's raw score travels with it.
 template <int EPL>
-__device__ void select_token(const float* __restrict__ c_row, const float* __restrict__ s_row, int E,
-                             int K, float topp, int norm_topk, float routed_scale,
-                             int32_t* __restrict__ idx_out, float* __restrict__ w_out,
+__device__ void select_token(const float2* __restrict__ sc_row, int E, int K, float topp, int norm_topk,
+                             float routed_scale, int32_t* __restrict__ idx_out, float* __restrict__ w_out,
                              int32_t* __restrict__ nsel_out, int* err) {
   const int lane = threadIdx.x & 31;
-  float cv[EPL];
+  uint32_t key[EPL];
+  float sv[EPL];
   unsigned taken = 0;  // bit i: expert lane + 32 i already chosen (or absent)
   bool bad = false;
 #pragma unroll
   for (int i = 0; i < EPL; i++) {
-    int e = lane + 32 * i;
+    const int e = lane + 32 * i;
     if (e < E) {
-      cv[i] = ld_cg_f32(c_row + e);
-      if (!isfinite(cv[i])) bad = true;
+      const float2 v = __ldcg(sc_row + e);  // (score, choice)
+      if (!isfinite(v.x) || !isfinite(v.y)) bad = true;
+      key[i] = order_key(v.y);
+      sv[i] = v.x;
     } else {
-      cv[i] = 0.f;
+      key[i] = 0;
+      sv[i] = 0.f;
       taken |= 1u << i;
     }
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(err, COLI_E_NONFINITE);
-  int mine = -1;  // lane k keeps the expert chosen in round k
+  int mine = -1;      // lane k keeps the expert chosen in round k ...
+  float wmine = 0.f;  // ... and its raw score
   for (int k = 0; k < K; k++) {
-    float best = 0.f;
-    int besti = -1;
+    uint32_t bk = 0;
+    int bi = -1;
+    float bs = 0.f;
 #pragma unroll
     for (int i = 0; i < EPL; i++) {
-      if (!(taken & (1u << i)) && (besti < 0 || cv[i] > best)) {
-        best = cv[i];
-        besti = lane + 32 * i;
+      if (!(taken & (1u << i)) && (bi < 0 || key[i] > bk)) {
+        bk = key[i];
+        bi = i;
+        bs = sv[i];
       }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      float ob = __shfl_xor_sync(0xffffffffu, best, off);
-      int oi = __shfl_xor_sync(0xffffffffu, besti, off);
-      bool take = oi >= 0 && (besti < 0 || ob > best || (ob == best && oi < besti));
-      if (take) {
-        best = ob;
-        besti = oi;
-      }
+    const uint32_t best = __reduce_max_sync(0xffffffffu, bi >= 0 ? bk : 0u);
+    const uint32_t cand = (bi >= 0 && bk == best) ? (uint32_t)(lane + 32 * bi) : 0xffffffffu;
+    const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+    const float ws = __shfl_sync(0xffffffffu, bs, win & 31);
+    if ((int)(win & 31) == lane) taken |= 1u << (win >> 5);
+    if (lane == k) {
+      mine = (int)win;
+      wmine = ws;
     }
-    if (besti >= 0 && (besti & 31) == lane) taken |= 1u << (besti >> 5);
-    if (lane == k) mine = besti;
   }
   // weights from the raw (bias-free) score; every sum in slot order in binary32, no contraction
-  const float wmine = (lane < K && mine >= 0) ? ld_cg_f32(s_row + mine) : 0.f;
   int m = K;
   float denom = 1.f;
   float total = 0.f;
@@ -84,7 +95,7 @@ __device__ void select_token(const float* __restrict__ c_row, const float* __res
   }
   if (lane < K) {
     const bool kept = lane < m;
-    float wv = norm_topk ? __fdiv_rn(wmine, denom) : wmine;
+    const float wv = norm_topk ? __fdiv_rn(wmine, denom) : wmine;
     idx_out[lane] = kept ? mine : -1;
     w_out[lane] = kept ? __fmul_rn(wv, routed_scale) : 0.f;
   }
@@ -92,12 +103,12 @@ __device__ void select_token(const float* __restrict__ c_row, const float* __res
 }
 
 template <int EPL>
-__device__ void select_all(const float* s, const float* c, int S, int E, int K, float topp, int norm_topk,
-                           float routed_scale, int32_t* idx, float* w, int32_t* n_sel, int* err) {
+__device__ void select_all(const float2* sc, int S, int E, int K, float topp, int norm_topk, float routed_scale,
+                           int32_t* idx, float* w, int32_t* n_sel, int* err) {
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   for (int t = warp; t < S; t += nwarps)
-    select_token<EPL>(c + (size_t)t * E, s + (size_t)t * E, E, K, topp, norm_topk, routed_scale,
-                      idx + (size_t)t * K, w + (size_t)t * K, n_sel ? n_sel + t : nullptr, err);
+    select_token<EPL>(sc + (size_t)t * E, E, K, topp, norm_topk, routed_scale, idx + (size_t)t * K, w + (size_t)t * K,
+                      n_sel ? n_sel + t : nullptr, err);
 }
 
 // Logits GEMV: CTA b computes rows e = b * kRowsPerCta + r (r < kRowsPerCta) for every token;
@@ -107,7 +118,7 @@ template <bool VEC4>
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(
     const void* __restrict__ x, int x_dtype, int S, int D, const float* __restrict__ Wr,
     const float* __restrict__ bias, int E, int K, float topp, int norm_topk, float routed_scale,
-    float* __restrict__ s_ws, float* __restrict__ c_ws, int32_t* __restrict__ idx, float* __restrict__ w,
+    float2* __restrict__ sc_ws, int32_t* __restrict__ idx, float* __restrict__ w,
     int32_t* __restrict__ n_sel, int* __restrict__ status, int epl) {
   __shared__ float red[kRouterThreads / 32][kRowsPerCta];
   __shared__ int am_last;
@@ -158,8 +169,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(
       const int e = e0 + tid;
       const float sc = 1.0f / (1.0f + expf(-z));
       const float ch = bias ? __fadd_rn(sc, __ldg(bias + e)) : sc;
-      s_ws[(size_t)t * E + e] = sc;
-      c_ws[(size_t)t * E + e] = ch;
+      sc_ws[(size_t)t * E + e] = make_float2(sc, ch);
     }
     __syncthreads();
   }
@@ -173,12 +183,12 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(
   if (!am_last) return;
   __threadfence();
   switch (epl) {
-    case 1: select_all<1>(s_ws, c_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
-    case 2: select_all<2>(s_ws, c_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
-    case 4: select_all<4>(s_ws, c_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
-    case 8: select_all<8>(s_ws, c_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
-    case 16: select_all<16>(s_ws, c_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
-    default: select_all<32>(s_ws, c_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
+    case 1: select_all<1>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
+    case 2: select_all<2>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
+    case 4: select_all<4>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
+    case 8: select_all<8>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
+    case 16: select_all<16>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
+    default: select_all<32>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
   }
   __syncthreads();
   if (tid == 0) atomicExch(reinterpret_cast<unsigned*>(status + 1), 0u);
@@ -187,11 +197,9 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(
 int launch_router(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr, const float* bias,
                   int E, int K, float topp, int norm_topk, float routed_scale, int32_t* idx, float* w,
                   int32_t* n_sel) {
-  size_t half = align_up((size_t)S * E * sizeof(float), 256);
-  int rc = ensure_workspace(ctx, 2 * half);
+  int rc = ensure_workspace(ctx, align_up((size_t)S * E * sizeof(float2), 256));
   if (rc != COLI_OK) return rc;
-  float* s_ws = reinterpret_cast<float*>(ctx->ws.base);
-  float* c_ws = reinterpret_cast<float*>(ctx->ws.base + half);
+  float2* sc_ws = reinterpret_cast<float2*>(ctx->ws.base);
   int epl = 1;
   while (32 * epl < E) epl *= 2;
   bool vec4 = (D % 4 == 0) && ((reinterpret_cast<uintptr_t>(Wr) & 15) == 0) &&
@@ -209,9 +217,9 @@ int launch_router(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const
   cfg.numAttrs = 1;
   const void* xp = x;
   cudaError_t le = vec4 ? cudaLaunchKernelEx(&cfg, router_kernel<true>, xp, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk,
-                                             routed_scale, s_ws, c_ws, idx, w, n_sel, ctx->d_status, epl)
+                                             routed_scale, sc_ws, idx, w, n_sel, ctx->d_status, epl)
                         : cudaLaunchKernelEx(&cfg, router_kernel<false>, xp, x_dtype, S, D, Wr, bias, E, K, topp,
-                                             norm_topk, routed_scale, s_ws, c_ws, idx, w, n_sel, ctx->d_status, epl);
+                                             norm_topk, routed_scale, sc_ws, idx, w, n_sel, ctx->d_status, epl);
   if (le != cudaSuccess) return cuda_fail(ctx, le, "router launch");
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(ctx, e, "router launch");

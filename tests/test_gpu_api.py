@@ -9,7 +9,7 @@ import torch
 from int4_grouped_expert_router_gb300 import binding as B
 from int4_grouped_expert_router_gb300 import synth
 from int4_grouped_expert_router_gb300.workload import DeviceLayer, LayerConfig, router_host_inputs
-from gpu_util import F32_ATOL, F32_RTOL, Ctx, assert_close, ffn_reference, to_np
+from gpu_util import F32_ATOL, F32_RTOL, Ctx, f32_atol, assert_close, ffn_reference, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -53,7 +53,7 @@ def test_upload_copies_host_data(ctx):
     from workload_helpers import oracle_for_layer_seed
     ref = oracle_for_layer_seed(cfg, x, idx, w)
     for y in outs:
-        assert_close(to_np(y), ref, F32_RTOL, F32_ATOL, "after host scribble")
+        assert_close(to_np(y), ref, F32_RTOL, f32_atol(ref), "after host scribble")
 
 
 def test_upload_from_device_memory(ctx):
@@ -137,6 +137,6 @@ def test_healthy_call_after_failed_allocation(ctx):
         layer.step(layer.act_tensor(x), layer.act_tensor(resid), out)
         assert B.coli_check_error(ctx) == 0
         ref = ffn_reference(cfg, x, to_np(out["idx"]), to_np(out["w"]), to_np(out["n_sel"]), resid)
-        assert_close(to_np(out["y"]), ref, F32_RTOL, F32_ATOL, "after failed alloc")
+        assert_close(to_np(out["y"]), ref, F32_RTOL, f32_atol(ref), "after failed alloc")
     finally:
         layer.free()

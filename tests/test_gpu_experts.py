@@ -7,7 +7,7 @@ import oracle.moe as O
 from int4_grouped_expert_router_gb300 import binding as B
 from int4_grouped_expert_router_gb300 import synth
 from int4_grouped_expert_router_gb300.workload import CONFIGS, DeviceLayer, LayerConfig, router_host_inputs
-from gpu_util import BF16_RTOL, F32_ATOL, F32_RTOL, Ctx, assert_close, check_router, ffn_reference, to_np
+from gpu_util import BF16_RTOL, F32_ATOL, F32_RTOL, Ctx, bf16_atol, f32_atol, assert_close, check_router, ffn_reference, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -34,8 +34,8 @@ def run_layer(ctx, cfg, token0=0, with_resid=True):
         layer.free()
 
 
-def tol(cfg):
-    return (BF16_RTOL, BF16_RTOL * 1e-2) if cfg.x_dtype == "bf16" else (F32_RTOL, F32_ATOL)
+def tol(cfg, ref):
+    return (BF16_RTOL, bf16_atol(ref)) if cfg.x_dtype == "bf16" else (F32_RTOL, f32_atol(ref))
 
 
 @pytest.mark.parametrize("cfg", [
@@ -58,7 +58,7 @@ def tol(cfg):
 def test_layer_matches_oracle(ctx, cfg):
     y, ref, near = run_layer(ctx, cfg, with_resid=cfg.name != "tiny-noresid")
     assert near == 0
-    rtol, atol = tol(cfg)
+    rtol, atol = tol(cfg, ref)
     stats = assert_close(y, ref, rtol, atol, cfg.name)
     print(cfg.name, stats)
 
@@ -76,7 +76,7 @@ def test_given_routes_including_dropped_slots(ctx):
                             torch.from_numpy(n).cuda(), cfg.K, layer.act_tensor(resid), y)
         assert B.coli_check_error(ctx) == 0
         ref = ffn_reference(cfg, x, idx, w, n, resid)
-        assert_close(to_np(y), ref, F32_RTOL, F32_ATOL, "given routes")
+        assert_close(to_np(y), ref, F32_RTOL, f32_atol(ref), "given routes")
         # n_sel NULL means every slot is kept
         idx2 = np.array([[1, 4, 5, 6], [0, 1, 2, 3]], np.int32)
         y2 = torch.empty(2, cfg.D, device="cuda")
@@ -84,7 +84,7 @@ def test_given_routes_including_dropped_slots(ctx):
                             cfg.K, None, y2)
         assert B.coli_check_error(ctx) == 0
         ref2 = ffn_reference(cfg, x, idx2, w, np.array([4, 4]), None)
-        assert_close(to_np(y2), ref2, F32_RTOL, F32_ATOL, "n_sel NULL")
+        assert_close(to_np(y2), ref2, F32_RTOL, f32_atol(ref2), "n_sel NULL")
     finally:
         layer.free()
 
@@ -112,7 +112,7 @@ def test_exact_integer_sums(ctx):
         assert B.coli_check_error(ctx) == 0
         yo = to_np(y)[0]
         ref = ffn_reference_single(pg, sg, pu, su, pd, sd, D, I, xi[0])
-        assert_close(yo, ref, F32_RTOL, F32_ATOL, "exact-integer")
+        assert_close(yo, ref, F32_RTOL, f32_atol(ref), "exact-integer")
         assert np.all(yo[I:] == 0.0)
     finally:
         B.coli_expert_table_set(ctx, 0, 0, 0, 0)
@@ -135,7 +135,7 @@ def test_activation_outliers_dense_weights(ctx):
                             cfg.K, layer.act_tensor(resid), y)
         assert B.coli_check_error(ctx) == 0
         ref = ffn_reference(cfg, x, idx, w, np.array([4]), resid)
-        print("outliers", assert_close(to_np(y), ref, F32_RTOL, F32_ATOL, "outliers"))
+        print("outliers", assert_close(to_np(y), ref, F32_RTOL, f32_atol(ref), "outliers"))
     finally:
         layer.free()
 

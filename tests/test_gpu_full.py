@@ -5,7 +5,7 @@ import pytest
 
 from int4_grouped_expert_router_gb300 import binding as B
 from int4_grouped_expert_router_gb300.workload import CONFIGS, DeviceLayer, router_host_inputs
-from gpu_util import BF16_RTOL, F32_ATOL, F32_RTOL, Ctx, assert_close, check_router, ffn_reference, to_np
+from gpu_util import BF16_RTOL, F32_ATOL, F32_RTOL, Ctx, bf16_atol, f32_atol, assert_close, check_router, ffn_reference, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -32,9 +32,9 @@ def test_full_shape_layer(ctx, name, tokens):
             near, werr = check_router(idx, w, n, x, Wr, bias, cfg.K, cfg.topp, cfg.norm_topk, cfg.routed_scale)
             ref = ffn_reference(cfg, x, idx, w, n, resid)
             if cfg.x_dtype == "bf16":
-                stats = assert_close(y, ref, BF16_RTOL, BF16_RTOL * 1e-2, name)
+                stats = assert_close(y, ref, BF16_RTOL, bf16_atol(ref), name)
             else:
-                stats = assert_close(y, ref, F32_RTOL, F32_ATOL, name)
+                stats = assert_close(y, ref, F32_RTOL, f32_atol(ref), name)
             print(name, tok, "near-ties", near, "distinct", len(set(idx[idx >= 0].tolist())), stats)
             assert near <= 1
     finally:
