@@ -125,6 +125,26 @@ COLI_API int coli_router_select(coli_ctx *ctx, const void *x, int x_dtype, int S
                        int norm_topk, float routed_scale, int32_t *idx, float *w, int32_t *n_sel);
 
 /*
+ * Same computation, arguments, outputs and error behaviour as coli_router_select, but the call
+ * allocates nothing: no cudaMalloc or cudaFree and no allocating library call, whatever the size.
+ * The router's pages have no counterpart for this entry; it serves callers that cannot let a call
+ * allocate: a server that has given all free device memory to its own caching pool, or a decode
+ * loop that cannot take the stall of cudaMalloc (which may synchronise the device) or of a
+ * workspace that grows (which first waits for the context's stream).
+ *   - Scratch: a fixed device array of the library, one per device, holding the (score, choice)
+ *     pairs of at most 65536 (token, expert) cells; S * E above that returns COLI_E_INVAL.
+ *   - The first call on a device looks up that array's address (a CUDA symbol query with the
+ *     context's device current); make that first call before any stream capture.
+ *   - The array's arrival counter is cleared on the context's stream before each launch.
+ *   - All contexts on a device share the array: calls whose kernels may run at the same time
+ *     (different streams, contexts or unordered host threads) race on it and give wrong results.
+ *   - Not covered by coli_profile_enable's per-kernel timing.
+ */
+COLI_API int coli_router_select_noalloc(coli_ctx *ctx, const void *x, int x_dtype, int S, int D,
+                       const float *Wr, const float *bias, int E, int K, float topp,
+                       int norm_topk, float routed_scale, int32_t *idx, float *w, int32_t *n_sel);
+
+/*
  * Upload one int4 weight tensor W [O x I], [g4]:
  *   packed: O rows of ceil(I/2) bytes; byte m of a row holds column 2m in its low nibble and
  *           column 2m+1 in its high nibble; the stored nibble n means the value n - 8.

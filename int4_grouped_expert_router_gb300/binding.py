@@ -56,6 +56,7 @@ SIGNATURES = {
     "coli_check_error": (_I, [_P]),
     "coli_reserve": (_I, [_P, _I, _I, _I, _I, _I]),
     "coli_router_select": (_I, [_P, _P, _I, _I, _I, _P, _P, _I, _I, _F, _I, _F, _P, _P, _P]),
+    "coli_router_select_noalloc": (_I, [_P, _P, _I, _I, _I, _P, _P, _I, _I, _F, _I, _F, _P, _P, _P]),
     "coli_expert_upload": (_U64, [_P, _P, _P, _I, _I, _I]),
     "coli_expert_free": (_I, [_P, _U64]),
     "coli_expert_table_set": (_I, [_P, _I, _U64, _U64, _U64]),
@@ -160,7 +161,7 @@ def coli_reserve(ctx, max_S, max_E, max_K, max_D, max_I):
     return _check(ctx, library().coli_reserve(ctx, max_S, max_E, max_K, max_D, max_I), "coli_reserve")
 
 
-def coli_router_select(ctx, x, Wr, bias, K, topp, norm_topk, routed_scale, idx, w, n_sel=None):
+def _router_args(x, Wr, bias, K, idx, w, n_sel):
     S, D = x.shape
     E = Wr.shape[0]
     _dev(x, name="x")
@@ -173,9 +174,23 @@ def coli_router_select(ctx, x, Wr, bias, K, topp, norm_topk, routed_scale, idx, 
         raise ValueError("router_select: inconsistent shapes")
     if bias is not None and bias.numel() != E:
         raise ValueError("router_select: bias must have E entries")
+    return S, D, E
+
+
+def coli_router_select(ctx, x, Wr, bias, K, topp, norm_topk, routed_scale, idx, w, n_sel=None):
+    S, D, E = _router_args(x, Wr, bias, K, idx, w, n_sel)
     rc = library().coli_router_select(ctx, _ptr(x), act_dtype(x), S, D, _ptr(Wr), _ptr(bias), E, K, float(topp),
                                       int(bool(norm_topk)), float(routed_scale), _ptr(idx), _ptr(w), _ptr(n_sel))
     return _check(ctx, rc, "coli_router_select")
+
+
+def coli_router_select_noalloc(ctx, x, Wr, bias, K, topp, norm_topk, routed_scale, idx, w, n_sel=None):
+    """coli_router_select with the library's fixed device scratch (S * E <= 65536): allocates nothing."""
+    S, D, E = _router_args(x, Wr, bias, K, idx, w, n_sel)
+    rc = library().coli_router_select_noalloc(ctx, _ptr(x), act_dtype(x), S, D, _ptr(Wr), _ptr(bias), E, K,
+                                              float(topp), int(bool(norm_topk)), float(routed_scale), _ptr(idx),
+                                              _ptr(w), _ptr(n_sel))
+    return _check(ctx, rc, "coli_router_select_noalloc")
 
 
 def coli_expert_upload(ctx, packed, scales, O, I, gs):

@@ -412,6 +412,22 @@ int coli_router_select(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, 
   return rc;
 }
 
+int coli_router_select_noalloc(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr,
+                               const float* bias, int E, int K, float topp, int norm_topk, float routed_scale,
+                               int32_t* idx, float* w, int32_t* n_sel) {
+  if (!ctx) return COLI_E_INVAL;
+  if (!x || !Wr || !idx || !w) return fail(ctx, COLI_E_INVAL, "router_noalloc: NULL pointer");
+  if (x_dtype != COLI_DTYPE_F32 && x_dtype != COLI_DTYPE_BF16) return fail(ctx, COLI_E_INVAL, "router_noalloc: dtype");
+  if (S < 1 || S > COLI_MAX_TOKENS || D < 1 || D > COLI_MAX_DIM || E < 1 || E > COLI_MAX_EXPERTS || K < 1 ||
+      K > COLI_MAX_K || K > E)
+    return fail(ctx, COLI_E_INVAL, "router_noalloc: size out of range");
+  if (injected(ctx)) return COLI_E_INJECTED;
+  cudaSetDevice(ctx->device);
+  int rc = launch_router_noalloc(ctx, x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk, routed_scale, idx, w, n_sel);
+  if (rc == COLI_OK) ctx->compute_calls++;
+  return rc;
+}
+
 int coli_expert_group(coli_ctx* ctx, const void* x_rows, int x_dtype, int S, const int32_t* idx,
                       const float* w, const int32_t* n_sel, int K, const void* resid, void* y) {
   if (!ctx) return COLI_E_INVAL;

@@ -123,6 +123,9 @@ struct ProfScope {
 int launch_router(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr,
                   const float* bias, int E, int K, float topp, int norm_topk, float routed_scale,
                   int32_t* idx, float* w, int32_t* n_sel);
+int launch_router_noalloc(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr,
+                          const float* bias, int E, int K, float topp, int norm_topk, float routed_scale,
+                          int32_t* idx, float* w, int32_t* n_sel);
 int launch_expert_group(coli_ctx* ctx, const void* x, int x_dtype, int S, const int32_t* idx,
                         const float* w, const int32_t* n_sel, int K, const void* resid, void* y);
 

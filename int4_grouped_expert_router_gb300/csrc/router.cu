@@ -6,6 +6,9 @@
 // strict '>' tie-break, weights from the raw score, route-level TOPP truncation, norm_topk and
 // routed_scale. For S > 1 the logits of all tokens come from one launch (the batched router of
 // the "GPU resident pipeline" commit).
+#include <mutex>
+#include <string>
+
 #include "coli_internal.h"
 #include "pipe.h"
 
@@ -114,12 +117,15 @@ __device__ void select_all(const float2* sc, int S, int E, int K, float topp, in
 // Logits GEMV: CTA b computes rows e = b * kRowsPerCta + r (r < kRowsPerCta) for every token;
 // thread t accumulates columns t, t + kRouterThreads, ... (float4 when aligned) for all rows at
 // once, so all of a row group's loads are in flight together.
+// `status` is the context's error word; `arrivals` counts the CTAs that have stored their scores
+// (zero on entry, reset to zero by the CTA that finishes last).
 template <bool VEC4>
-__global__ void __launch_bounds__(kRouterThreads) router_kernel(
-    const void* __restrict__ x, int x_dtype, int S, int D, const float* __restrict__ Wr,
-    const float* __restrict__ bias, int E, int K, float topp, int norm_topk, float routed_scale,
-    float2* __restrict__ sc_ws, int32_t* __restrict__ idx, float* __restrict__ w,
-    int32_t* __restrict__ n_sel, int* __restrict__ status, int epl) {
+__device__ __forceinline__ void router_body(const void* __restrict__ x, int x_dtype, int S, int D,
+                                            const float* __restrict__ Wr, const float* __restrict__ bias, int E,
+                                            int K, float topp, int norm_topk, float routed_scale,
+                                            float2* __restrict__ sc_ws, int32_t* __restrict__ idx,
+                                            float* __restrict__ w, int32_t* __restrict__ n_sel,
+                                            int* __restrict__ status, unsigned* arrivals, int epl) {
   __shared__ float red[kRouterThreads / 32][kRowsPerCta];
   __shared__ int am_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -176,7 +182,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(
   // The CTA that finishes last runs the selection over every token's complete score row.
   if (tid == 0) {
     __threadfence();
-    unsigned prev = atomicAdd(reinterpret_cast<unsigned*>(status + 1), 1u);
+    unsigned prev = atomicAdd(arrivals, 1u);
     am_last = prev == gridDim.x - 1;
   }
   __syncthreads();
@@ -191,7 +197,27 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(
     default: select_all<32>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
   }
   __syncthreads();
-  if (tid == 0) atomicExch(reinterpret_cast<unsigned*>(status + 1), 0u);
+  if (tid == 0) atomicExch(arrivals, 0u);
+}
+
+template <bool VEC4>
+__global__ void __launch_bounds__(kRouterThreads) router_kernel(
+    const void* __restrict__ x, int x_dtype, int S, int D, const float* __restrict__ Wr,
+    const float* __restrict__ bias, int E, int K, float topp, int norm_topk, float routed_scale,
+    float2* __restrict__ sc_ws, int32_t* __restrict__ idx, float* __restrict__ w,
+    int32_t* __restrict__ n_sel, int* __restrict__ status, int epl) {
+  router_body<VEC4>(x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk, routed_scale, sc_ws, idx, w, n_sel, status,
+                    reinterpret_cast<unsigned*>(status + 1), epl);
+}
+
+template <bool VEC4>
+__global__ void __launch_bounds__(kRouterThreads) router_fixed_kernel(
+    const void* __restrict__ x, int x_dtype, int S, int D, const float* __restrict__ Wr,
+    const float* __restrict__ bias, int E, int K, float topp, int norm_topk, float routed_scale,
+    float2* __restrict__ sc_ws, int32_t* __restrict__ idx, float* __restrict__ w,
+    int32_t* __restrict__ n_sel, int* __restrict__ status, unsigned* arrivals, int epl) {
+  router_body<VEC4>(x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk, routed_scale, sc_ws, idx, w, n_sel, status,
+                    arrivals, epl);
 }
 
 int launch_router(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr, const float* bias,
@@ -223,6 +249,77 @@ int launch_router(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const
   if (le != cudaSuccess) return cuda_fail(ctx, le, "router launch");
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(ctx, e, "router launch");
+  return COLI_OK;
+}
+
+// ------------------------------------------------------------------------------------------
+// Router entry that allocates nothing (coli_router_select_noalloc).
+//
+// Some callers cannot let a call allocate device memory: a server that has handed all free HBM to
+// its own caching pool (a cudaMalloc would fail or force it to evict), or a decode loop that must
+// not stall, since cudaMalloc may synchronise the device and a workspace that grows waits for the
+// context's stream first. This entry therefore keeps its scratch in a fixed file-scope device
+// array instead of the context's workspace: the arrival counter in the first 256 bytes, then the
+// (score, choice) pairs of at most kFixedRouterCells (token, expert) cells. Its address is looked
+// up once per device (the first call on that device); the counter is cleared on the stream before
+// every launch. All contexts on a device share the array, so calls whose kernels could overlap
+// (different streams, contexts or host threads without ordering) race on it.
+// ------------------------------------------------------------------------------------------
+
+constexpr int kFixedRouterCells = 65536;  // S * E limit: 512 KiB of pairs
+constexpr int kFixedMaxDevices = 64;
+static __device__ __align__(256) unsigned char g_router_fixed[256 + (size_t)kFixedRouterCells * sizeof(float2)];
+
+static std::mutex g_fixed_mu;
+static unsigned char* g_fixed_addr[kFixedMaxDevices];  // device address of g_router_fixed, once set up
+
+int launch_router_noalloc(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr,
+                          const float* bias, int E, int K, float topp, int norm_topk, float routed_scale,
+                          int32_t* idx, float* w, int32_t* n_sel) {
+  if ((long long)S * E > kFixedRouterCells)
+    return fail(ctx, COLI_E_INVAL,
+                "router_select_noalloc: S * E = " + std::to_string((long long)S * E) + " exceeds the fixed scratch limit " +
+                    std::to_string(kFixedRouterCells));
+  if (ctx->device < 0 || ctx->device >= kFixedMaxDevices)
+    return fail(ctx, COLI_E_INVAL, "router_select_noalloc: device ordinal beyond the fixed scratch table");
+  unsigned char* base;
+  {
+    std::lock_guard<std::mutex> lock(g_fixed_mu);
+    base = g_fixed_addr[ctx->device];
+    if (!base) {  // the caller has made ctx->device current
+      void* p = nullptr;
+      cudaError_t e = cudaGetSymbolAddress(&p, g_router_fixed);
+      if (e != cudaSuccess || !p) return cuda_fail(ctx, e != cudaSuccess ? e : cudaErrorInvalidSymbol, "router_select_noalloc: scratch address");
+      base = static_cast<unsigned char*>(p);
+      g_fixed_addr[ctx->device] = base;
+    }
+  }
+  unsigned* arrivals = reinterpret_cast<unsigned*>(base);
+  float2* sc_ws = reinterpret_cast<float2*>(base + 256);
+  cudaError_t e = cudaMemsetAsync(arrivals, 0, sizeof(unsigned), ctx->stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "router_select_noalloc: clear counter");
+  int epl = 1;
+  while (32 * epl < E) epl *= 2;
+  const bool vec4 = (D % 4 == 0) && ((reinterpret_cast<uintptr_t>(Wr) & 15) == 0) &&
+                    ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
+  const int grid = (E + kRowsPerCta - 1) / kRowsPerCta;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kRouterThreads);
+  cfg.stream = ctx->stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const void* xp = x;
+  e = vec4 ? cudaLaunchKernelEx(&cfg, router_fixed_kernel<true>, xp, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk,
+                                routed_scale, sc_ws, idx, w, n_sel, ctx->d_status, arrivals, epl)
+           : cudaLaunchKernelEx(&cfg, router_fixed_kernel<false>, xp, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk,
+                                routed_scale, sc_ws, idx, w, n_sel, ctx->d_status, arrivals, epl);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "router_select_noalloc launch");
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "router_select_noalloc launch");
   return COLI_OK;
 }
 
