@@ -10,13 +10,13 @@
 //
 // Dot-product arithmetic. A thread owns one 16-byte chunk of a weight row (32 columns) and keeps
 // the matching 32 activations in registers in block-fixed-point form: the chunk is scaled by a
-// power of two 2^q so that its largest magnitude lies in [2^29, 2^30), rounded to integers and
-// split into four balanced signed bytes (x = l3 2^24 + l2 2^16 + l1 2^8 + l0). The nibble-by-limb
+// power of two 2^q so that its largest magnitude lies in [2^21, 2^22), rounded to integers and
+// split into three balanced signed bytes (x = l2 2^16 + l1 2^8 + l0). The nibble-by-limb
 // products are then summed exactly in 32-bit integers with dp4a (four products per
-// instruction), the offset 8 is removed through a precomputed -8 * sum(l), and the four exact
-// limb sums are combined in binary32 and scaled back by 2^-q. The chunk result therefore differs
-// from the exact dot product of the given activations by at most one rounding of the final sum
-// plus the activation quantisation (below 2^-30 of the chunk's largest activation, per column).
+// instruction), the offset 8 is removed through a precomputed -8 * sum(l), and the exact limb
+// sums are combined in binary32 and scaled back by 2^-q. The chunk result therefore differs from
+// the exact dot product of the given activations by two roundings of binary32 plus the
+// activation quantisation: at most 2^-22 of the chunk's largest activation, per column.
 // Chunk results are summed across the warp by a butterfly and across warps in a fixed order.
 #include "coli_internal.h"
 #include "pipe.h"
@@ -28,10 +28,10 @@ namespace coli {
 // ------------------------------------------------------------------------------------------
 
 struct Limbs {
-  uint32_t r[4][2][4];  // [32-bit word of the chunk][even/odd columns][limb]: 4 bytes each
-  int32_t a0[4];        // even-column accumulator start: -8 * sum over the even columns of limb l
-  int32_t b0[4];        // odd-column accumulator start: -128 * sum over the odd columns of limb l
-  float k01, k23;       // 2^(-q-4) and 2^(16-q-4)
+  uint32_t r[4][2][3];  // [32-bit word of the chunk][even/odd columns][limb]: 4 bytes each
+  int32_t a0[3];        // even-column accumulator start: -8 * sum over the even columns of limb l
+  int32_t b0[3];        // odd-column accumulator start: -128 * sum over the odd columns of limb l
+  float k01, k2;        // 2^(-q-4) and 2^(16-q-4)
 };
 
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
@@ -40,76 +40,80 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
   return d;
 }
 
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
 // v[j] = activation of column 32 c + j (0 beyond the matrix). Returns false if any is not finite.
+// Balanced base-256 digits: for |X| < 2^23 - 2^15 the bytes of Y = X + 0x808080 are the digits
+// l_k + 128 (each in [0, 255], so no carries), hence the bytes of Y ^ 0x808080 are the signed
+// digits l_0, l_1, l_2 with X = l_2 2^16 + l_1 2^8 + l_0.
 __device__ __forceinline__ bool make_limbs(const float (&v)[32], Limbs& L) {
-  float M = 0.f;
-  bool finite = true;
+  float M = 0.f, nan_probe = 0.f;
 #pragma unroll
   for (int j = 0; j < 32; j++) {
-    float a = fabsf(v[j]);
-    finite = finite && (a <= 3.402823466e38f);
-    M = fmaxf(M, a);
+    M = fmaxf(M, fabsf(v[j]));
+    nan_probe = fmaf(v[j], 0.f, nan_probe);  // NaN once any v is NaN or infinite
   }
+  const bool finite = nan_probe == 0.f;
+  int e = 0;
+  if (finite && M > 0.f) frexpf(M, &e);  // M < 2^e
+  int q = 22 - e;                         // M 2^q in [2^21, 2^22)
+  q = q > 122 ? 122 : q;                  // 2^(-q-4) stays a normal float (|x| < 2^-100 only)
+  const float scale = (finite && M > 0.f) ? __int_as_float((127 + q) << 23) : 0.f;  // 2^q, q in [-107, 122]
+  uint32_t z[32];
+#pragma unroll
+  for (int j = 0; j < 32; j++) {
+    const int xi = __float2int_rn(v[j] * scale);  // exact scaling by a power of two; |xi| <= 2^22
+    z[j] = ((uint32_t)xi + 0x808080u) ^ 0x808080u;
+  }
+  // word w, parity p, limb l: byte b is limb l of column 8 w + 2 b + p
 #pragma unroll
   for (int w = 0; w < 4; w++)
 #pragma unroll
-    for (int p = 0; p < 2; p++)
-#pragma unroll
-      for (int l = 0; l < 4; l++) L.r[w][p][l] = 0u;
-#pragma unroll
-  for (int l = 0; l < 4; l++) {
-    L.a0[l] = 0;
-    L.b0[l] = 0;
-  }
-  if (!finite || M == 0.f) {
-    L.k01 = 0.f;
-    L.k23 = 0.f;
-    return finite;
-  }
-  int e;
-  frexpf(M, &e);            // M < 2^e
-  int q = 30 - e;           // M 2^q in [2^29, 2^30)
-  if (q > 122) q = 122;     // keep 2^(-q-4) a normal float (only for |x| < 2^-92)
-#pragma unroll
-  for (int j = 0; j < 32; j++) {
-    int xi = __float2int_rn(ldexpf(v[j], q));
-    int l0 = (int)(int8_t)(xi & 0xff);
-    xi = (xi - l0) >> 8;
-    int l1 = (int)(int8_t)(xi & 0xff);
-    xi = (xi - l1) >> 8;
-    int l2 = (int)(int8_t)(xi & 0xff);
-    int l3 = (xi - l2) >> 8;
-    const int w = j >> 3, p = j & 1, b = (j & 7) >> 1;
-    L.r[w][p][0] |= ((uint32_t)l0 & 0xffu) << (8 * b);
-    L.r[w][p][1] |= ((uint32_t)l1 & 0xffu) << (8 * b);
-    L.r[w][p][2] |= ((uint32_t)l2 & 0xffu) << (8 * b);
-    L.r[w][p][3] |= ((uint32_t)l3 & 0xffu) << (8 * b);
-    if (p == 0) {
-      L.a0[0] -= 8 * l0;
-      L.a0[1] -= 8 * l1;
-      L.a0[2] -= 8 * l2;
-      L.a0[3] -= 8 * l3;
-    } else {
-      L.b0[0] -= 128 * l0;
-      L.b0[1] -= 128 * l1;
-      L.b0[2] -= 128 * l2;
-      L.b0[3] -= 128 * l3;
+    for (int p = 0; p < 2; p++) {
+      const uint32_t z0 = z[8 * w + p], z1 = z[8 * w + 2 + p], z2 = z[8 * w + 4 + p], z3 = z[8 * w + 6 + p];
+      const uint32_t a01 = prmt(z0, z1, 0x5140u);  // z0.b0 z1.b0 z0.b1 z1.b1
+      const uint32_t a23 = prmt(z2, z3, 0x5140u);
+      const uint32_t c01 = prmt(z0, z1, 0x6262u);  // z0.b2 z1.b2 (twice)
+      const uint32_t c23 = prmt(z2, z3, 0x6262u);
+      L.r[w][p][0] = prmt(a01, a23, 0x5410u);
+      L.r[w][p][1] = prmt(a01, a23, 0x7632u);
+      L.r[w][p][2] = prmt(c01, c23, 0x5410u);
     }
+#pragma unroll
+  for (int l = 0; l < 3; l++) {
+    int se = 0, so = 0;
+#pragma unroll
+    for (int w = 0; w < 4; w++) {
+      se = dp4a_ss(L.r[w][0][l], 0x01010101u, se);
+      so = dp4a_ss(L.r[w][1][l], 0x01010101u, so);
+    }
+    L.a0[l] = -8 * se;
+    L.b0[l] = -128 * so;
   }
-  L.k01 = ldexpf(1.0f, -q - 4);
-  L.k23 = ldexpf(1.0f, 16 - q - 4);
-  return true;
+  L.k01 = (finite && M > 0.f) ? __int_as_float((127 - q - 4) << 23) : 0.f;
+  L.k2 = (finite && M > 0.f) ? __int_as_float((127 + 12 - q) << 23) : 0.f;
+  return finite;
 }
 
 // sum_j (n_j - 8) x_j over the 32 columns of one chunk, n_j the stored nibbles in wv.
 // Even columns (low nibbles, w & 0x0f0f0f0f) and odd columns (high nibbles kept in place,
 // w & 0xf0f0f0f0 = 16 n) accumulate in separate dp4a chains; t_l = 16 a_l + b_l is then 16 times
-// the exact limb sum sum_j (n_j - 8) l_j (|t_l| <= 2^19). Limb pairs are joined exactly in 32-bit
-// integers, t_0 + 256 t_1 and t_2 + 256 t_3 (below 2^28), converted once each and scaled by
+// the exact limb sum sum_j (n_j - 8) l_j (|t_l| < 2^19). Limbs 0 and 1 are joined exactly in
+// 32-bit integers, t_0 + 256 t_1 (below 2^28); that and t_2 are converted once each and scaled by
 // powers of two: the result is the dot product with the quantised activations, rounded twice.
 __device__ __forceinline__ float chunk_dot(const uint4 wv, const Limbs& L) {
-  int a0 = L.a0[0], a1 = L.a0[1], a2 = L.a0[2], a3 = L.a0[3];
-  int b0 = L.b0[0], b1 = L.b0[1], b2 = L.b0[2], b3 = L.b0[3];
+  int a0 = L.a0[0], a1 = L.a0[1], a2 = L.a0[2];
+  int b0 = L.b0[0], b1 = L.b0[1], b2 = L.b0[2];
   const uint32_t words[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
   for (int w = 0; w < 4; w++) {
@@ -118,15 +122,13 @@ __device__ __forceinline__ float chunk_dot(const uint4 wv, const Limbs& L) {
     a0 = dp4a_us(lo, L.r[w][0][0], a0);
     a1 = dp4a_us(lo, L.r[w][0][1], a1);
     a2 = dp4a_us(lo, L.r[w][0][2], a2);
-    a3 = dp4a_us(lo, L.r[w][0][3], a3);
     b0 = dp4a_us(hi, L.r[w][1][0], b0);
     b1 = dp4a_us(hi, L.r[w][1][1], b1);
     b2 = dp4a_us(hi, L.r[w][1][2], b2);
-    b3 = dp4a_us(hi, L.r[w][1][3], b3);
   }
-  const int t0 = 16 * a0 + b0, t1 = 16 * a1 + b1, t2 = 16 * a2 + b2, t3 = 16 * a3 + b3;
-  const int p01 = t0 + 256 * t1, p23 = t2 + 256 * t3;
-  return fmaf(__int2float_rn(p23), L.k23, __int2float_rn(p01) * L.k01);
+  const int t0 = 16 * a0 + b0, t1 = 16 * a1 + b1, t2 = 16 * a2 + b2;
+  const int p01 = t0 + 256 * t1;
+  return fmaf(__int2float_rn(t2), L.k2, __int2float_rn(p01) * L.k01);
 }
 
 // Any even gs that is not a multiple of 32: a chunk may cross group boundaries, so each column
@@ -307,6 +309,8 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
 struct SlotTensor {
   const TensorDesc* d;  // in the device expert table (the TMA maps live there)
   const float* s;       // scales
+  const uint8_t* w;     // packed rows
+  uint32_t pitch;       // bytes per packed row
   int mode, G, gs, box_s, box_w, box_rows;
 };
 
@@ -318,6 +322,8 @@ struct RouteSlot {
 __device__ __forceinline__ void fill_slot_tensor(SlotTensor& st, const TensorDesc* d) {
   st.d = d;
   st.s = d->s;
+  st.w = d->w;
+  st.pitch = d->pitch;
   st.mode = d->mode;
   st.G = d->G;
   st.gs = d->gs;
@@ -378,7 +384,14 @@ __device__ __forceinline__ float chunk_dot_slow(const uint4 wv, const Limbs& L, 
 // CTA, at most kSeg) form a finishing segment.
 // ------------------------------------------------------------------------------------------
 
-constexpr int kGUStages = 3;                 // stages per warp ring
+#ifndef COLI_GU_STAGES
+#define COLI_GU_STAGES 3
+#endif
+#ifndef COLI_GU_MIN_CTAS
+#define COLI_GU_MIN_CTAS 2
+#endif
+constexpr int kGUStages = COLI_GU_STAGES;    // stages per warp ring
+constexpr int kGUMinCtas = COLI_GU_MIN_CTAS; // CTAs per SM the register budget is sized for
 
 __device__ const float kOneF = 1.0f;         // stand-in scale for unconditional loads
 
@@ -388,6 +401,8 @@ struct GateUpSmem {
   int e_spec[COLI_MAX_K];          // S == 1: the expert of each slot, read with n_sel
 };
 // followed in dynamic shared memory by the warps' rings, pg[W][kSeg], pu[W][kSeg], pre[S + 1]
+
+static_assert((kBoxRows & (kBoxRows - 1)) == 0, "kBoxRows must be a power of two");
 
 __host__ __device__ constexpr uint32_t gateup_stage_bytes() {
   // gate box + up box (kBoxRows x 512 B each) + two scale boxes (kBoxRows x kScaleBox floats)
@@ -407,7 +422,7 @@ inline size_t gateup_smem_bytes(int W, int S) {
 }
 
 template <int MAXT>
-__global__ void __launch_bounds__(MAXT, MAXT <= 192 ? 2 : 1) gateup_kernel(GroupParams P) {
+__global__ void __launch_bounds__(MAXT, MAXT <= 192 ? kGUMinCtas : 1) gateup_kernel(GroupParams P) {
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem_raw = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 127) & ~uintptr_t(127));
   const int C = (P.D + 31) >> 5;
@@ -473,12 +488,12 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 192 ? 2 : 1) gateup_kernel(Group
     if (!rs.ok) set_error(P.err, COLI_E_ROUTE);
   }
   __syncthreads();
-
   // issue side of this warp's ring: kGUStages batches ahead of the compute (lane 0)
-  int iq = qbeg, ij = j_first, ii = (qbeg - j_first * Bpr) * kBoxRows, issued = 0;
+  int iq = qbeg, ij = j_first, ii = (qbeg - j_first * Bpr) * kBoxRows, istage = 0, issued = 0;
   auto issue_next = [&]() {
-    for (; iq < qend; iq++) {
+    while (iq < qend) {
       const int j = ij, i0 = ii;
+      iq++;
       ii += kBoxRows;
       if (ii >= Bpr * kBoxRows) {
         ii = 0;
@@ -488,8 +503,9 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 192 ? 2 : 1) gateup_kernel(Group
       if (!rs.ok) continue;
       const SlotTensor& g = rs.ts[0];
       const SlotTensor& u = rs.ts[1];
-      uint64_t* bar = &bars[issued % kGUStages];
-      uint8_t* st = ring + (size_t)(issued % kGUStages) * SB;
+      uint64_t* bar = &bars[istage];
+      uint8_t* st = ring + (size_t)istage * SB;
+      istage = istage + 1 == kGUStages ? 0 : istage + 1;
       uint32_t bytes = 2u * g.box_rows * g.box_w * 4;
       if (g.box_s) bytes += g.box_rows * g.box_s * 4;
       if (u.box_s) bytes += u.box_rows * u.box_s * 4;
@@ -501,15 +517,14 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 192 ? 2 : 1) gateup_kernel(Group
       if (u.box_s)
         tma_load_2d(st + 2 * kBoxRows * kSliceWords * 4 + kBoxRows * kScaleBox * 4, &u.d->map_s, u.box_s * warp, i0, bar);
       issued++;
-      iq++;
       return;
     }
   };
   if (lane == 0)
     for (int s = 0; s < kGUStages; s++) issue_next();
 
-  // finaliser thread `tid` (< kSeg) of a segment: where its row pair goes and its row scales,
-  // loaded unconditionally when the segment starts and consumed when it ends
+  // finaliser thread `tid` (< segB kBoxRows) of a segment: where its row pair goes and its row
+  // scales, loaded when the segment starts and consumed when it ends
   float fg = 1.f, fu = 1.f;
   size_t hdst = 0;
   bool fin_ok = false;
@@ -526,93 +541,124 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 192 ? 2 : 1) gateup_kernel(Group
   // ---------------- compute ----------------
   int cur_slot = -1;
   LaneTensor tg, tu;
-  bool stop = false;
-  int cq = 0;  // batches consumed by this warp
-  for (int q = qbeg, j = j_first, i0 = (qbeg - j_first * Bpr) * kBoxRows; q < qend; q++) {
-    if ((q - qbeg) % segB == 0) prefetch_finaliser(q);
-    const int slot = j - j_first;
-    const int n = min(kBoxRows, P.I - i0);
-    const bool rok = sm.routes[slot].ok;
-    if (rok) {
-      if (slot != cur_slot) {
-        cur_slot = slot;
-        const RouteSlot& rs = sm.routes[slot];
-        lane_tensor(tg, rs.ts[0], c);
-        lane_tensor(tu, rs.ts[1], c);
-        if (rs.t != cur_tok) {
-          cur_tok = rs.t;
-          float xv[32];
-          load_chunk_f32(P.x, P.x_dtype, (size_t)cur_tok * P.D, 32 * c, has_chunk ? P.D : 0, xv);
-          if (!make_limbs(xv, L) && has_chunk) set_error(P.err, COLI_E_NONFINITE);
-        }
-      }
-      const bool ok = !stop && mbar_wait(&bars[cq % kGUStages], (cq / kGUStages) & 1);
-      const uint8_t* st = ring + (size_t)(cq % kGUStages) * SB;
-      const uint8_t* sgb = st + 2 * kBoxRows * kSliceWords * 4;
-      float acc[2 * kBoxRows];  // gate rows 0..3, then up rows 0..3
-      if (ok && has_chunk && tg.fast && tu.fast) {
-#pragma unroll
-        for (int u = 0; u < kBoxRows; u++) {
-          float dg = chunk_dot(lds128(st + u * tg.rowB + 16 * lane), L);
-          float du = chunk_dot(lds128(st + kBoxRows * kSliceWords * 4 + u * tu.rowB + 16 * lane), L);
-          if (tg.box_s) dg *= lds32f(sgb + (u * tg.box_s + tg.cg - tg.box_s * warp) * 4);
-          if (tu.box_s) du *= lds32f(sgb + kBoxRows * kScaleBox * 4 + (u * tu.box_s + tu.cg - tu.box_s * warp) * 4);
-          acc[u] = dg;
-          acc[kBoxRows + u] = du;
-        }
-      } else {
-        float tmp[2 * kBoxRows];  // local memory: the rarely used slow path keeps the code small
-#pragma unroll 1
-        for (int v = 0; v < 2 * kBoxRows; v++) {
-          const int u = v % kBoxRows;
-          const LaneTensor& lt = v < kBoxRows ? tg : tu;
-          float d = 0.f;
-          if (ok && has_chunk && u < n) {
-            const uint4 wv = lds128(st + (v / kBoxRows) * (kBoxRows * kSliceWords * 4) + u * lt.rowB + 16 * lane);
-            if (lt.fast)
-              d = chunk_dot(wv, L) *
-                  (lt.box_s ? lds32f(sgb + (v / kBoxRows) * (kBoxRows * kScaleBox * 4) +
-                                     (u * lt.box_s + lt.cg - lt.box_s * warp) * 4)
-                            : 1.f);
-            else
-              d = chunk_dot_slow(wv, L, lt, P.x, P.x_dtype, (size_t)cur_tok * P.D, i0 + u, c);
+  bool stop = false, row_scales = false;
+  int stage = 0;
+  uint32_t phase = 0;
+  constexpr uint32_t kUpOff = kBoxRows * kSliceWords * 4;  // up box within a stage
+  constexpr uint32_t kScaleOff = 2 * kUpOff;               // gate scale box, then the up scale box
+  int j = j_first, i0 = (qbeg - j_first * Bpr) * kBoxRows;
+  for (int qs = qbeg; qs < qend; qs += segB) {
+    const int qe = min(qs + segB, qend);
+    prefetch_finaliser(qs);
+    for (int q = qs; q < qe; q++) {
+      const int slot = j - j_first;
+      if (sm.routes[slot].ok) {
+        if (slot != cur_slot) {
+          cur_slot = slot;
+          const RouteSlot& rs = sm.routes[slot];
+          lane_tensor(tg, rs.ts[0], c);
+          lane_tensor(tu, rs.ts[1], c);
+          row_scales = tg.fast && tu.fast && !tg.box_s && !tu.box_s;
+          if (rs.t != cur_tok) {
+            cur_tok = rs.t;
+            float xv[32];
+            load_chunk_f32(P.x, P.x_dtype, (size_t)cur_tok * P.D, 32 * c, has_chunk ? P.D : 0, xv);
+            if (!make_limbs(xv, L) && has_chunk) set_error(P.err, COLI_E_NONFINITE);
           }
-          tmp[v] = d;
         }
+        const bool ok = !stop && mbar_wait(&bars[stage], phase);
+        const uint8_t* st = ring + (size_t)stage * SB + 16 * lane;
+        float acc[2 * kBoxRows];  // gate rows 0..3, then up rows 0..3
+        if (ok && has_chunk && row_scales) {
 #pragma unroll
-        for (int v = 0; v < 2 * kBoxRows; v++) acc[v] = tmp[v];
-      }
-      __syncwarp();
-      if (lane == 0 && ok) issue_next();  // refill the stage just consumed
-      if (!ok && !stop) {
-        stop = true;
-        set_error(P.err, COLI_E_TIMEOUT);
-      }
-      cq++;
-      // lane l ends with the warp total of value l / 4: gate row v (v < 4) or up row v - 4
-      warp_transpose_reduce<2 * kBoxRows>(acc, lane);
-      if ((lane & 3) == 0) {
-        const int v = lane >> 2, u = v % kBoxRows;
-        if (u < n) (v < kBoxRows ? pg : pu)[warp * kSeg + ((q - qbeg) % segB) * kBoxRows + u] = acc[0];
-      }
-    }
-    if ((q - qbeg) % segB == segB - 1 || q + 1 == qend) {  // segment end: finish its rows
-      const bool any_stop = named_sync_or(1, W * 32, stop);
-      if (!any_stop && fin_ok) {
-        float g = 0.f, u = 0.f;
-        for (int wi = 0; wi < W; wi++) {
-          g += pg[wi * kSeg + tid];
-          u += pu[wi * kSeg + tid];
+          for (int u = 0; u < kBoxRows; u++) {
+            acc[u] = chunk_dot(lds128(st + u * tg.rowB), L);
+            acc[kBoxRows + u] = chunk_dot(lds128(st + kUpOff + u * tu.rowB), L);
+          }
+        } else if (ok && has_chunk && tg.fast && tu.fast) {
+          const uint8_t* sgb = ring + (size_t)stage * SB + kScaleOff;
+#pragma unroll
+          for (int u = 0; u < kBoxRows; u++) {
+            float dg = chunk_dot(lds128(st + u * tg.rowB), L);
+            float du = chunk_dot(lds128(st + kUpOff + u * tu.rowB), L);
+            if (tg.box_s) dg *= lds32f(sgb + (u * tg.box_s + tg.cg - tg.box_s * warp) * 4);
+            if (tu.box_s) du *= lds32f(sgb + kBoxRows * kScaleBox * 4 + (u * tu.box_s + tu.cg - tu.box_s * warp) * 4);
+            acc[u] = dg;
+            acc[kBoxRows + u] = du;
+          }
+        } else {
+          const uint8_t* sgb = ring + (size_t)stage * SB + kScaleOff;
+          const int n = min(kBoxRows, P.I - i0);
+          float tmp[2 * kBoxRows];  // local memory: the rarely used slow path keeps the code small
+#pragma unroll 1
+          for (int v = 0; v < 2 * kBoxRows; v++) {
+            const int u = v % kBoxRows;
+            const LaneTensor& lt = v < kBoxRows ? tg : tu;
+            float d = 0.f;
+            if (ok && has_chunk && u < n) {
+              const uint4 wv = lds128(st + (v / kBoxRows) * kUpOff + u * lt.rowB);
+              if (lt.fast)
+                d = chunk_dot(wv, L) * (lt.box_s ? lds32f(sgb + (v / kBoxRows) * (kBoxRows * kScaleBox * 4) +
+                                                          (u * lt.box_s + lt.cg - lt.box_s * warp) * 4)
+                                                 : 1.f);
+              else
+                d = chunk_dot_slow(wv, L, lt, P.x, P.x_dtype, (size_t)cur_tok * P.D, i0 + u, c);
+            }
+            tmp[v] = d;
+          }
+#pragma unroll
+          for (int v = 0; v < 2 * kBoxRows; v++) acc[v] = tmp[v];
         }
-        P.h[hdst] = silu_mul(g * fg, u * fu);
+        __syncwarp();
+        if (lane == 0 && ok) issue_next();  // refill the stage just consumed
+        if (!ok && !stop) {
+          stop = true;
+          set_error(P.err, COLI_E_TIMEOUT);
+        }
+        if (++stage == kGUStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        // lane l ends with the warp total of value l / 4: gate row v (v < 4) or up row v - 4.
+        // Box rows at and beyond I (zero-filled by TMA) give values that are never read back.
+        warp_transpose_reduce<2 * kBoxRows>(acc, lane);
+        if ((lane & 3) == 0) {
+          const int v = lane >> 2;
+          (v < kBoxRows ? pg : pu)[warp * kSeg + (q - qs) * kBoxRows + (v & (kBoxRows - 1))] = acc[0];
+        }
       }
-      named_sync(1, W * 32);  // the partial buffers are reused by the next segment
-      if (any_stop) stop = true;
+      i0 += kBoxRows;
+      if (i0 >= Bpr * kBoxRows) {
+        i0 = 0;
+        j++;
+      }
     }
-    i0 += kBoxRows;
-    if (i0 >= Bpr * kBoxRows) {
-      i0 = 0;
-      j++;
+    // segment end: finish its rows
+    const bool any_stop = named_sync_or(1, W * 32, stop);
+    if (!any_stop && fin_ok) {
+      float g = 0.f, u = 0.f;
+      for (int wi = 0; wi < W; wi++) {
+        g += pg[wi * kSeg + tid];
+        u += pu[wi * kSeg + tid];
+      }
+      P.h[hdst] = silu_mul(g * fg, u * fu);
+    }
+    named_sync(1, W * 32);  // the partial buffers are reused by the next segment
+    if (any_stop) stop = true;
+  }
+  // S == 1: this CTA's share of the kept slots' down rows (and scales) goes to L2 for the down
+  // kernel, which starts only when every gate/up CTA has finished.
+  if (P.S == 1 && tid == 0 && !stop) {
+    const long long tot = (long long)R * P.D;
+    const long long a = (long long)blockIdx.x * tot / gridDim.x, b = (long long)(blockIdx.x + 1) * tot / gridDim.x;
+    for (long long j = a / P.D; j < R && j * P.D < b; j++) {
+      const int e = sm.e_spec[j];
+      if (e < 0 || e >= COLI_MAX_EXPERTS) continue;
+      const TensorDesc* td = &P.table[e].t[T_DOWN];
+      if (!P.table[e].valid) continue;
+      const long long r0 = max(a, j * P.D) - j * P.D, r1 = min(b, (j + 1) * P.D) - j * P.D;
+      prefetch_range_l2(td->w + (size_t)r0 * td->pitch, (size_t)(r1 - r0) * td->pitch);
+      prefetch_range_l2(td->s + (size_t)r0 * td->G, (size_t)(r1 - r0) * td->G * sizeof(float));
     }
   }
   // never leave with TMA loads in flight into this warp's ring (the last issued phases)
@@ -699,7 +745,7 @@ __global__ void __launch_bounds__(MAXT, 1) down_fused_kernel(GroupParams P, int 
     issued++;
   };
   if (warp_on && lane == 0)
-    for (int s = 0; s < kDStages; s++) issue_next();  // the weight stream starts before h is ready
+    for (int s = 0; s < kDStages / 2; s++) issue_next();  // the weight stream starts before h is ready
 
   LaneTensor lt;
   lane_tensor(lt, *sl, c);
@@ -709,6 +755,8 @@ __global__ void __launch_bounds__(MAXT, 1) down_fused_kernel(GroupParams P, int 
   Limbs L;
   load_chunk_f32(P.h, COLI_DTYPE_F32, (size_t)k * P.I, 32 * c, active ? P.I : 0, hv);
   if (!make_limbs(hv, L) && active) set_error(P.err, COLI_E_NONFINITE);
+  if (warp_on && lane == 0)  // the rest of the ring once h has arrived (its loads go first)
+    for (int s = kDStages / 2; s < kDStages; s++) issue_next();
 
   uint32_t b = 0;
   bool stop = false;

@@ -32,7 +32,7 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 template <int EPL>
 __device__ void select_token(const float2* __restrict__ sc_row, int E, int K, float topp, int norm_topk,
                              float routed_scale, int32_t* __restrict__ idx_out, float* __restrict__ w_out,
-                             int32_t* __restrict__ nsel_out, int* err) {
+                             int32_t* __restrict__ nsel_out, int* err, const ExpertDesc* table) {
   const int lane = threadIdx.x & 31;
   uint32_t key[EPL];
   float sv[EPL];
@@ -77,6 +77,11 @@ __device__ void select_token(const float2* __restrict__ sc_row, int E, int K, fl
       wmine = ws;
     }
   }
+  // The chosen experts' table entries go to L2 now: the expert kernels that follow read them
+  // first (a hint only; every id below E is inside the table).
+  if (table && lane < K)
+    for (int l = 0; l < (int)(sizeof(ExpertDesc) / 128); l++)
+      prefetch_l2_line(reinterpret_cast<const char*>(table + mine) + 128 * l);
   // weights from the raw (bias-free) score; every sum in slot order in binary32, no contraction
   int m = K;
   float denom = 1.f;
@@ -107,11 +112,11 @@ __device__ void select_token(const float2* __restrict__ sc_row, int E, int K, fl
 
 template <int EPL>
 __device__ void select_all(const float2* sc, int S, int E, int K, float topp, int norm_topk, float routed_scale,
-                           int32_t* idx, float* w, int32_t* n_sel, int* err) {
+                           int32_t* idx, float* w, int32_t* n_sel, int* err, const ExpertDesc* table) {
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   for (int t = warp; t < S; t += nwarps)
     select_token<EPL>(sc + (size_t)t * E, E, K, topp, norm_topk, routed_scale, idx + (size_t)t * K, w + (size_t)t * K,
-                      n_sel ? n_sel + t : nullptr, err);
+                      n_sel ? n_sel + t : nullptr, err, table);
 }
 
 // Logits GEMV: CTA b computes rows e = b * kRowsPerCta + r (r < kRowsPerCta) for every token;
@@ -125,7 +130,8 @@ __device__ __forceinline__ void router_body(const void* __restrict__ x, int x_dt
                                             int K, float topp, int norm_topk, float routed_scale,
                                             float2* __restrict__ sc_ws, int32_t* __restrict__ idx,
                                             float* __restrict__ w, int32_t* __restrict__ n_sel,
-                                            int* __restrict__ status, unsigned* arrivals, int epl) {
+                                            int* __restrict__ status, unsigned* arrivals, int epl,
+                                            const ExpertDesc* table) {
   __shared__ float red[kRouterThreads / 32][kRowsPerCta];
   __shared__ int am_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -180,21 +186,22 @@ __device__ __forceinline__ void router_body(const void* __restrict__ x, int x_dt
     __syncthreads();
   }
   // The CTA that finishes last runs the selection over every token's complete score row.
+  // (the arrival is a release of this CTA's stores, ordered after them by the barrier above, and
+  // for the last CTA an acquire of every other CTA's)
   if (tid == 0) {
-    __threadfence();
-    unsigned prev = atomicAdd(arrivals, 1u);
+    unsigned prev;
+    asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(prev) : "l"(arrivals) : "memory");
     am_last = prev == gridDim.x - 1;
   }
   __syncthreads();
   if (!am_last) return;
-  __threadfence();
   switch (epl) {
-    case 1: select_all<1>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
-    case 2: select_all<2>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
-    case 4: select_all<4>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
-    case 8: select_all<8>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
-    case 16: select_all<16>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
-    default: select_all<32>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status); break;
+    case 1: select_all<1>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
+    case 2: select_all<2>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
+    case 4: select_all<4>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
+    case 8: select_all<8>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
+    case 16: select_all<16>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
+    default: select_all<32>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
   }
   __syncthreads();
   if (tid == 0) atomicExch(arrivals, 0u);
@@ -205,9 +212,9 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(
     const void* __restrict__ x, int x_dtype, int S, int D, const float* __restrict__ Wr,
     const float* __restrict__ bias, int E, int K, float topp, int norm_topk, float routed_scale,
     float2* __restrict__ sc_ws, int32_t* __restrict__ idx, float* __restrict__ w,
-    int32_t* __restrict__ n_sel, int* __restrict__ status, int epl) {
+    int32_t* __restrict__ n_sel, int* __restrict__ status, int epl, const ExpertDesc* table) {
   router_body<VEC4>(x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk, routed_scale, sc_ws, idx, w, n_sel, status,
-                    reinterpret_cast<unsigned*>(status + 1), epl);
+                    reinterpret_cast<unsigned*>(status + 1), epl, table);
 }
 
 template <bool VEC4>
@@ -215,9 +222,9 @@ __global__ void __launch_bounds__(kRouterThreads) router_fixed_kernel(
     const void* __restrict__ x, int x_dtype, int S, int D, const float* __restrict__ Wr,
     const float* __restrict__ bias, int E, int K, float topp, int norm_topk, float routed_scale,
     float2* __restrict__ sc_ws, int32_t* __restrict__ idx, float* __restrict__ w,
-    int32_t* __restrict__ n_sel, int* __restrict__ status, unsigned* arrivals, int epl) {
+    int32_t* __restrict__ n_sel, int* __restrict__ status, unsigned* arrivals, int epl, const ExpertDesc* table) {
   router_body<VEC4>(x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk, routed_scale, sc_ws, idx, w, n_sel, status,
-                    arrivals, epl);
+                    arrivals, epl, table);
 }
 
 int launch_router(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr, const float* bias,
@@ -232,6 +239,7 @@ int launch_router(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const
               ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
   int grid = (E + kRowsPerCta - 1) / kRowsPerCta;
   ProfScope prof(ctx, COLI_KERNEL_ROUTER);
+  const ExpertDesc* table = ctx->table_count > 0 ? ctx->d_table : nullptr;  // for the L2 prefetch hint
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kRouterThreads);
@@ -243,9 +251,9 @@ int launch_router(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const
   cfg.numAttrs = 1;
   const void* xp = x;
   cudaError_t le = vec4 ? cudaLaunchKernelEx(&cfg, router_kernel<true>, xp, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk,
-                                             routed_scale, sc_ws, idx, w, n_sel, ctx->d_status, epl)
+                                             routed_scale, sc_ws, idx, w, n_sel, ctx->d_status, epl, table)
                         : cudaLaunchKernelEx(&cfg, router_kernel<false>, xp, x_dtype, S, D, Wr, bias, E, K, topp,
-                                             norm_topk, routed_scale, sc_ws, idx, w, n_sel, ctx->d_status, epl);
+                                             norm_topk, routed_scale, sc_ws, idx, w, n_sel, ctx->d_status, epl, table);
   if (le != cudaSuccess) return cuda_fail(ctx, le, "router launch");
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(ctx, e, "router launch");
@@ -303,6 +311,7 @@ int launch_router_noalloc(coli_ctx* ctx, const void* x, int x_dtype, int S, int 
   const bool vec4 = (D % 4 == 0) && ((reinterpret_cast<uintptr_t>(Wr) & 15) == 0) &&
                     ((reinterpret_cast<uintptr_t>(x) & 15) == 0);
   const int grid = (E + kRowsPerCta - 1) / kRowsPerCta;
+  const ExpertDesc* table = ctx->table_count > 0 ? ctx->d_table : nullptr;  // for the L2 prefetch hint
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kRouterThreads);
@@ -314,9 +323,9 @@ int launch_router_noalloc(coli_ctx* ctx, const void* x, int x_dtype, int S, int 
   cfg.numAttrs = 1;
   const void* xp = x;
   e = vec4 ? cudaLaunchKernelEx(&cfg, router_fixed_kernel<true>, xp, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk,
-                                routed_scale, sc_ws, idx, w, n_sel, ctx->d_status, arrivals, epl)
+                                routed_scale, sc_ws, idx, w, n_sel, ctx->d_status, arrivals, epl, table)
            : cudaLaunchKernelEx(&cfg, router_fixed_kernel<false>, xp, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk,
-                                routed_scale, sc_ws, idx, w, n_sel, ctx->d_status, arrivals, epl);
+                                routed_scale, sc_ws, idx, w, n_sel, ctx->d_status, arrivals, epl, table);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "router_select_noalloc launch");
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(ctx, e, "router_select_noalloc launch");
