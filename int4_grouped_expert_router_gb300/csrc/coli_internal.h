@@ -84,7 +84,7 @@ struct coli_ctx {
   std::vector<uint64_t> table_handles;       // 3 per entry
   int table_D = 0, table_I = 0, table_count = 0;
   // device status words: [0] error code, [1] router completion counter
-  int* d_status = nullptr;
+  int* d_status = nullptr;  // [0] device error word, [1] router arrivals
   coli::Workspace ws;
   // COLI_FAIL_AFTER test hook
   long long fail_after = -1;

@@ -373,6 +373,71 @@ __device__ __forceinline__ float chunk_dot_slow(const uint4 wv, const Limbs& L, 
 }
 
 
+constexpr uint32_t kUpOff = kBoxRows * kSliceWords * 4;  // up box within a gate/up stage
+constexpr uint32_t kScaleOff = 2 * kUpOff;               // gate scale box, then the up scale box
+
+// Dot products of one batch from a stage of the warp's ring: acc[u] = gate row u, acc[kBoxRows + u]
+// = up row u of this lane's chunk (scaled by chunk scales when those are staged; row scales are
+// applied when the rows are finished). `st` is the stage base plus 16 * lane; n = rows of the batch
+// inside the matrix (the fast paths compute all kBoxRows, the extra rows are never read back).
+__device__ __forceinline__ void gateup_batch(float (&acc)[2 * kBoxRows], bool ok, bool has_chunk, bool row_scales,
+                                             const LaneTensor& tg, const LaneTensor& tu, const uint8_t* st,
+                                             const uint8_t* sgb, int warp, const Limbs& L, const GroupParams& P,
+                                             int cur_tok, int i0, int n, int c) {
+  if (ok && has_chunk && row_scales) {
+#pragma unroll
+    for (int u = 0; u < kBoxRows; u++) {
+      acc[u] = chunk_dot(lds128(st + u * tg.rowB), L);
+      acc[kBoxRows + u] = chunk_dot(lds128(st + kUpOff + u * tu.rowB), L);
+    }
+  } else if (ok && has_chunk && tg.fast && tu.fast) {
+#pragma unroll
+    for (int u = 0; u < kBoxRows; u++) {
+      float dg = chunk_dot(lds128(st + u * tg.rowB), L);
+      float du = chunk_dot(lds128(st + kUpOff + u * tu.rowB), L);
+      if (tg.box_s) dg *= lds32f(sgb + (u * tg.box_s + tg.cg - tg.box_s * warp) * 4);
+      if (tu.box_s) du *= lds32f(sgb + kBoxRows * kScaleBox * 4 + (u * tu.box_s + tu.cg - tu.box_s * warp) * 4);
+      acc[u] = dg;
+      acc[kBoxRows + u] = du;
+    }
+  } else {
+    float tmp[2 * kBoxRows];  // local memory: the rarely used slow path keeps the code small
+#pragma unroll 1
+    for (int v = 0; v < 2 * kBoxRows; v++) {
+      const int u = v % kBoxRows;
+      const LaneTensor& lt = v < kBoxRows ? tg : tu;
+      float d = 0.f;
+      if (ok && has_chunk && u < n) {
+        const uint4 wv = lds128(st + (v / kBoxRows) * kUpOff + u * lt.rowB);
+        if (lt.fast)
+          d = chunk_dot(wv, L) * (lt.box_s ? lds32f(sgb + (v / kBoxRows) * (kBoxRows * kScaleBox * 4) +
+                                                    (u * lt.box_s + lt.cg - lt.box_s * warp) * 4)
+                                           : 1.f);
+        else
+          d = chunk_dot_slow(wv, L, lt, P.x, P.x_dtype, (size_t)cur_tok * P.D, i0 + u, c);
+      }
+      tmp[v] = d;
+    }
+#pragma unroll
+    for (int v = 0; v < 2 * kBoxRows; v++) acc[v] = tmp[v];
+  }
+}
+
+// Issue the TMA loads of one batch (gate and up boxes, and staged chunk scales) into a stage.
+__device__ __forceinline__ void gateup_issue(const RouteSlot& rs, uint8_t* st, uint64_t* bar, int warp, int i0) {
+  const SlotTensor& g = rs.ts[0];
+  const SlotTensor& u = rs.ts[1];
+  uint32_t bytes = 2u * g.box_rows * g.box_w * 4;
+  if (g.box_s) bytes += g.box_rows * g.box_s * 4;
+  if (u.box_s) bytes += u.box_rows * u.box_s * 4;
+  mbar_arrive_expect_tx(bar, bytes);
+  const int x = kSliceWords * warp;
+  tma_load_2d(st, &g.d->map_w, x, i0, bar);
+  tma_load_2d(st + kUpOff, &u.d->map_w, x, i0, bar);
+  if (g.box_s) tma_load_2d(st + kScaleOff, &g.d->map_s, g.box_s * warp, i0, bar);
+  if (u.box_s) tma_load_2d(st + kScaleOff + kBoxRows * kScaleBox * 4, &u.d->map_s, u.box_s * warp, i0, bar);
+}
+
 // ------------------------------------------------------------------------------------------
 // Gate + up dual GEMV with the SiLU(g) * u epilogue.
 // Thread c of the CTA owns column chunk c (warp c / 32 owns slice c / 32) of every row and keeps
@@ -501,21 +566,8 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 192 ? kGUMinCtas : 1) gateup_ker
       }
       const RouteSlot& rs = sm.routes[j - j_first];
       if (!rs.ok) continue;
-      const SlotTensor& g = rs.ts[0];
-      const SlotTensor& u = rs.ts[1];
-      uint64_t* bar = &bars[istage];
-      uint8_t* st = ring + (size_t)istage * SB;
+      gateup_issue(rs, ring + (size_t)istage * SB, &bars[istage], warp, i0);
       istage = istage + 1 == kGUStages ? 0 : istage + 1;
-      uint32_t bytes = 2u * g.box_rows * g.box_w * 4;
-      if (g.box_s) bytes += g.box_rows * g.box_s * 4;
-      if (u.box_s) bytes += u.box_rows * u.box_s * 4;
-      mbar_arrive_expect_tx(bar, bytes);
-      const int x = kSliceWords * warp;
-      tma_load_2d(st, &g.d->map_w, x, i0, bar);
-      tma_load_2d(st + kBoxRows * kSliceWords * 4, &u.d->map_w, x, i0, bar);
-      if (g.box_s) tma_load_2d(st + 2 * kBoxRows * kSliceWords * 4, &g.d->map_s, g.box_s * warp, i0, bar);
-      if (u.box_s)
-        tma_load_2d(st + 2 * kBoxRows * kSliceWords * 4 + kBoxRows * kScaleBox * 4, &u.d->map_s, u.box_s * warp, i0, bar);
       issued++;
       return;
     }
@@ -544,8 +596,6 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 192 ? kGUMinCtas : 1) gateup_ker
   bool stop = false, row_scales = false;
   int stage = 0;
   uint32_t phase = 0;
-  constexpr uint32_t kUpOff = kBoxRows * kSliceWords * 4;  // up box within a stage
-  constexpr uint32_t kScaleOff = 2 * kUpOff;               // gate scale box, then the up scale box
   int j = j_first, i0 = (qbeg - j_first * Bpr) * kBoxRows;
   for (int qs = qbeg; qs < qend; qs += segB) {
     const int qe = min(qs + segB, qend);
@@ -569,46 +619,8 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 192 ? kGUMinCtas : 1) gateup_ker
         const bool ok = !stop && mbar_wait(&bars[stage], phase);
         const uint8_t* st = ring + (size_t)stage * SB + 16 * lane;
         float acc[2 * kBoxRows];  // gate rows 0..3, then up rows 0..3
-        if (ok && has_chunk && row_scales) {
-#pragma unroll
-          for (int u = 0; u < kBoxRows; u++) {
-            acc[u] = chunk_dot(lds128(st + u * tg.rowB), L);
-            acc[kBoxRows + u] = chunk_dot(lds128(st + kUpOff + u * tu.rowB), L);
-          }
-        } else if (ok && has_chunk && tg.fast && tu.fast) {
-          const uint8_t* sgb = ring + (size_t)stage * SB + kScaleOff;
-#pragma unroll
-          for (int u = 0; u < kBoxRows; u++) {
-            float dg = chunk_dot(lds128(st + u * tg.rowB), L);
-            float du = chunk_dot(lds128(st + kUpOff + u * tu.rowB), L);
-            if (tg.box_s) dg *= lds32f(sgb + (u * tg.box_s + tg.cg - tg.box_s * warp) * 4);
-            if (tu.box_s) du *= lds32f(sgb + kBoxRows * kScaleBox * 4 + (u * tu.box_s + tu.cg - tu.box_s * warp) * 4);
-            acc[u] = dg;
-            acc[kBoxRows + u] = du;
-          }
-        } else {
-          const uint8_t* sgb = ring + (size_t)stage * SB + kScaleOff;
-          const int n = min(kBoxRows, P.I - i0);
-          float tmp[2 * kBoxRows];  // local memory: the rarely used slow path keeps the code small
-#pragma unroll 1
-          for (int v = 0; v < 2 * kBoxRows; v++) {
-            const int u = v % kBoxRows;
-            const LaneTensor& lt = v < kBoxRows ? tg : tu;
-            float d = 0.f;
-            if (ok && has_chunk && u < n) {
-              const uint4 wv = lds128(st + (v / kBoxRows) * kUpOff + u * lt.rowB);
-              if (lt.fast)
-                d = chunk_dot(wv, L) * (lt.box_s ? lds32f(sgb + (v / kBoxRows) * (kBoxRows * kScaleBox * 4) +
-                                                          (u * lt.box_s + lt.cg - lt.box_s * warp) * 4)
-                                                 : 1.f);
-              else
-                d = chunk_dot_slow(wv, L, lt, P.x, P.x_dtype, (size_t)cur_tok * P.D, i0 + u, c);
-            }
-            tmp[v] = d;
-          }
-#pragma unroll
-          for (int v = 0; v < 2 * kBoxRows; v++) acc[v] = tmp[v];
-        }
+        gateup_batch(acc, ok, has_chunk, row_scales, tg, tu, st, ring + (size_t)stage * SB + kScaleOff, warp, L, P,
+                     cur_tok, i0, min(kBoxRows, P.I - i0), c);
         __syncwarp();
         if (lane == 0 && ok) issue_next();  // refill the stage just consumed
         if (!ok && !stop) {
@@ -706,8 +718,11 @@ __global__ void __launch_bounds__(MAXT, 1) down_fused_kernel(GroupParams P, int 
   uint8_t* ring = smem_raw + kDCtrlBytes + (size_t)warp * kDStages * SB;
   uint64_t* bars = sm.bars[warp];
 
-  // routes of token 0 (written by the router, complete before the gate/up kernel started)
+  // routes of token 0 (written by the router, complete before the gate/up kernel started); the
+  // count, ids and weights are read in one round trip
   int m = P.n_sel ? ld_cg_i32(P.n_sel) : P.K;
+  const int e_slot = tid < P.K ? ld_cg_i32(P.idx + tid) : -1;
+  const float w_slot = tid < P.K ? ld_cg_f32(P.w + tid) : 0.f;
   m = m < 0 ? 0 : (m > P.K ? P.K : m);
   if (lane == 0) {
     for (int s = 0; s < kDStages; s++) mbar_init(&bars[s], 1);
@@ -716,13 +731,12 @@ __global__ void __launch_bounds__(MAXT, 1) down_fused_kernel(GroupParams P, int 
   if (tid < P.K) {
     bool ok = false;
     if (tid < m) {
-      const int e = ld_cg_i32(P.idx + tid);
-      ok = e >= 0 && e < COLI_MAX_EXPERTS && P.table[e].valid;
-      if (ok) fill_slot_tensor(sm.st[tid], &P.table[e].t[T_DOWN]);
+      ok = e_slot >= 0 && e_slot < COLI_MAX_EXPERTS && P.table[e_slot].valid;
+      if (ok) fill_slot_tensor(sm.st[tid], &P.table[e_slot].t[T_DOWN]);
       else set_error(P.err, COLI_E_ROUTE);
     }
     sm.ok[tid] = ok;
-    sm.wk[tid] = ok ? ld_cg_f32(P.w + tid) : 0.f;
+    sm.wk[tid] = ok ? w_slot : 0.f;
   }
   __syncthreads();
   const int d_begin = (int)((long long)blockIdx.x * P.D / gridDim.x);

@@ -77,11 +77,6 @@ __device__ void select_token(const float2* __restrict__ sc_row, int E, int K, fl
       wmine = ws;
     }
   }
-  // The chosen experts' table entries go to L2 now: the expert kernels that follow read them
-  // first (a hint only; every id below E is inside the table).
-  if (table && lane < K)
-    for (int l = 0; l < (int)(sizeof(ExpertDesc) / 128); l++)
-      prefetch_l2_line(reinterpret_cast<const char*>(table + mine) + 128 * l);
   // weights from the raw (bias-free) score; every sum in slot order in binary32, no contraction
   int m = K;
   float denom = 1.f;
@@ -108,6 +103,11 @@ __device__ void select_token(const float2* __restrict__ sc_row, int E, int K, fl
     w_out[lane] = kept ? __fmul_rn(wv, routed_scale) : 0.f;
   }
   if (lane == 0 && nsel_out) *nsel_out = m;
+  // The chosen experts' table entries go to L2: the expert kernels that follow read them first
+  // (a hint only; every id below E is inside the table).
+  if (table && lane < K)
+    for (int l = 0; l < (int)(sizeof(ExpertDesc) / 128); l++)
+      prefetch_l2_line(reinterpret_cast<const char*>(table + mine) + 128 * l);
 }
 
 template <int EPL>

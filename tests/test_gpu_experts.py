@@ -54,6 +54,9 @@ def tol(cfg, ref):
     LayerConfig("S5-bf16", D=512, I=256, E=16, K=4, S=5, x_dtype="bf16", zipf=True),
     LayerConfig("S1-bf16", D=256, I=128, E=16, K=4, x_dtype="bf16"),
     LayerConfig("K16", D=128, I=64, E=64, K=16),
+    # many kept routes: CTAs whose batch ranges span several routes
+    LayerConfig("S9-36routes", D=256, I=136, E=24, K=4, S=9, topp=0.9, zipf=True),
+    LayerConfig("S5K8-40routes-g64", D=320, I=200, E=32, K=8, S=5, gs="mixed:64"),
 ], ids=lambda c: c.name)
 def test_layer_matches_oracle(ctx, cfg):
     y, ref, near = run_layer(ctx, cfg, with_resid=cfg.name != "tiny-noresid")
