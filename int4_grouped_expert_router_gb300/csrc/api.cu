@@ -134,6 +134,16 @@ static int make_desc(coli_ctx* ctx, HostTensor& t) {
                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(ctx, COLI_E_CUDA, "upload: weight tensor map encoding failed");
   }
+  {
+    cuuint64_t dims[2] = {words, (cuuint64_t)t.O};
+    cuuint64_t strides[1] = {t.pitch};
+    cuuint32_t box[2] = {(cuuint32_t)kTcWords, (cuuint32_t)kTcRows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(&d.map_tc, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, t.w, dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(ctx, COLI_E_CUDA, "upload: tensor-core tile map encoding failed");
+  }
   d.box_s = 0;
   if (d.mode == SCALE_CHUNK && t.gs >= 64 && t.gs <= 256 && t.G % 4 == 0) {
     uint32_t per_warp = (uint32_t)(32 * 32 / t.gs);  // chunk groups under one warp's 32 chunks
@@ -147,6 +157,19 @@ static int make_desc(coli_ctx* ctx, HostTensor& t) {
     if (r == CUDA_SUCCESS) d.box_s = bs;
   }
   t.desc = d;
+  return COLI_OK;
+}
+
+int encode_bf16_rows_map(coli_ctx* ctx, CUtensorMap* map, void* base, long long rows, int cols) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(ctx, COLI_E_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, 16};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ctx, COLI_E_CUDA, "activation tensor map encoding failed");
   return COLI_OK;
 }
 

@@ -22,12 +22,16 @@ constexpr int kBoxRows = 4;
 constexpr int kSliceWords = 128;
 // Chunk-group scales of one warp's slice that travel by TMA (group sizes 64..256).
 constexpr int kScaleBox = 16;
+// Tensor-core (prefill) weight tiles: 128 rows x 64 columns (8 words of packed nibbles).
+constexpr int kTcRows = 128;
+constexpr int kTcWords = 8;
 
 // One uploaded int4 tensor as the kernels see it. Rows are padded to a whole number of 16-byte
 // chunks (32 columns each); padding nibbles hold 8, i.e. the value 0.
 struct TensorDesc {
   CUtensorMap map_w;   // 2-D map over the weights as uint32 [rows x pitch/4], box [box_rows x box_w]
   CUtensorMap map_s;   // 2-D map over chunk-group scales f32 [rows x G], box [box_rows x box_s]
+  CUtensorMap map_tc;  // 2-D map over the weights as uint32 [rows x pitch/4], box [kTcRows x kTcWords]
   const uint8_t* w;    // rows x pitch bytes
   const float* s;      // scales: rows (gs == 0) or rows * G (gs > 0)
   uint32_t pitch;      // bytes per row, multiple of 16
@@ -123,6 +127,14 @@ struct ProfScope {
 int launch_router(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr,
                   const float* bias, int E, int K, float topp, int norm_topk, float routed_scale,
                   int32_t* idx, float* w, int32_t* n_sel);
+// Tensor-core (prefill) path of coli_expert_group: bf16 activations, many routed rows per expert.
+bool prefill_eligible(const coli_ctx* ctx, const void* x, int S, int K, int x_dtype);
+int launch_prefill(coli_ctx* ctx, const void* x, int S, const int32_t* idx, const float* w, const int32_t* n_sel,
+                   int K, const void* resid, void* y);
+// TMA map over a row-major bf16 matrix [rows x cols] read in 16-row x 64-column boxes with the
+// 128-byte swizzle (cols a multiple of 8).
+int encode_bf16_rows_map(coli_ctx* ctx, CUtensorMap* map, void* base, long long rows, int cols);
+
 int launch_router_noalloc(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr,
                           const float* bias, int E, int K, float topp, int norm_topk, float routed_scale,
                           int32_t* idx, float* w, int32_t* n_sel);

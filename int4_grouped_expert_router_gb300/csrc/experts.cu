@@ -297,13 +297,6 @@ constexpr int kDStages = 4;  // stages per warp ring of the down kernel
 constexpr int kSeg = 64;          // rows (down) or row pairs (gate/up) finished together
 constexpr int kRouteCache = 16;   // routes resolved once into shared memory
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          smem_u32(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
 
 // Everything a kernel needs about one tensor of a kept route, copied once into shared memory.
 struct SlotTensor {
@@ -986,6 +979,7 @@ static cudaError_t launch_k(void (*kern)(KArgs...), int grid, int block, size_t 
 
 int launch_expert_group(coli_ctx* ctx, const void* x, int x_dtype, int S, const int32_t* idx, const float* w,
                         const int32_t* n_sel, int K, const void* resid, void* y) {
+  if (prefill_eligible(ctx, x, S, K, x_dtype)) return launch_prefill(ctx, x, S, idx, w, n_sel, K, resid, y);
   if (S > COLI_MAX_GROUP_TOKENS) return fail(ctx, COLI_E_INVAL, "expert_group: S above COLI_MAX_GROUP_TOKENS");
   const int D = ctx->table_D, I = ctx->table_I;
   if (D > COLI_MAX_GROUP_DIM) return fail(ctx, COLI_E_INVAL, "expert_group: D above COLI_MAX_GROUP_DIM");

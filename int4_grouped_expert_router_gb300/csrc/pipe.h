@@ -98,6 +98,19 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return p;
 }
 
+// 2-D tiled TMA load of the box at element coordinates (x, y) of `map` (a tensor map in global,
+// constant or parameter memory) into shared memory; completion on `bar` as transaction bytes.
+// x times the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ int ld_volatile_int(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
+
 // Prefetch one 128-byte line into L2 (a hint; no fault on any address of a live allocation).
 __device__ __forceinline__ void prefetch_l2_line(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));

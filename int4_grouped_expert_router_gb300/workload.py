@@ -53,6 +53,7 @@ CONFIGS = {
     "decode_g64": LayerConfig("decode_g64", D=6144, I=2048, E=256, K=8, gs="mixed:64", topp=0.9),
     "decode_g64_tail": LayerConfig("decode_g64_tail", D=6144, I=2000, E=256, K=8, gs=64, topp=0.9),
     "decode_s4_bf16": LayerConfig("decode_s4_bf16", D=6144, I=2048, E=256, K=8, S=4, x_dtype="bf16", zipf=True),
+    "prefill": LayerConfig("prefill", D=6144, I=2048, E=256, K=8, S=512, gs=64, x_dtype="bf16", zipf=True),
 }
 
 
