@@ -131,8 +131,9 @@ COLI_API int coli_router_select(coli_ctx *ctx, const void *x, int x_dtype, int S
  * allocate: a server that has given all free device memory to its own caching pool, or a decode
  * loop that cannot take the stall of cudaMalloc (which may synchronise the device) or of a
  * workspace that grows (which first waits for the context's stream).
- *   - Scratch: a fixed device array of the library, one per device, holding the (score, choice)
- *     pairs of at most 65536 (token, expert) cells; S * E above that returns COLI_E_INVAL.
+ *   - Scratch: a fixed device array of the library, one per device (2.5 MiB), holding the
+ *     (score, choice) pairs and, for S >= 16, the partial logits of at most 65536 (token, expert)
+ *     cells; S * E above that returns COLI_E_INVAL.
  *   - The first call on a device looks up that array's address (a CUDA symbol query with the
  *     context's device current); make that first call before any stream capture.
  *   - The array's arrival counter is cleared on the context's stream before each launch.

@@ -72,11 +72,14 @@ __global__ void pf_count_kernel(const int32_t* idx, const int32_t* n_sel, int S,
   if (lane == 0) cnt[e] = c;
 }
 
-// One CTA: row offsets of every expert's padded blocks, the work entries, and pos[] = -1.
-__global__ void pf_plan_kernel(const int* cnt, int E, int SK, int* row_off, PfEntry* entries, int* n_entries, int* pos) {
+// One CTA: row offsets of every expert's padded blocks, the work entries, the total rows, and
+// pos[] = src[] = -1.
+__global__ void pf_plan_kernel(const int* cnt, int E, int SK, int R_max, int* row_off, PfEntry* entries, int* n_entries,
+                               int* n_rows, int* pos, int* src) {
   __shared__ int s_rows[32], s_ents[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
   for (int i = tid; i < SK; i += blockDim.x) pos[i] = -1;
+  for (int i = tid; i < R_max; i += blockDim.x) src[i] = -1;
   const int per = (E + blockDim.x - 1) / blockDim.x;
   const int e0 = tid * per, e1 = min(E, e0 + per);
   int rows = 0, ents = 0;
@@ -124,50 +127,59 @@ __global__ void pf_plan_kernel(const int* cnt, int E, int SK, int* row_off, PfEn
       row += en.npad;
     }
   }
-  if (tid == 0) *n_entries = te;
-  (void)tr;
+  if (tid == 0) {
+    *n_entries = te;
+    *n_rows = tr;
+  }
 }
 
-// One warp per expert: the sorted row of each of its routes (pos), and its activation rows copied
-// into the grouped matrix in the tensor-core column order; padding rows are zeroed.
-__global__ void pf_place_kernel(const uint16_t* __restrict__ x, const int32_t* idx, const int32_t* n_sel, int S, int K,
-                                int D, int E, const int* cnt, const int* row_off, int* pos, uint16_t* __restrict__ xs) {
+// One warp per expert: the grouped row of each of its routes (pos[t K + k]) and, per row, the token
+// it holds (src; padding rows keep -1).
+__global__ void pf_rank_kernel(const int32_t* idx, const int32_t* n_sel, int S, int K, int E, const int* cnt,
+                               const int* row_off, int* pos, int* src) {
   const int lane = threadIdx.x & 31;
   const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (e >= E) return;
   const int c = cnt[e];
   if (c == 0) return;
-  const int SK = S * K, row0 = row_off[e], G8 = D / 8;
+  const int SK = S * K, row0 = row_off[e];
   int rank = 0;
   for (int base = 0; base < SK && rank < c; base += 32) {
     const bool m = pf_route_is(idx, n_sel, K, base + lane, SK, e);
-    unsigned bal = __ballot_sync(0xffffffffu, m);
-    if (m) pos[base + lane] = row0 + rank + __popc(bal & ((1u << lane) - 1u));
-    while (bal) {
-      const int src = __ffs(bal) - 1;
-      bal &= bal - 1;
-      const int t = (base + src) / K;
-      const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * D);
-      uint4* dr = reinterpret_cast<uint4*>(xs + (size_t)(row0 + rank) * D);
-      for (int g = lane; g < G8; g += 32) {
-        const uint4 v = __ldg(xr + g);  // columns 8g .. 8g+7 as bf16 pairs
-        uint4 o;
-        o.x = __byte_perm(v.x, v.z, 0x5410);  // (c0, c4)
-        o.y = __byte_perm(v.x, v.z, 0x7632);  // (c1, c5)
-        o.z = __byte_perm(v.y, v.w, 0x5410);  // (c2, c6)
-        o.w = __byte_perm(v.y, v.w, 0x7632);  // (c3, c7)
-        dr[g] = o;
-      }
-      rank++;
+    const unsigned bal = __ballot_sync(0xffffffffu, m);
+    if (m) {
+      const int row = row0 + rank + __popc(bal & ((1u << lane) - 1u));
+      pos[base + lane] = row;
+      src[row] = (base + lane) / K;
     }
+    rank += __popc(bal);
   }
-  // zero the padding rows of the last block
-  const int nch = (c + kPfRows - 1) / kPfRows;
-  const int last_n = c - (nch - 1) * kPfRows;
-  const int pad_end = (nch - 1) * kPfRows + (last_n + kPfPad - 1) / kPfPad * kPfPad;
-  for (int r = c; r < pad_end; r++) {
-    uint4* dr = reinterpret_cast<uint4*>(xs + (size_t)(row0 + r) * D);
-    for (int g = lane; g < G8; g += 32) dr[g] = make_uint4(0, 0, 0, 0);
+}
+
+// One warp per grouped row: the token's activations in the tensor-core column order (each group of
+// 8 columns as 0 4 1 5 2 6 3 7), or zeros for a padding row.
+__global__ void pf_gather_kernel(const uint16_t* __restrict__ x, int D, int R_max, const int* n_rows, const int* src,
+                                 uint16_t* __restrict__ xs) {
+  const int lane = threadIdx.x & 31, G8 = D / 8;
+  const int nr = *n_rows;
+  for (int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < nr && row < R_max;
+       row += gridDim.x * (blockDim.x >> 5)) {
+    const int t = src[row];
+    uint4* dr = reinterpret_cast<uint4*>(xs + (size_t)row * D);
+    if (t < 0) {
+      for (int g = lane; g < G8; g += 32) dr[g] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * D);
+    for (int g = lane; g < G8; g += 32) {
+      const uint4 v = __ldg(xr + g);  // columns 8g .. 8g+7 as bf16 pairs
+      uint4 o;
+      o.x = __byte_perm(v.x, v.z, 0x5410);  // (c0, c4)
+      o.y = __byte_perm(v.x, v.z, 0x7632);  // (c1, c5)
+      o.z = __byte_perm(v.y, v.w, 0x5410);  // (c2, c6)
+      o.w = __byte_perm(v.y, v.w, 0x7632);  // (c3, c7)
+      dr[g] = o;
+    }
   }
 }
 
@@ -532,8 +544,9 @@ int launch_prefill(coli_ctx* ctx, const void* x, int S, const int32_t* idx, cons
     off = align_up(off + bytes, 256);
     return o;
   };
-  const size_t o_cnt = take((size_t)E * 4), o_roff = take((size_t)E * 4), o_nent = take(4),
+  const size_t o_cnt = take((size_t)E * 4), o_roff = take((size_t)E * 4), o_nent = take(8),
                o_ent = take((size_t)max_entries * sizeof(PfEntry)), o_pos = take((size_t)SK * 4),
+               o_src = take((size_t)R_max * 4),
                o_xs = take((size_t)R_max * D * 2), o_hs = take((size_t)R_max * I * 2), o_yr = take((size_t)R_max * D * 4);
   int rc = ensure_workspace(ctx, off);
   if (rc != COLI_OK) return rc;
@@ -543,6 +556,8 @@ int launch_prefill(coli_ctx* ctx, const void* x, int S, const int32_t* idx, cons
   int* nent = reinterpret_cast<int*>(ws + o_nent);
   PfEntry* ents = reinterpret_cast<PfEntry*>(ws + o_ent);
   int* pos = reinterpret_cast<int*>(ws + o_pos);
+  int* src = reinterpret_cast<int*>(ws + o_src);
+  int* nrows = nent + 1;
   uint16_t* xs = reinterpret_cast<uint16_t*>(ws + o_xs);
   uint16_t* hs = reinterpret_cast<uint16_t*>(ws + o_hs);
   float* yr = reinterpret_cast<float*>(ws + o_yr);
@@ -554,9 +569,13 @@ int launch_prefill(coli_ctx* ctx, const void* x, int S, const int32_t* idx, cons
   cudaError_t e;
   const int wpb = 8;  // warps (experts) per block of the grouping kernels
   pf_count_kernel<<<(E + wpb - 1) / wpb, wpb * 32, 0, ctx->stream>>>(idx, n_sel, S, K, E, ctx->d_table, cnt);
-  pf_plan_kernel<<<1, 1024, 0, ctx->stream>>>(cnt, E, (int)SK, roff, ents, nent, pos);
-  pf_place_kernel<<<(E + wpb - 1) / wpb, wpb * 32, 0, ctx->stream>>>(static_cast<const uint16_t*>(x), idx, n_sel, S, K, D,
-                                                                     E, cnt, roff, pos, xs);
+  pf_plan_kernel<<<1, 1024, 0, ctx->stream>>>(cnt, E, (int)SK, (int)R_max, roff, ents, nent, nrows, pos, src);
+  pf_rank_kernel<<<(E + wpb - 1) / wpb, wpb * 32, 0, ctx->stream>>>(idx, n_sel, S, K, E, cnt, roff, pos, src);
+  {
+    int g = (int)((R_max + 7) / 8);
+    if (g > 8 * ctx->num_sms) g = 8 * ctx->num_sms;
+    pf_gather_kernel<<<g, 256, 0, ctx->stream>>>(static_cast<const uint16_t*>(x), D, (int)R_max, nrows, src, xs);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(ctx, e, "prefill grouping launch");
 
   PfGemmParams G{};

@@ -227,9 +227,140 @@ __global__ void __launch_bounds__(kRouterThreads) router_fixed_kernel(
                     arrivals, epl, table);
 }
 
+// ------------------------------------------------------------------------------------------
+// Many tokens (S >= kBatchedS): the logits as a tiled f32 GEMM, each CTA a 64-token x 64-expert
+// tile over one of kRSplit column ranges of D; the ranges are summed in a fixed order, then
+// sigmoid and bias give the (score, choice) pairs and one warp per token selects.
+// ------------------------------------------------------------------------------------------
+
+constexpr int kBatchedS = 16;
+constexpr int kRT = 64;     // tokens and experts per tile
+constexpr int kRBK = 32;    // columns of D per step
+constexpr int kRSplit = 8;  // column ranges of D
+
+__global__ void __launch_bounds__(256) router_gemm_kernel(const void* __restrict__ x, int x_dtype, int S, int D,
+                                                          const float* __restrict__ Wr, int E, float* __restrict__ part) {
+  __shared__ __align__(16) float xs[kRBK][kRT + 4];  // [column][token]
+  __shared__ __align__(16) float ws[kRBK][kRT + 4];  // [column][expert]
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;  // thread: tokens 4 ty .., experts 4 tx ..
+  const int e0 = blockIdx.x * kRT, s0 = blockIdx.y * kRT;
+  const int per = ((D + kRSplit - 1) / kRSplit + kRBK - 1) / kRBK * kRBK;
+  const int d0 = blockIdx.z * per, d1 = min(D, d0 + per);
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; i++)
+#pragma unroll
+    for (int j = 0; j < 4; j++) acc[i][j] = 0.f;
+  // thread loads 8 elements of each tile per step: row (i / kRBK), column (i % kRBK), i = tid + 256 m
+  float px[8], pw[8];
+  auto fetch = [&](int k0) {
+#pragma unroll
+    for (int m = 0; m < 8; m++) {
+      const int i = tid + 256 * m, r = i / kRBK, k = k0 + i % kRBK;
+      px[m] = (s0 + r < S && k < d1) ? load_act(x, x_dtype, (size_t)(s0 + r) * D + k) : 0.f;
+      pw[m] = (e0 + r < E && k < d1) ? __ldg(Wr + (size_t)(e0 + r) * D + k) : 0.f;
+    }
+  };
+  if (d0 < d1) fetch(d0);
+  for (int k0 = d0; k0 < d1; k0 += kRBK) {
+#pragma unroll
+    for (int m = 0; m < 8; m++) {
+      const int i = tid + 256 * m;
+      xs[i % kRBK][i / kRBK] = px[m];
+      ws[i % kRBK][i / kRBK] = pw[m];
+    }
+    __syncthreads();
+    if (k0 + kRBK < d1) fetch(k0 + kRBK);  // the next step's loads overlap this step's FMAs
+#pragma unroll 8
+    for (int kk = 0; kk < kRBK; kk++) {
+      const float4 a = *reinterpret_cast<const float4*>(&xs[kk][4 * ty]);
+      const float4 b = *reinterpret_cast<const float4*>(&ws[kk][4 * tx]);
+      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 4; i++)
+#pragma unroll
+        for (int j = 0; j < 4; j++) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; i++)
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      const int s = s0 + 4 * ty + i, e = e0 + 4 * tx + j;
+      if (s < S && e < E) part[((size_t)blockIdx.z * S + s) * E + e] = acc[i][j];
+    }
+}
+
+__global__ void router_finish_kernel(const float* __restrict__ part, int S, int E, const float* __restrict__ bias,
+                                     float2* __restrict__ sc_ws) {
+  const long long n = (long long)S * E;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    float z = 0.f;
+    for (int sp = 0; sp < kRSplit; sp++) z += part[(size_t)sp * n + i];
+    const int e = (int)(i % E);
+    const float sc = 1.0f / (1.0f + expf(-z));
+    sc_ws[i] = make_float2(sc, bias ? __fadd_rn(sc, __ldg(bias + e)) : sc);
+  }
+}
+
+template <int EPL>
+__global__ void router_select_kernel(const float2* sc, int S, int E, int K, float topp, int norm_topk,
+                                     float routed_scale, int32_t* idx, float* w, int32_t* n_sel, int* err,
+                                     const ExpertDesc* table) {
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= S) return;  // uniform per warp
+  select_token<EPL>(sc + (size_t)t * E, E, K, topp, norm_topk, routed_scale, idx + (size_t)t * K, w + (size_t)t * K,
+                    n_sel ? n_sel + t : nullptr, err, table);
+}
+
+// sc_ws: S E (score, choice) pairs; part: kRSplit S E floats
+static int launch_router_batched(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr,
+                                 const float* bias, int E, int K, float topp, int norm_topk, float routed_scale,
+                                 int32_t* idx, float* w, int32_t* n_sel, float2* sc_ws, float* part) {
+  const ExpertDesc* table = ctx->table_count > 0 ? ctx->d_table : nullptr;
+  ProfScope prof(ctx, COLI_KERNEL_ROUTER);
+  router_gemm_kernel<<<dim3((E + kRT - 1) / kRT, (S + kRT - 1) / kRT, kRSplit), 256, 0, ctx->stream>>>(x, x_dtype, S, D,
+                                                                                                     Wr, E, part);
+  const long long n = (long long)S * E;
+  int g = (int)((n + 255) / 256);
+  if (g > 4 * ctx->num_sms) g = 4 * ctx->num_sms;
+  router_finish_kernel<<<g, 256, 0, ctx->stream>>>(part, S, E, bias, sc_ws);
+  int epl = 1;
+  while (32 * epl < E) epl *= 2;
+  const int sg = (S + 7) / 8;
+  switch (epl) {
+#define COLI_SELECT_CASE(N)                                                                                        \
+  case N:                                                                                                          \
+    router_select_kernel<N><<<sg, 256, 0, ctx->stream>>>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w,   \
+                                                         n_sel, ctx->d_status, table);                            \
+    break;
+    COLI_SELECT_CASE(1)
+    COLI_SELECT_CASE(2)
+    COLI_SELECT_CASE(4)
+    COLI_SELECT_CASE(8)
+    COLI_SELECT_CASE(16)
+    default:
+      router_select_kernel<32><<<sg, 256, 0, ctx->stream>>>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel,
+                                                             ctx->d_status, table);
+#undef COLI_SELECT_CASE
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "batched router launch");
+  return COLI_OK;
+}
+
 int launch_router(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr, const float* bias,
                   int E, int K, float topp, int norm_topk, float routed_scale, int32_t* idx, float* w,
                   int32_t* n_sel) {
+  if (S >= kBatchedS) {
+    const size_t sc_bytes = align_up((size_t)S * E * sizeof(float2), 256);
+    int rc = ensure_workspace(ctx, sc_bytes + (size_t)kRSplit * S * E * sizeof(float));
+    if (rc != COLI_OK) return rc;
+    return launch_router_batched(ctx, x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk, routed_scale, idx, w, n_sel,
+                                 reinterpret_cast<float2*>(ctx->ws.base),
+                                 reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ctx->ws.base) + sc_bytes));
+  }
   int rc = ensure_workspace(ctx, align_up((size_t)S * E * sizeof(float2), 256));
   if (rc != COLI_OK) return rc;
   float2* sc_ws = reinterpret_cast<float2*>(ctx->ws.base);
@@ -268,15 +399,20 @@ int launch_router(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const
 // not stall, since cudaMalloc may synchronise the device and a workspace that grows waits for the
 // context's stream first. This entry therefore keeps its scratch in a fixed file-scope device
 // array instead of the context's workspace: the arrival counter in the first 256 bytes, then the
-// (score, choice) pairs of at most kFixedRouterCells (token, expert) cells. Its address is looked
+// (score, choice) pairs of at most kFixedRouterCells (token, expert) cells, then the partial
+// logits of the many-token path. Its address is looked
 // up once per device (the first call on that device); the counter is cleared on the stream before
 // every launch. All contexts on a device share the array, so calls whose kernels could overlap
 // (different streams, contexts or host threads without ordering) race on it.
 // ------------------------------------------------------------------------------------------
 
-constexpr int kFixedRouterCells = 65536;  // S * E limit: 512 KiB of pairs
+constexpr int kFixedRouterCells = 65536;  // S * E limit
 constexpr int kFixedMaxDevices = 64;
-static __device__ __align__(256) unsigned char g_router_fixed[256 + (size_t)kFixedRouterCells * sizeof(float2)];
+// counter (256 B), pairs (512 KiB), partial logits of the many-token path (2 MiB)
+constexpr size_t kFixedPairsOff = 256;
+constexpr size_t kFixedPartOff = kFixedPairsOff + (size_t)kFixedRouterCells * sizeof(float2);
+static __device__ __align__(256) unsigned char
+    g_router_fixed[kFixedPartOff + (size_t)kRSplit * kFixedRouterCells * sizeof(float)];
 
 static std::mutex g_fixed_mu;
 static unsigned char* g_fixed_addr[kFixedMaxDevices];  // device address of g_router_fixed, once set up
@@ -303,7 +439,10 @@ int launch_router_noalloc(coli_ctx* ctx, const void* x, int x_dtype, int S, int 
     }
   }
   unsigned* arrivals = reinterpret_cast<unsigned*>(base);
-  float2* sc_ws = reinterpret_cast<float2*>(base + 256);
+  float2* sc_ws = reinterpret_cast<float2*>(base + kFixedPairsOff);
+  if (S >= kBatchedS)  // the many-token path, as coli_router_select takes it (no arrival counter)
+    return launch_router_batched(ctx, x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk, routed_scale, idx, w, n_sel,
+                                 sc_ws, reinterpret_cast<float*>(base + kFixedPartOff));
   cudaError_t e = cudaMemsetAsync(arrivals, 0, sizeof(unsigned), ctx->stream);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "router_select_noalloc: clear counter");
   int epl = 1;
