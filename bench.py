@@ -37,6 +37,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the tensor-core prefill figure")
     ap.add_argument("--cpu-worker", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -55,6 +56,88 @@ def peaks():
             p = json.load(f)
         return float(p["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def bf16_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
+def prefill_leg(ctx, stream, flush, steps=10, warmup=3):
+    """Config-5 prefill layer (S=512, g64 int4, bf16, Zipf routing) on the tensor-core path:
+    graph-replayed steps with a cold L2, TFLOP/s and HBM bytes of the touched experts."""
+    import numpy as np
+    import torch
+
+    from int4_grouped_expert_router_gb300 import binding as B
+    from int4_grouped_expert_router_gb300.workload import CONFIGS, DeviceLayer, router_host_inputs
+
+    cfg = CONFIGS["prefill"]
+    layer = DeviceLayer(ctx, cfg)
+    n = warmup + steps
+    xs, rs, outs = [], [], []
+    for s in range(n):
+        x, _, _, resid = router_host_inputs(cfg, 500000 + s)
+        xs.append(layer.act_tensor(x))
+        rs.append(layer.act_tensor(resid))
+        outs.append(layer.outputs())
+    for s in range(n):  # eager once (sizes the workspace), then one graph per step
+        layer.step(xs[s], rs[s], outs[s])
+    torch.cuda.synchronize()
+    graphs = []
+    for s in range(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            layer.step(xs[s], rs[s], outs[s])
+        graphs.append(g)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for s in range(n):
+        flush.zero_()
+        ev[s][0].record(stream)
+        graphs[s].replay()
+        ev[s][1].record(stream)
+    torch.cuda.synchronize()
+    assert B.coli_check_error(ctx) == 0, B.coli_last_error(ctx)
+    ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(warmup, n)]
+    del graphs
+    B.coli_profile_enable(ctx, True)
+    for k in (B.COLI_KERNEL_ROUTER, B.COLI_KERNEL_GATEUP, B.COLI_KERNEL_DOWN, B.COLI_KERNEL_COMBINE):
+        B.coli_profile_read(ctx, k)
+    for s in range(warmup, n):
+        flush.zero_()
+        layer.step(xs[s], rs[s], outs[s])
+    kern = {}
+    for name, k in (("router", B.COLI_KERNEL_ROUTER), ("gateup", B.COLI_KERNEL_GATEUP), ("down", B.COLI_KERNEL_DOWN),
+                    ("combine", B.COLI_KERNEL_COMBINE)):
+        t, c = B.coli_profile_read(ctx, k)
+        if c:
+            kern[name] = t * 1000.0 / c
+    B.coli_profile_enable(ctx, False)
+    routes, touched = [], []
+    for s in range(warmup, n):
+        idx = outs[s]["idx"].cpu().numpy()
+        ids = idx[idx >= 0]
+        routes.append(int(ids.size))
+        touched.append(sum(cfg.expert_bytes(int(e)) for e in np.unique(ids)))
+    layer.free()
+    t_ms = statistics.mean(ms)
+    flops = 6.0 * cfg.D * cfg.I * statistics.mean(routes)
+    bpeak, bkind = bf16_peak()
+    hpeak, hkind = peaks()
+    tflops = flops / (t_ms * 1e-3) / 1e12
+    gbs = statistics.mean(touched) / (t_ms * 1e-3) / 1e9
+    mm_us = kern.get("gateup", 0.0) + kern.get("down", 0.0)
+    return {
+        "workload": f"prefill layer S={cfg.S} D={cfg.D} I={cfg.I} E={cfg.E} K={cfg.K}, int4 gs={cfg.gs}, bf16, Zipf routing",
+        "ms_per_layer": t_ms, "steps": steps, "launch": "one CUDA graph per step", "l2": "flushed between steps",
+        "routes": statistics.mean(routes), "gflop": flops / 1e9, "tflops": tflops,
+        "tensor_frac": tflops / bpeak, "tensor_peak_tflops": bpeak, "tensor_peak_kind": f"{bkind} bf16_tflops",
+        "expert_bytes": statistics.mean(touched), "hbm_gbs": gbs, "hbm_frac": gbs / hpeak,
+        "gemm_tflops": flops / (mm_us * 1e-6) / 1e12 if mm_us else None, "kernels_us": kern,
+    }
 
 
 def workload_desc(cfg):
@@ -394,6 +477,14 @@ def gpu_arm(args, rank, world, local):
             "clocks": clock_info,
         }
     layer.free()
+    prefill = None
+    if rank == 0 and not args.no_prefill:
+        try:
+            prefill = prefill_leg(ctx, stream, flush)
+        except Exception as exc:  # the prefill figure must not hide the decode number
+            prefill = {"error": f"{exc}"[:300]}
+    if result is not None:
+        result["prefill"] = prefill
     B.coli_destroy(ctx)
     if dist is not None:
         dist.destroy_process_group()

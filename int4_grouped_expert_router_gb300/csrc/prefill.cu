@@ -28,11 +28,17 @@
 
 namespace coli {
 
-constexpr int kPfRows = 128;    // tokens (GEMM N) per work entry
+#ifndef COLI_PF_ROWS
+#define COLI_PF_ROWS 128
+#endif
+#ifndef COLI_PF_CONV_WARPS
+#define COLI_PF_CONV_WARPS 16
+#endif
+constexpr int kPfRows = COLI_PF_ROWS;  // tokens (GEMM N) per work entry
 constexpr int kPfPad = 16;      // per-entry token blocks are padded to a multiple of 16
 constexpr int kPfKTile = 64;    // K columns per pipeline stage
 constexpr int kPfStages = 3;
-constexpr int kPfConvWarps = 8;  // warps 2..9 convert; warps 4..7 also drain the accumulators
+constexpr int kPfConvWarps = COLI_PF_CONV_WARPS;  // warps 2.. convert; warps 4..7 also drain the accumulator
 constexpr int kPfThreads = (2 + kPfConvWarps) * 32;
 constexpr uint32_t kPfTileBytes = kTcRows * 128;       // one bf16 operand tile: 128 rows x 128 bytes
 constexpr uint32_t kPfPackedBytes = kTcRows * kTcWords * 4;  // one packed int4 weight tile
@@ -193,32 +199,61 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint3
   return d;
 }
 
-// 8 nibbles (columns 8j .. 8j+7) -> 8 bf16 s (n - 8) in the order 0 4 1 5 2 6 3 7.
-__device__ __forceinline__ uint4 pf_dequant8(uint32_t w, __nv_bfloat162 s2) {
-  const __nv_bfloat162 c136 = __floats2bfloat162_rn(136.f, 136.f);
-  uint32_t v[4];
-  v[0] = lop3_and_or(w, 0x000f000fu, 0x43004300u);        // (128 + n0, 128 + n4)
-  v[1] = lop3_and_or(w >> 4, 0x000f000fu, 0x43004300u);   // (n1, n5)
-  v[2] = lop3_and_or(w >> 8, 0x000f000fu, 0x43004300u);   // (n2, n6)
-  v[3] = lop3_and_or(w >> 12, 0x000f000fu, 0x43004300u);  // (n3, n7)
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_splat(float f) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(d) : "f"(f));
+  return d;
+}
+
+constexpr uint32_t kBf16x2_136 = 0x43084308u;  // (136, 136): the magic 128 plus the offset 8
+
+// 8 nibbles (columns 8j .. 8j+7) -> 8 bf16 values s (n - 8) in the order 0 4 1 5 2 6 3 7.
+// (0x4300 | n) is the bf16 number 128 + n; subtracting 136 is exact, the product rounds once.
+__device__ __forceinline__ uint4 pf_dequant8(uint32_t w, uint32_t s2) {
   uint4 o;
-  uint32_t* op = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-  for (int i = 0; i < 4; i++) {
-    __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&v[i]);
-    b = __hmul2(__hsub2(b, c136), s2);  // exact n - 8, then one rounding of the product
-    op[i] = *reinterpret_cast<const uint32_t*>(&b);
-  }
+  o.x = bf16x2_mul(bf16x2_sub(lop3_and_or(w, 0x000f000fu, 0x43004300u), kBf16x2_136), s2);        // (n0, n4)
+  o.y = bf16x2_mul(bf16x2_sub(lop3_and_or(w >> 4, 0x000f000fu, 0x43004300u), kBf16x2_136), s2);   // (n1, n5)
+  o.z = bf16x2_mul(bf16x2_sub(lop3_and_or(w >> 8, 0x000f000fu, 0x43004300u), kBf16x2_136), s2);   // (n2, n6)
+  o.w = bf16x2_mul(bf16x2_sub(lop3_and_or(w >> 12, 0x000f000fu, 0x43004300u), kBf16x2_136), s2);  // (n3, n7)
   return o;
 }
 
 // ------------------------------------------------------------------------------------------
 // Grouped GEMM with the tensor cores: DUAL = gate and up (epilogue SiLU(g) u -> bf16 h rows), else
-// down (epilogue f32 rows of the routed outputs).
-//   warp 0: TMA producer; warp 1: tensor-memory owner and MMA issuer; warps 2..9: converters;
-//   warps 4..7 also read the accumulators (warp w reads tensor-memory lanes 32 (w % 4) ..).
-// Work units are (entry, 128-row weight tile), strided over the persistent grid.
+// down (epilogue f32 rows of the routed outputs). Three rings decouple the latencies:
+//   packed ring (kPkStages): packed int4 tiles, staged by TMA far ahead of their use;
+//   act ring (kActStages): 128-byte-swizzled bf16 activation tiles, staged by TMA;
+//   operand ring (kOpStages): bf16 weight tiles written by the converter warps.
+// warp 0: lane 0 stages packed tiles, lane 1 activation tiles; warp 1: tensor-memory owner, lane 0
+// issues the MMAs; warps 2..9 convert; warps 4..7 also read the accumulators (warp w reads
+// tensor-memory lanes 32 (w % 4) ..). Work units are (entry, 128-row weight tile), strided over
+// the persistent grid; every role walks the same units and K tiles.
 // ------------------------------------------------------------------------------------------
+
+#ifndef COLI_PF_PK_STAGES
+#define COLI_PF_PK_STAGES 6
+#endif
+#ifndef COLI_PF_ACT_STAGES
+#define COLI_PF_ACT_STAGES 3
+#endif
+#ifndef COLI_PF_OP_STAGES
+#define COLI_PF_OP_STAGES 2
+#endif
+constexpr int kPkStages = COLI_PF_PK_STAGES;
+constexpr int kActStages = COLI_PF_ACT_STAGES;
+constexpr int kOpStages = COLI_PF_OP_STAGES;
 
 struct PfGemmParams {
   const ExpertDesc* table;
@@ -235,34 +270,33 @@ struct PfGemmParams {
 template <bool DUAL>
 struct PfLayout {
   static constexpr int kT = DUAL ? 2 : 1;
-  static constexpr uint32_t kA = 0;                                // kT bf16 weight tiles
-  static constexpr uint32_t kAct = kT * kPfTileBytes;             // activation tile (<= 128 rows)
-  static constexpr uint32_t kPacked = kAct + kPfTileBytes;        // kT packed tiles
-  static constexpr uint32_t kStage = kPacked + kT * kPfPackedBytes;
-  static constexpr uint32_t kAccCols = kT * 128;  // tensor-memory columns of one accumulator buffer
-  static constexpr uint32_t kTmemCols = 2 * kAccCols;
-  static_assert(kStage % 1024 == 0, "stage must keep 1024-byte alignment");
+  static constexpr uint32_t kOpStage = kT * kPfTileBytes;            // bf16 weight tiles
+  static constexpr uint32_t kActStage = kPfRows * 128;               // <= kPfRows rows x 128 bytes
+  static constexpr uint32_t kPkStage = kT * kPfPackedBytes;          // packed tiles
+  static constexpr uint32_t kOp = 0;
+  static constexpr uint32_t kAct = kOp + kOpStages * kOpStage;
+  static constexpr uint32_t kPk = kAct + kActStages * kActStage;
+  static constexpr uint32_t kBytes = kPk + kPkStages * kPkStage;
+  static_assert(kAct % 1024 == 0 && kPk % 1024 == 0 && kOpStage % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+  static constexpr uint32_t kAccCols = kT * kPfRows;  // tensor-memory columns of the accumulator
+  static constexpr uint32_t kTmemCols = kAccCols;
 };
 
 struct PfCtrl {
-  uint64_t full[kPfStages];   // TMA bytes of the stage landed
-  uint64_t conv[kPfStages];   // converter warps wrote the stage's bf16 weight tiles
-  uint64_t freed[kPfStages];  // the MMAs reading the stage completed
-  uint64_t acc_full[2];       // accumulator buffer complete
-  uint64_t acc_empty[2];      // accumulator buffer drained by the epilogue warps
-  uint64_t mma_done;          // every MMA of this CTA completed (teardown)
+  uint64_t pk_full[kPkStages], pk_empty[kPkStages];
+  uint64_t act_full[kActStages], act_empty[kActStages];
+  uint64_t op_full[kOpStages], op_empty[kOpStages];
+  uint64_t acc_full;      // accumulator complete
+  uint64_t acc_empty;     // accumulator drained by the epilogue warps
+  uint64_t mma_done;      // every MMA of this CTA completed (teardown)
   uint32_t tmem_base;
   int stop;
 };
+static_assert(sizeof(PfCtrl) <= 1024, "control block");
 
 template <bool DUAL>
 inline size_t pf_smem_bytes() {
-  return 1024 + 1024 + (size_t)kPfStages * PfLayout<DUAL>::kStage;
-}
-
-__device__ __forceinline__ float pf_scale(const float* s, int gs, int G, int row, int col) {
-  if (gs == 0) return __ldg(s + row);
-  return __ldg(s + (size_t)row * G + col / gs);
+  return 1024 + 1024 + PfLayout<DUAL>::kBytes;
 }
 
 __device__ __forceinline__ bool pf_wait(PfCtrl& c, uint64_t* bar, uint32_t parity, int* err) {
@@ -273,25 +307,42 @@ __device__ __forceinline__ bool pf_wait(PfCtrl& c, uint64_t* bar, uint32_t parit
   return false;
 }
 
+// ring position: stage index and phase parity, advanced once per K tile
+struct RingPos {
+  int s = 0;
+  uint32_t ph = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++s == n) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+};
+
 template <bool DUAL>
 __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(PfGemmParams P, const __grid_constant__ CUtensorMap act_map) {
   using Lay = PfLayout<DUAL>;
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   PfCtrl& c = *reinterpret_cast<PfCtrl*>(base);
-  uint8_t* stages = base + 1024;
+  uint8_t* sm = base + 1024;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   if (tid == 0) {
-    for (int s = 0; s < kPfStages; s++) {
-      mbar_init(&c.full[s], 1);
-      mbar_init(&c.conv[s], kPfConvWarps);
-      mbar_init(&c.freed[s], 1);
+    for (int s = 0; s < kPkStages; s++) {
+      mbar_init(&c.pk_full[s], 1);
+      mbar_init(&c.pk_empty[s], kPfConvWarps);
     }
-    for (int b = 0; b < 2; b++) {
-      mbar_init(&c.acc_full[b], 1);
-      mbar_init(&c.acc_empty[b], 4);
+    for (int s = 0; s < kActStages; s++) {
+      mbar_init(&c.act_full[s], 1);
+      mbar_init(&c.act_empty[s], 1);
     }
+    for (int s = 0; s < kOpStages; s++) {
+      mbar_init(&c.op_full[s], kPfConvWarps);
+      mbar_init(&c.op_empty[s], 1);
+    }
+    mbar_init(&c.acc_full, 1);
+    mbar_init(&c.acc_empty, 4);
     mbar_init(&c.mma_done, 1);
     c.stop = 0;
     mbar_fence_init();
@@ -305,148 +356,175 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(PfGemmParams P, 
   const int n_units = *P.n_entries * P.tiles;
   const int nkt = (P.K + kPfKTile - 1) / kPfKTile;
 
-  if (warp == 0) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      long long issued = 0;
-      for (int u = blockIdx.x; u < n_units && !ld_volatile_int(&c.stop); u += gridDim.x) {
-        const PfEntry en = P.entries[u / P.tiles];
-        const int t = u % P.tiles;
-        const ExpertDesc& ed = P.table[en.e];
-        for (int kt = 0; kt < nkt; kt++) {
-          if (!pf_wait(c, &c.freed[stage], phase ^ 1u, P.err)) break;
-          uint8_t* st = stages + (size_t)stage * Lay::kStage;
-          mbar_arrive_expect_tx(&c.full[stage], Lay::kT * kPfPackedBytes + (uint32_t)en.npad * 128u);
-          tma_load_2d(st + Lay::kPacked, &ed.t[P.t0].map_tc, kt * kTcWords, t * kTcRows, &c.full[stage]);
-          if (DUAL)
-            tma_load_2d(st + Lay::kPacked + kPfPackedBytes, &ed.t[P.t1].map_tc, kt * kTcWords, t * kTcRows, &c.full[stage]);
+  if (warp == 0 && lane < 2) {
+    // ---------------- TMA producers: lane 0 packed tiles, lane 1 activation tiles ----------------
+    const bool packed = lane == 0;
+    const int nst = packed ? kPkStages : kActStages;
+    uint64_t* fullb = packed ? c.pk_full : c.act_full;
+    uint64_t* emptyb = packed ? c.pk_empty : c.act_empty;
+    RingPos rp;
+    long long issued = 0;
+    for (int u = blockIdx.x; u < n_units && !ld_volatile_int(&c.stop); u += gridDim.x) {
+      const PfEntry en = P.entries[u / P.tiles];
+      const int t = u % P.tiles;
+      const ExpertDesc& ed = P.table[en.e];
+      for (int kt = 0; kt < nkt; kt++) {
+        if (!pf_wait(c, &emptyb[rp.s], rp.ph ^ 1u, P.err)) break;
+        if (packed) {
+          uint8_t* st = sm + Lay::kPk + (size_t)rp.s * Lay::kPkStage;
+          mbar_arrive_expect_tx(&fullb[rp.s], Lay::kPkStage);
+          tma_load_2d(st, &ed.t[P.t0].map_tc, kt * kTcWords, t * kTcRows, &fullb[rp.s]);
+          if (DUAL) tma_load_2d(st + kPfPackedBytes, &ed.t[P.t1].map_tc, kt * kTcWords, t * kTcRows, &fullb[rp.s]);
+        } else {
+          uint8_t* st = sm + Lay::kAct + (size_t)rp.s * Lay::kActStage;
+          mbar_arrive_expect_tx(&fullb[rp.s], (uint32_t)en.npad * 128u);
           for (int j = 0; j < en.npad; j += 16)
-            tma_load_2d(st + Lay::kAct + (uint32_t)j * 128u, &act_map, kt * kPfKTile, en.row0 + j, &c.full[stage]);
-          issued++;
-          if (++stage == kPfStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+            tma_load_2d(st + (uint32_t)j * 128u, &act_map, kt * kPfKTile, en.row0 + j, &fullb[rp.s]);
         }
+        issued++;
+        rp.next(nst);
       }
-      // after a timeout elsewhere, never leave with copies in flight: wait (bounded) for the last
-      // issued phase of every stage
-      if (ld_volatile_int(&c.stop))
-        for (long long q = issued > kPfStages ? issued - kPfStages : 0; q < issued; q++)
-          (void)mbar_wait(&c.full[q % kPfStages], (uint32_t)((q / kPfStages) & 1));
     }
+    // after a timeout elsewhere, never leave with copies in flight: wait (bounded) for the last
+    // issued phase of every stage
+    if (ld_volatile_int(&c.stop))
+      for (long long q = issued > nst ? issued - nst : 0; q < issued; q++)
+        (void)mbar_wait(&fullb[q % nst], (uint32_t)((q / nst) & 1));
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
+      RingPos ra, ro;
       int lu = 0;
       for (int u = blockIdx.x; u < n_units && !ld_volatile_int(&c.stop); u += gridDim.x, lu++) {
         const PfEntry en = P.entries[u / P.tiles];
-        const int buf = lu & 1;
         const uint32_t idesc = bf16_f32_idesc(128, (uint32_t)en.npad);
-        if (!pf_wait(c, &c.acc_empty[buf], (((uint32_t)lu >> 1) & 1u) ^ 1u, P.err)) break;
+        if (!pf_wait(c, &c.acc_empty, ((uint32_t)lu & 1u) ^ 1u, P.err)) break;
         tc_fence_after_sync();
         bool ok = true;
         for (int kt = 0; kt < nkt; kt++) {
-          if (!pf_wait(c, &c.full[stage], phase, P.err) || !pf_wait(c, &c.conv[stage], phase, P.err)) {
+          if (!pf_wait(c, &c.act_full[ra.s], ra.ph, P.err) || !pf_wait(c, &c.op_full[ro.s], ro.ph, P.err)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          uint8_t* st = stages + (size_t)stage * Lay::kStage;
-          const uint64_t bdesc = sw128_kmajor_desc(st + Lay::kAct);
+          const uint64_t bdesc = sw128_kmajor_desc(sm + Lay::kAct + (size_t)ra.s * Lay::kActStage);
 #pragma unroll
           for (int x = 0; x < Lay::kT; x++) {
-            const uint64_t adesc = sw128_kmajor_desc(st + Lay::kA + x * kPfTileBytes);
-            const uint32_t dcol = tmem + (uint32_t)buf * Lay::kAccCols + (uint32_t)(x * 128);
+            const uint64_t adesc = sw128_kmajor_desc(sm + Lay::kOp + (size_t)ro.s * Lay::kOpStage + x * kPfTileBytes);
+            const uint32_t dcol = tmem + (uint32_t)(x * kPfRows);
 #pragma unroll
             for (int ks = 0; ks < kPfKTile / 16; ks++)
               tc_mma_bf16(dcol, adesc + 2 * ks, bdesc + 2 * ks, idesc, kt > 0 || ks > 0);
           }
-          tc_commit(&c.freed[stage]);
-          if (++stage == kPfStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          tc_commit(&c.act_empty[ra.s]);
+          tc_commit(&c.op_empty[ro.s]);
+          ra.next(kActStages);
+          ro.next(kOpStages);
         }
         if (!ok) break;
-        tc_commit(&c.acc_full[buf]);
+        tc_commit(&c.acc_full);
       }
       tc_commit(&c.mma_done);  // teardown: tensor memory is released only after every MMA
       if (!mbar_wait(&c.mma_done, 0)) set_error(P.err, COLI_E_TIMEOUT);
     }
-  } else {
+  } else if (warp >= 2) {
     // ---------------- converters (+ epilogue on warps 4..7) ----------------
-    const int cw = warp - 2;                 // converter warp 0..7
-    const int ct = cw * 32 + lane;           // converter thread 0..255
-    // DUAL: thread ct converts all 8 words of row ct % 128 of tensor ct / 128.
-    // single: thread ct converts words 4 h .. 4 h + 3 (h = ct / 128) of row ct % 128.
+    const int ct = (warp - 2) * 32 + lane;   // converter thread 0..511
+    // kParts threads share a row of a tensor: thread ct converts words w0 .. w0 + kW - 1 (w0 = kW
+    // ((ct / 128) % kParts)) of row ct % 128 of tensor ct / (128 kParts).
+    constexpr int kParts = kPfConvWarps * 32 / (Lay::kT * kTcRows);
+    constexpr int kW = kTcWords / kParts;
+    static_assert(kParts * kW == kTcWords && kW >= 2, "converter split");
     const int r = ct & (kTcRows - 1);
-    const int x = DUAL ? (ct >> 7) : 0;
-    const int w0 = DUAL ? 0 : (ct >> 7) * 4;
-    constexpr int kW = DUAL ? 8 : 4;
+    const int x = DUAL ? ct / (kTcRows * kParts) : 0;
+    const int w0 = ((ct / kTcRows) % kParts) * kW;
     const bool epi = warp >= 4 && warp < 8;
     const int q = warp & 3;                  // tensor-memory lane quarter of an epilogue warp
-    int stage = 0;
-    uint32_t phase = 0;
+    const uint32_t swz = (uint32_t)(r & 7);
+    RingPos rp, ro;
     int lu = 0;
     for (int u = blockIdx.x; u < n_units && !ld_volatile_int(&c.stop); u += gridDim.x, lu++) {
       const PfEntry en = P.entries[u / P.tiles];
       const int t = u % P.tiles;
       const TensorDesc& td = P.table[en.e].t[x == 0 ? P.t0 : P.t1];
-      const float* sp = td.s;
-      const int gs = td.gs, G = td.G;
-      const int row = t * kTcRows + r;
+      const int gs = td.gs, row = t * kTcRows + r;
       const bool row_ok = row < P.rows;
+      const float* srow = row_ok ? td.s + (gs == 0 ? (size_t)row : (size_t)row * td.G) : nullptr;
+      // this thread's 32-column half of every K tile: columns c0 + 8 w0 .. + 8 kW - 1 (gs is 0 or a
+      // multiple of 32, so the half has one scale); its group advances incrementally
+      const int hoff = 8 * w0;
+      int grp = 0, nb = gs > 0 ? gs : 0;
+      auto scale_of = [&](int col) -> float {
+        if (!row_ok || col >= P.K) return 0.f;
+        if (gs == 0) return __ldg(srow);
+        while (col >= nb) {
+          grp++;
+          nb += gs;
+        }
+        return __ldg(srow + grp);
+      };
+      float s_next0 = scale_of(hoff), s_next1 = nkt > 1 ? scale_of(kPfKTile + hoff) : 0.f;  // two K tiles ahead
       bool ok = true;
       for (int kt = 0; kt < nkt; kt++) {
-        if (!pf_wait(c, &c.full[stage], phase, P.err)) {
+        const uint32_t s2 = bf16x2_splat(s_next0);
+        s_next0 = s_next1;
+        s_next1 = kt + 2 < nkt ? scale_of((kt + 2) * kPfKTile + hoff) : 0.f;
+        if (!pf_wait(c, &c.pk_full[rp.s], rp.ph, P.err) || !pf_wait(c, &c.op_empty[ro.s], ro.ph ^ 1u, P.err)) {
           ok = false;
           break;
         }
-        uint8_t* st = stages + (size_t)stage * Lay::kStage;
-        const uint32_t* pk = reinterpret_cast<const uint32_t*>(st + Lay::kPacked + x * kPfPackedBytes + r * (kTcWords * 4));
-        uint8_t* arow = st + Lay::kA + x * kPfTileBytes + r * 128;
-        const int c0 = kt * kPfKTile;
-        __nv_bfloat162 s_lo = __floats2bfloat162_rn(0.f, 0.f), s_hi = s_lo;
-        if (row_ok) {
-          const float a = c0 < P.K ? pf_scale(sp, gs, G, row, c0) : 0.f;
-          const float b = c0 + 32 < P.K ? pf_scale(sp, gs, G, row, c0 + 32) : 0.f;
-          s_lo = __floats2bfloat162_rn(a, a);
-          s_hi = __floats2bfloat162_rn(b, b);
-        }
+        const uint8_t* pk = sm + Lay::kPk + (size_t)rp.s * Lay::kPkStage + x * kPfPackedBytes + r * (kTcWords * 4) + w0 * 4;
+        uint8_t* arow = sm + Lay::kOp + (size_t)ro.s * Lay::kOpStage + x * kPfTileBytes + r * 128;
+        uint32_t wv[kW];
+        if (kW >= 4) {
 #pragma unroll
-        for (int j = 0; j < kW; j++) {
-          const int wj = w0 + j;
-          uint4 o = make_uint4(0, 0, 0, 0);
-          if (row_ok && c0 + 8 * wj < P.K) o = pf_dequant8(pk[wj], wj < 4 ? s_lo : s_hi);
-          *reinterpret_cast<uint4*>(arow + ((wj ^ (r & 7)) << 4)) = o;
+          for (int j = 0; j < kW; j += 4) {
+            const uint4 v = lds128(pk + 4 * j);
+            wv[j] = v.x;
+            wv[(j + 1) % kW] = v.y;
+            wv[(j + 2) % kW] = v.z;
+            wv[(j + 3) % kW] = v.w;
+          }
+        } else {
+          uint2 v;
+          asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_u32(pk)) : "memory");
+          wv[0] = v.x;
+          wv[kW - 1] = v.y;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&c.pk_empty[rp.s]);  // packed words are in registers
+        const int c0 = kt * kPfKTile + hoff;
+        if (row_ok && c0 + 8 * kW <= P.K) {  // whole half inside the matrix
+#pragma unroll
+          for (int j = 0; j < kW; j++)
+            *reinterpret_cast<uint4*>(arow + (((uint32_t)(w0 + j) ^ swz) << 4)) = pf_dequant8(wv[j], s2);
+        } else {
+#pragma unroll
+          for (int j = 0; j < kW; j++) {
+            uint4 o = make_uint4(0, 0, 0, 0);
+            if (row_ok && c0 + 8 * j < P.K) o = pf_dequant8(wv[j], s2);
+            *reinterpret_cast<uint4*>(arow + (((uint32_t)(w0 + j) ^ swz) << 4)) = o;
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&c.conv[stage]);
-        if (++stage == kPfStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        if (lane == 0) mbar_arrive(&c.op_full[ro.s]);
+        rp.next(kPkStages);
+        ro.next(kOpStages);
       }
       if (!ok) break;
       if (epi) {
         // ---------------- epilogue of this unit ----------------
-        const int buf = lu & 1;
-        if (!pf_wait(c, &c.acc_full[buf], ((uint32_t)lu >> 1) & 1u, P.err)) break;
+        if (!pf_wait(c, &c.acc_full, (uint32_t)lu & 1u, P.err)) break;
         tc_fence_after_sync();
         const int orow = t * kTcRows + q * 32 + lane;  // weight row this lane holds
-        const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)buf * Lay::kAccCols;
+        const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
         for (int n0 = 0; n0 < en.npad; n0 += 16) {
           float a[16];
           tmem_ld16(tl + (uint32_t)n0, a);
           if (DUAL) {
             float b[16];
-            tmem_ld16(tl + 128u + (uint32_t)n0, b);
+            tmem_ld16(tl + (uint32_t)kPfRows + (uint32_t)n0, b);
             if (orow < P.rows) {
               uint16_t* h = static_cast<uint16_t*>(P.out);
               const int pcol = (orow & ~7) + pf_perm8(orow & 7);
@@ -467,7 +545,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(PfGemmParams P, 
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&c.acc_empty[buf]);
+        if (lane == 0) mbar_arrive(&c.acc_empty);
       }
     }
   }

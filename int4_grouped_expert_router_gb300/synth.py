@@ -176,9 +176,9 @@ def zipf_bias(seed: int, E: int, s: float = 1.1, lam: float = 0.25) -> np.ndarra
     return (base + lam * np.log(p)).astype(np.float32)
 
 
-def router_inputs(seed: int, S: int, D: int, E: int, zipf: bool = False):
-    """x ~ N(0,1) [S x D] f32, Wr ~ N(0, 0.02^2) [E x D] f32, bias [E] f32."""
+def router_inputs(seed: int, S: int, D: int, E: int, zipf: bool = False, zipf_lambda: float = 0.25):
+    """x ~ N(0,1) [S x D] f32, Wr ~ N(0, 0.02^2) [E x D] f32, bias [E] f32 (Zipf-skewed if zipf)."""
     x = normal(stream_seed(seed, "x"), S * D).reshape(S, D)
     Wr = normal(stream_seed(seed, "Wr"), E * D, std=0.02).reshape(E, D)
-    bias = zipf_bias(seed, E) if zipf else uniform(stream_seed(seed, "bias"), E, -0.1, 0.1)
+    bias = zipf_bias(seed, E, lam=zipf_lambda) if zipf else uniform(stream_seed(seed, "bias"), E, -0.1, 0.1)
     return x, Wr, bias

@@ -31,6 +31,7 @@ class LayerConfig:
     norm_topk: bool = True
     routed_scale: float = 2.5
     zipf: bool = False
+    zipf_lambda: float = 0.25  # strength of the popularity bias (lambda ln p_rank)
     seed: int = synth.BASE_SEED
 
     def gs_of(self, e: int) -> int:
@@ -53,7 +54,9 @@ CONFIGS = {
     "decode_g64": LayerConfig("decode_g64", D=6144, I=2048, E=256, K=8, gs="mixed:64", topp=0.9),
     "decode_g64_tail": LayerConfig("decode_g64_tail", D=6144, I=2000, E=256, K=8, gs=64, topp=0.9),
     "decode_s4_bf16": LayerConfig("decode_s4_bf16", D=6144, I=2048, E=256, K=8, S=4, x_dtype="bf16", zipf=True),
-    "prefill": LayerConfig("prefill", D=6144, I=2048, E=256, K=8, S=512, gs=64, x_dtype="bf16", zipf=True),
+    # lambda 0.05: 4096 routes over ~150 experts, at most ~130 rows each (0.25 would put them on ~44)
+    "prefill": LayerConfig("prefill", D=6144, I=2048, E=256, K=8, S=512, gs=64, x_dtype="bf16", zipf=True,
+                           zipf_lambda=0.05),
 }
 
 
@@ -73,7 +76,7 @@ def host_expert(cfg: LayerConfig, e: int):
 
 def router_host_inputs(cfg: LayerConfig, token0: int = 0):
     """x [S x D] f32 (bf16-representable when x_dtype is bf16), Wr [E x D], bias [E] for a batch."""
-    _, Wr, bias = synth.router_inputs(cfg.seed, 1, cfg.D, cfg.E, zipf=cfg.zipf)
+    _, Wr, bias = synth.router_inputs(cfg.seed, 1, cfg.D, cfg.E, zipf=cfg.zipf, zipf_lambda=cfg.zipf_lambda)
     x = synth.normal(synth.stream_seed(cfg.seed, "tokens", token0), cfg.S * cfg.D).reshape(cfg.S, cfg.D)
     if cfg.x_dtype == "bf16":
         x = synth.bf16_bits_to_f32(synth.to_bf16_bits(x))
@@ -104,7 +107,7 @@ class DeviceLayer:
                 del p, s
             B.coli_expert_table_set(ctx, e, *hs)
             self.handles.append(hs)
-        _, Wr, bias = synth.router_inputs(cfg.seed, 1, cfg.D, cfg.E, zipf=cfg.zipf)
+        _, Wr, bias = synth.router_inputs(cfg.seed, 1, cfg.D, cfg.E, zipf=cfg.zipf, zipf_lambda=cfg.zipf_lambda)
         self.Wr = torch.from_numpy(Wr).to(device)
         self.bias = torch.from_numpy(bias).to(device)
 

@@ -39,3 +39,30 @@ def test_full_shape_layer(ctx, name, tokens):
             assert near <= 1
     finally:
         layer.free()
+
+
+def test_full_shape_prefill_tensor_core_path(ctx):
+    """S=512 tokens, g64 int4, bf16, Zipf routing: the tensor-core path. Router checked on every
+    token; the FFN on sampled tokens (bf16 tensor-core tolerance: see test_gpu_prefill)."""
+    from test_gpu_prefill import TC_NORM, TC_RTOL, tc_atol
+
+    cfg = CONFIGS["prefill"]
+    layer = DeviceLayer(ctx, cfg)
+    try:
+        x, Wr, bias, resid = router_host_inputs(cfg, 7)
+        out = layer.outputs()
+        xt, rt = layer.act_tensor(x), layer.act_tensor(resid)
+        layer.step(xt, rt, out)
+        assert B.coli_check_error(ctx) == 0, B.coli_last_error(ctx)
+        idx, w, n, y = (to_np(out[k]) for k in ("idx", "w", "n_sel", "y"))
+        xb, rb = to_np(xt), to_np(rt)
+        near, _ = check_router(idx, w, n, xb, Wr, bias, cfg.K, cfg.topp, cfg.norm_topk, cfg.routed_scale)
+        assert near <= 3
+        rows = np.bincount(idx[idx >= 0].reshape(-1), minlength=cfg.E)
+        sel = [0, 137, 511]
+        ref = ffn_reference(cfg, xb[sel], idx[sel], w[sel], n[sel], rb[sel])
+        stats = assert_close(y[sel], ref, TC_RTOL, tc_atol(ref), "prefill")
+        assert stats["norm_rel"] < TC_NORM, stats
+        print("prefill near-ties", near, "experts touched", int((rows > 0).sum()), "max rows", int(rows.max()), stats)
+    finally:
+        layer.free()
