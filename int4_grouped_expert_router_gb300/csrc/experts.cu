@@ -294,6 +294,10 @@ struct GroupParams {
 // ------------------------------------------------------------------------------------------
 
 constexpr int kDStages = 4;  // stages per warp ring of the down kernel
+#ifndef COLI_DOWN_PRE_STAGES
+#define COLI_DOWN_PRE_STAGES 2
+#endif
+constexpr int kDPreStages = COLI_DOWN_PRE_STAGES;  // of them issued before the wait for h
 constexpr int kSeg = 64;          // rows (down) or row pairs (gate/up) finished together
 constexpr int kRouteCache = 16;   // routes resolved once into shared memory
 
@@ -313,6 +317,7 @@ struct RouteSlot {
 };
 
 __device__ __forceinline__ void fill_slot_tensor(SlotTensor& st, const TensorDesc* d) {
+  prefetch_tensormap(&d->map_w);  // the first TMA load of this tensor follows shortly
   st.d = d;
   st.s = d->s;
   st.w = d->w;
@@ -651,21 +656,6 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 192 ? kGUMinCtas : 1) gateup_ker
     named_sync(1, W * 32);  // the partial buffers are reused by the next segment
     if (any_stop) stop = true;
   }
-  // S == 1: this CTA's share of the kept slots' down rows (and scales) goes to L2 for the down
-  // kernel, which starts only when every gate/up CTA has finished.
-  if (P.S == 1 && tid == 0 && !stop) {
-    const long long tot = (long long)R * P.D;
-    const long long a = (long long)blockIdx.x * tot / gridDim.x, b = (long long)(blockIdx.x + 1) * tot / gridDim.x;
-    for (long long j = a / P.D; j < R && j * P.D < b; j++) {
-      const int e = sm.e_spec[j];
-      if (e < 0 || e >= COLI_MAX_EXPERTS) continue;
-      const TensorDesc* td = &P.table[e].t[T_DOWN];
-      if (!P.table[e].valid) continue;
-      const long long r0 = max(a, j * P.D) - j * P.D, r1 = min(b, (j + 1) * P.D) - j * P.D;
-      prefetch_range_l2(td->w + (size_t)r0 * td->pitch, (size_t)(r1 - r0) * td->pitch);
-      prefetch_range_l2(td->s + (size_t)r0 * td->G, (size_t)(r1 - r0) * td->G * sizeof(float));
-    }
-  }
   // never leave with TMA loads in flight into this warp's ring (the last issued phases)
   if (lane == 0)
     for (int q = issued > kGUStages ? issued - kGUStages : 0; q < issued; q++)
@@ -752,7 +742,7 @@ __global__ void __launch_bounds__(MAXT, 1) down_fused_kernel(GroupParams P, int 
     issued++;
   };
   if (warp_on && lane == 0)
-    for (int s = 0; s < kDStages / 2; s++) issue_next();  // the weight stream starts before h is ready
+    for (int s = 0; s < kDPreStages; s++) issue_next();  // the weight stream starts before h is ready
 
   LaneTensor lt;
   lane_tensor(lt, *sl, c);
@@ -763,7 +753,7 @@ __global__ void __launch_bounds__(MAXT, 1) down_fused_kernel(GroupParams P, int 
   load_chunk_f32(P.h, COLI_DTYPE_F32, (size_t)k * P.I, 32 * c, active ? P.I : 0, hv);
   if (!make_limbs(hv, L) && active) set_error(P.err, COLI_E_NONFINITE);
   if (warp_on && lane == 0)  // the rest of the ring once h has arrived (its loads go first)
-    for (int s = kDStages / 2; s < kDStages; s++) issue_next();
+    for (int s = kDPreStages; s < kDStages; s++) issue_next();
 
   uint32_t b = 0;
   bool stop = false;

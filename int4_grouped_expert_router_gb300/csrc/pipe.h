@@ -111,26 +111,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, i
 
 __device__ __forceinline__ int ld_volatile_int(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
 
+// Bring a TMA descriptor (in global memory) into the copy engine's descriptor cache ahead of use.
+__device__ __forceinline__ void prefetch_tensormap(const void* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
 // Prefetch one 128-byte line into L2 (a hint; no fault on any address of a live allocation).
 __device__ __forceinline__ void prefetch_l2_line(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
-// Bulk prefetch of [p, p + bytes) into L2 by the copy engine: p 16-byte aligned, bytes a multiple
-// of 16. Completion is not tracked (a later load of the same lines hits L2 or joins the request).
-__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
-// Prefetch the 16-byte-aligned interior of [p, p + bytes) in pieces of at most 64 KiB; the range
-// must lie inside one allocation.
-__device__ __forceinline__ void prefetch_range_l2(const void* p, size_t bytes) {
-  uintptr_t a = (reinterpret_cast<uintptr_t>(p) + 15) & ~uintptr_t(15);
-  const uintptr_t end = (reinterpret_cast<uintptr_t>(p) + bytes) & ~uintptr_t(15);
-  for (; a < end; a += 65536) {
-    const uintptr_t n = end - a < 65536 ? end - a : 65536;
-    bulk_prefetch_l2(reinterpret_cast<const void*>(a), (uint32_t)n);
-  }
 }
 
 // Programmatic dependent launch: wait for the preceding grid's completion and memory flush /// Programmatic dependent launch: wait for the preceding grid's completion and memory flush /

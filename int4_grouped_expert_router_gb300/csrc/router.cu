@@ -15,7 +15,10 @@
 namespace coli {
 
 constexpr int kRouterThreads = 256;
-constexpr int kRowsPerCta = 2;  // E = 256 -> 128 CTAs, every row group in flight at once
+#ifndef COLI_ROUTER_ROWS
+#define COLI_ROUTER_ROWS 1
+#endif
+constexpr int kRowsPerCta = COLI_ROUTER_ROWS;  // E = 256 -> 256 CTAs, every row in flight at once
 
 // Order-preserving map of a finite binary32 value to uint32 (larger float -> larger integer;
 // -0 is folded onto +0 so that the two compare equal, as floats do).
