@@ -140,6 +140,27 @@ def prefill_leg(ctx, stream, flush, steps=10, warmup=3):
     }
 
 
+def token_seed(rank: int, step: int) -> int:
+    """Seed of the token a rank processes at a step: every rank (replica) gets its own tokens."""
+    return rank * 100000 + step
+
+
+def max_over_ranks(value: float, dist, device: str) -> float:
+    """The largest value over the ranks (the job takes as long as its slowest rank)."""
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_us_per_layer(total_ms: float, steps: int, world: int) -> float:
+    """Whole-job time per layer: every rank ran `steps` layers within `total_ms` (max over ranks)."""
+    return total_ms * 1000.0 / (steps * world)
+
+
 def workload_desc(cfg):
     return (f"MoE decode layer D={cfg.D} I={cfg.I} E={cfg.E} resident experts K={cfg.K} S={cfg.S}, "
             f"int4 gs={cfg.gs}, {cfg.x_dtype} activations, top-p={cfg.topp}")
@@ -301,7 +322,7 @@ def gpu_arm(args, rank, world, local):
     # per-step inputs, resident on the device before timing (each rank its own tokens)
     xs, rs = [], []
     for s in range(n_tok):
-        x, _, _, resid = router_host_inputs(cfg, rank * 100000 + s)
+        x, _, _, resid = router_host_inputs(cfg, token_seed(rank, s))
         xs.append(layer.act_tensor(x))
         rs.append(layer.act_tensor(resid))
     outs = [layer.outputs() for _ in range(n_tok)]
@@ -363,12 +384,8 @@ def gpu_arm(args, rank, world, local):
     assert B.coli_check_error(ctx) == 0, B.coli_last_error(ctx)
     step_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.warmup, n_tok)]
     del graphs
-    total_ms = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    us_per_layer = total_ms * 1000.0 / (args.steps * world)
+    total_ms = max_over_ranks(sum(step_ms), dist, "cuda")
+    us_per_layer = job_us_per_layer(total_ms, args.steps, world)
 
     # bytes each step had to read: the kept experts' packed weights + scales
     expert_bytes = []
@@ -432,12 +449,8 @@ def gpu_arm(args, rank, world, local):
         hy[s].copy_(outs[s]["y"], non_blocking=True)
         e2e_ev[s][1].record(stream)
     barrier()
-    e2e_ms = sum(e2e_ev[s][0].elapsed_time(e2e_ev[s][1]) for s in range(args.warmup, n_tok))
-    if dist is not None:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_us = e2e_ms * 1000.0 / (args.steps * world)
+    e2e_ms = max_over_ranks(sum(e2e_ev[s][0].elapsed_time(e2e_ev[s][1]) for s in range(args.warmup, n_tok)), dist, "cuda")
+    e2e_us = job_us_per_layer(e2e_ms, args.steps, world)
     h2d = xs[0].numel() * xs[0].element_size() + rs[0].numel() * rs[0].element_size()
     d2h = outs[0]["y"].numel() * outs[0]["y"].element_size()
 
