@@ -140,7 +140,7 @@ static int make_desc(coli_ctx* ctx, HostTensor& t) {
     cuuint32_t box[2] = {(cuuint32_t)kTcWords, (cuuint32_t)kTcRows};
     cuuint32_t es[2] = {1, 1};
     CUresult r = enc(&d.map_tc, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, t.w, dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(ctx, COLI_E_CUDA, "upload: tensor-core tile map encoding failed");
   }

@@ -22,16 +22,17 @@ constexpr int kBoxRows = 4;
 constexpr int kSliceWords = 128;
 // Chunk-group scales of one warp's slice that travel by TMA (group sizes 64..256).
 constexpr int kScaleBox = 16;
-// Tensor-core (prefill) weight tiles: 128 rows x 64 columns (8 words of packed nibbles).
+// Tensor-core (prefill) weight tiles: 128 rows x 256 columns (32 words = 128 bytes of packed
+// nibbles per row, staged with the 128-byte swizzle), four 64-column K tiles of the MMA.
 constexpr int kTcRows = 128;
-constexpr int kTcWords = 8;
+constexpr int kTcWords = 32;
 
 // One uploaded int4 tensor as the kernels see it. Rows are padded to a whole number of 16-byte
 // chunks (32 columns each); padding nibbles hold 8, i.e. the value 0.
 struct TensorDesc {
   CUtensorMap map_w;   // 2-D map over the weights as uint32 [rows x pitch/4], box [box_rows x box_w]
   CUtensorMap map_s;   // 2-D map over chunk-group scales f32 [rows x G], box [box_rows x box_s]
-  CUtensorMap map_tc;  // 2-D map over the weights as uint32 [rows x pitch/4], box [kTcRows x kTcWords]
+  CUtensorMap map_tc;  // 2-D map over the weights as uint32 [rows x pitch/4], box [kTcRows x kTcWords], 128B swizzle
   const uint8_t* w;    // rows x pitch bytes
   const float* s;      // scales: rows (gs == 0) or rows * G (gs > 0)
   uint32_t pitch;      // bytes per row, multiple of 16

@@ -109,6 +109,22 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, i
       : "memory");
 }
 
+// Same, with an L2 cache policy (from createpolicy) for the lines the copy brings in.
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const void* map, int x, int y, uint64_t* bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 __device__ __forceinline__ int ld_volatile_int(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
 
 // Bring a TMA descriptor (in global memory) into the copy engine's descriptor cache ahead of use.

@@ -38,10 +38,11 @@ constexpr int kPfRows = COLI_PF_ROWS;  // tokens (GEMM N) per work entry
 constexpr int kPfPad = 16;      // per-entry token blocks are padded to a multiple of 16
 constexpr int kPfKTile = 64;    // K columns per pipeline stage
 constexpr int kPfStages = 3;
-constexpr int kPfConvWarps = COLI_PF_CONV_WARPS;  // warps 2.. convert; warps 4..7 also drain the accumulator
-constexpr int kPfThreads = (2 + kPfConvWarps) * 32;
+constexpr int kPfConvWarps = COLI_PF_CONV_WARPS;  // warps 3.. convert; warps 4..7 also drain the accumulator
+constexpr int kPfThreads = (3 + kPfConvWarps) * 32;  // + the two producer warps and the MMA warp
 constexpr uint32_t kPfTileBytes = kTcRows * 128;       // one bf16 operand tile: 128 rows x 128 bytes
-constexpr uint32_t kPfPackedBytes = kTcRows * kTcWords * 4;  // one packed int4 weight tile
+constexpr uint32_t kPfPackedBytes = kTcRows * kTcWords * 4;  // one packed int4 weight tile (4 K tiles)
+constexpr int kPfSuper = kTcWords * 8 / kPfKTile;            // K tiles per packed tile
 
 // position of column c (0..7) of an 8-column group in the tensor-core K order
 __host__ __device__ constexpr int pf_perm8(int c) { return c < 4 ? 2 * c : 2 * (c - 4) + 1; }
@@ -236,14 +237,15 @@ __device__ __forceinline__ uint4 pf_dequant8(uint32_t w, uint32_t s2) {
 //   packed ring (kPkStages): packed int4 tiles, staged by TMA far ahead of their use;
 //   act ring (kActStages): 128-byte-swizzled bf16 activation tiles, staged by TMA;
 //   operand ring (kOpStages): bf16 weight tiles written by the converter warps.
-// warp 0: lane 0 stages packed tiles, lane 1 activation tiles; warp 1: tensor-memory owner, lane 0
-// issues the MMAs; warps 2..9 convert; warps 4..7 also read the accumulators (warp w reads
+// warp 0 stages packed tiles; warp 1 owns tensor memory, its lane 0 issues the MMAs; warp 2 stages
+// activation tiles (each producer has a warp of its own, so neither waits while the other sleeps
+// in a barrier wait); warps 3.. convert; warps 4..7 also read the accumulators (warp w reads
 // tensor-memory lanes 32 (w % 4) ..). Work units are (entry, 128-row weight tile), strided over
 // the persistent grid; every role walks the same units and K tiles.
 // ------------------------------------------------------------------------------------------
 
 #ifndef COLI_PF_PK_STAGES
-#define COLI_PF_PK_STAGES 6
+#define COLI_PF_PK_STAGES 3
 #endif
 #ifndef COLI_PF_ACT_STAGES
 #define COLI_PF_ACT_STAGES 3
@@ -299,9 +301,25 @@ inline size_t pf_smem_bytes() {
   return 1024 + 1024 + PfLayout<DUAL>::kBytes;
 }
 
+#ifndef COLI_PF_POLL
+#define COLI_PF_POLL 0
+#endif
+// Wait for a ring barrier; COLI_PF_POLL polls try_wait without a suspend-time hint.
+__device__ __forceinline__ bool pf_mbar_wait(uint64_t* bar, uint32_t parity) {
+#if COLI_PF_POLL
+  if (mbar_test_parity(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_test_parity(bar, parity))
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  return true;
+#else
+  return mbar_wait(bar, parity);
+#endif
+}
+
 __device__ __forceinline__ bool pf_wait(PfCtrl& c, uint64_t* bar, uint32_t parity, int* err) {
   if (ld_volatile_int(&c.stop)) return false;
-  if (mbar_wait(bar, parity)) return true;
+  if (pf_mbar_wait(bar, parity)) return true;
   set_error(err, COLI_E_TIMEOUT);
   *reinterpret_cast<volatile int*>(&c.stop) = 1;
   return false;
@@ -356,30 +374,36 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(PfGemmParams P, 
   const int n_units = *P.n_entries * P.tiles;
   const int nkt = (P.K + kPfKTile - 1) / kPfKTile;
 
-  if (warp == 0 && lane < 2) {
-    // ---------------- TMA producers: lane 0 packed tiles, lane 1 activation tiles ----------------
-    const bool packed = lane == 0;
+  if ((warp == 0 || warp == 2) && lane == 0) {
+    // ---------------- TMA producers: warp 0 packed tiles, warp 2 activation tiles ----------------
+    const bool packed = warp == 0;
     const int nst = packed ? kPkStages : kActStages;
     uint64_t* fullb = packed ? c.pk_full : c.act_full;
     uint64_t* emptyb = packed ? c.pk_empty : c.act_empty;
     RingPos rp;
     long long issued = 0;
+    // weights stream through L2 once; the grouped activation rows are read by every weight tile of
+    // their entry, so they are kept in L2 ahead of the weights
+    const uint64_t policy = packed ? l2_evict_first_policy() : l2_evict_last_policy();
     for (int u = blockIdx.x; u < n_units && !ld_volatile_int(&c.stop); u += gridDim.x) {
       const PfEntry en = P.entries[u / P.tiles];
       const int t = u % P.tiles;
       const ExpertDesc& ed = P.table[en.e];
       for (int kt = 0; kt < nkt; kt++) {
+        if (packed && kt % kPfSuper != 0) continue;  // one packed tile covers kPfSuper K tiles
         if (!pf_wait(c, &emptyb[rp.s], rp.ph ^ 1u, P.err)) break;
         if (packed) {
           uint8_t* st = sm + Lay::kPk + (size_t)rp.s * Lay::kPkStage;
           mbar_arrive_expect_tx(&fullb[rp.s], Lay::kPkStage);
-          tma_load_2d(st, &ed.t[P.t0].map_tc, kt * kTcWords, t * kTcRows, &fullb[rp.s]);
-          if (DUAL) tma_load_2d(st + kPfPackedBytes, &ed.t[P.t1].map_tc, kt * kTcWords, t * kTcRows, &fullb[rp.s]);
+          tma_load_2d_hint(st, &ed.t[P.t0].map_tc, (kt / kPfSuper) * kTcWords, t * kTcRows, &fullb[rp.s], policy);
+          if (DUAL)
+            tma_load_2d_hint(st + kPfPackedBytes, &ed.t[P.t1].map_tc, (kt / kPfSuper) * kTcWords, t * kTcRows,
+                             &fullb[rp.s], policy);
         } else {
           uint8_t* st = sm + Lay::kAct + (size_t)rp.s * Lay::kActStage;
           mbar_arrive_expect_tx(&fullb[rp.s], (uint32_t)en.npad * 128u);
           for (int j = 0; j < en.npad; j += 16)
-            tma_load_2d(st + (uint32_t)j * 128u, &act_map, kt * kPfKTile, en.row0 + j, &fullb[rp.s]);
+            tma_load_2d_hint(st + (uint32_t)j * 128u, &act_map, kt * kPfKTile, en.row0 + j, &fullb[rp.s], policy);
         }
         issued++;
         rp.next(nst);
@@ -427,14 +451,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(PfGemmParams P, 
       tc_commit(&c.mma_done);  // teardown: tensor memory is released only after every MMA
       if (!mbar_wait(&c.mma_done, 0)) set_error(P.err, COLI_E_TIMEOUT);
     }
-  } else if (warp >= 2) {
+  } else if (warp >= 3) {
     // ---------------- converters (+ epilogue on warps 4..7) ----------------
-    const int ct = (warp - 2) * 32 + lane;   // converter thread 0..511
+    const int ct = (warp - 3) * 32 + lane;   // converter thread 0..511
     // kParts threads share a row of a tensor: thread ct converts words w0 .. w0 + kW - 1 (w0 = kW
     // ((ct / 128) % kParts)) of row ct % 128 of tensor ct / (128 kParts).
     constexpr int kParts = kPfConvWarps * 32 / (Lay::kT * kTcRows);
-    constexpr int kW = kTcWords / kParts;
-    static_assert(kParts * kW == kTcWords && kW >= 2, "converter split");
+    constexpr int kW = 8 / kParts;  // words of a 64-column K tile (8 words per row) per thread
+    static_assert(kParts * kW == 8 && kW >= 2, "converter split");
     const int r = ct & (kTcRows - 1);
     const int x = DUAL ? ct / (kTcRows * kParts) : 0;
     const int w0 = ((ct / kTcRows) % kParts) * kW;
@@ -469,17 +493,24 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(PfGemmParams P, 
         const uint32_t s2 = bf16x2_splat(s_next0);
         s_next0 = s_next1;
         s_next1 = kt + 2 < nkt ? scale_of((kt + 2) * kPfKTile + hoff) : 0.f;
-        if (!pf_wait(c, &c.pk_full[rp.s], rp.ph, P.err) || !pf_wait(c, &c.op_empty[ro.s], ro.ph ^ 1u, P.err)) {
+        const int sub = kt % kPfSuper;  // K tile within the packed tile
+        if ((sub == 0 && !pf_wait(c, &c.pk_full[rp.s], rp.ph, P.err)) || !pf_wait(c, &c.op_empty[ro.s], ro.ph ^ 1u, P.err)) {
           ok = false;
           break;
         }
-        const uint8_t* pk = sm + Lay::kPk + (size_t)rp.s * Lay::kPkStage + x * kPfPackedBytes + r * (kTcWords * 4) + w0 * 4;
+        // row r of the packed tile is 128 bytes, its 16-byte chunks swizzled by r % 8 (TMA 128B mode);
+        // this thread's words are bytes 4 (8 sub + w0) .. of the row
+        const uint8_t* prow = sm + Lay::kPk + (size_t)rp.s * Lay::kPkStage + x * kPfPackedBytes + r * 128;
+        auto pk_at = [&](int word) {  // address of word `word` (0..31) of this row
+          const uint32_t b = 4u * (uint32_t)word;
+          return prow + ((((b >> 4) ^ swz) << 4) | (b & 15u));
+        };
         uint8_t* arow = sm + Lay::kOp + (size_t)ro.s * Lay::kOpStage + x * kPfTileBytes + r * 128;
         uint32_t wv[kW];
         if (kW >= 4) {
 #pragma unroll
           for (int j = 0; j < kW; j += 4) {
-            const uint4 v = lds128(pk + 4 * j);
+            const uint4 v = lds128(pk_at(8 * sub + w0 + j));  // 4 words in one 16-byte chunk
             wv[j] = v.x;
             wv[(j + 1) % kW] = v.y;
             wv[(j + 2) % kW] = v.z;
@@ -487,12 +518,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(PfGemmParams P, 
           }
         } else {
           uint2 v;
-          asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_u32(pk)) : "memory");
+          asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_u32(pk_at(8 * sub + w0))) : "memory");
           wv[0] = v.x;
           wv[kW - 1] = v.y;
         }
+        const bool last_sub = sub == kPfSuper - 1 || kt + 1 == nkt;
         __syncwarp();
-        if (lane == 0) mbar_arrive(&c.pk_empty[rp.s]);  // packed words are in registers
+        if (last_sub && lane == 0) mbar_arrive(&c.pk_empty[rp.s]);  // the packed tile's words are all read
         const int c0 = kt * kPfKTile + hoff;
         if (row_ok && c0 + 8 * kW <= P.K) {  // whole half inside the matrix
 #pragma unroll
@@ -509,7 +541,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(PfGemmParams P, 
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&c.op_full[ro.s]);
-        rp.next(kPkStages);
+        if (last_sub) rp.next(kPkStages);
         ro.next(kOpStages);
       }
       if (!ok) break;
