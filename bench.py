@@ -291,7 +291,7 @@ def load_traffic(kernel: str, src_hash: str):
 def source_hash():
     import hashlib
     h = hashlib.sha256()
-    for name in ("experts.cu", "coli_internal.h"):
+    for name in ("experts.cu", "coli_internal.h", "pipe.h"):
         with open(os.path.join(ROOT, "int4_grouped_expert_router_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -419,9 +419,13 @@ def gpu_arm(args, rank, world, local):
         if n:
             kern[name] = {"launches": n, "mean_us": ms * 1000.0 / n}
     B.coli_profile_enable(ctx, False)
-    gu_us = kern["gateup"]["mean_us"]
-    achieved = float(np.mean(gateup_bytes)) / (gu_us * 1e-6) / 1e9
-    traffic = load_traffic("gateup_kernel", source_hash())
+    # S == 1 runs the whole expert FFN as one kernel (recorded as gate/up, no down launch): its
+    # algorithmic bytes are every kept expert's gate, up and down bytes; else the gate/up kernel's
+    fused = "down" not in kern
+    top_kernel = "decode_ffn_kernel" if fused else "gateup_kernel"
+    top_bytes = float(np.mean(expert_bytes if fused else gateup_bytes))
+    achieved = top_bytes / (kern["gateup"]["mean_us"] * 1e-6) / 1e9
+    traffic = load_traffic(top_kernel, source_hash())
 
     # ---- end to end through the C ABI with host buffers: H2D inputs, D2H result per step ----
     hx = [torch.empty_like(xs[s], device="cpu").pin_memory() for s in range(n_tok)]
@@ -454,7 +458,7 @@ def gpu_arm(args, rank, world, local):
     h2d = xs[0].numel() * xs[0].element_size() + rs[0].numel() * rs[0].element_size()
     d2h = outs[0]["y"].numel() * outs[0]["y"].element_size()
 
-    launches_per_step = 3 if cfg.S == 1 else 4
+    launches_per_step = 2 if fused else (3 if cfg.S == 1 else 4)
     result = None
     if rank == 0:
         cpu = None
@@ -482,8 +486,8 @@ def gpu_arm(args, rank, world, local):
                        "p90_us": float(np.percentile(step_ms, 90)) * 1000.0,
                        "kernels_us": kern, "wall_s": wall},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": traffic, "kernel": "gateup_kernel",
-                         "peak_kind": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": float(np.mean(gateup_bytes))},
+                         "frac": achieved / hbm_peak, "traffic": traffic, "kernel": top_kernel,
+                         "peak_kind": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": top_bytes},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,

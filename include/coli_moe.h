@@ -180,6 +180,11 @@ COLI_API int coli_expert_table_set(coli_ctx *ctx, int e, uint64_t gate, uint64_t
  * and y is rounded to bf16 once at the end). idx, w, n_sel: as produced by coli_router_select,
  * device pointers. Slots with idx < 0 beyond n_sel are ignored. D and I come from the table.
  * Every weight byte of an expert is read once per call however many of the S tokens chose it.
+ * Kernel forms: with S == 1, a gate/up kernel and a down kernel chained by programmatic dependent
+ * launch; with COLI_DECODE_FUSED=1 in the environment at coli_init, one cooperative kernel for the
+ * whole call (profiled as COLI_KERNEL_GATEUP) where the device supports cooperative launch and
+ * I <= 4096. The two forms give bit-identical y. bf16 batches with enough routed rows per expert
+ * run on the tensor cores instead ([tcgate]).
  */
 COLI_API int coli_expert_group(coli_ctx *ctx, const void *x_rows, int x_dtype, int S,
                       const int32_t *idx, const float *w, const int32_t *n_sel, int K,

@@ -198,15 +198,18 @@ int coli_init(coli_ctx** out, int device, void* cuda_stream) {
   cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, device);
   const char* fa = getenv("COLI_FAIL_AFTER");
   if (fa && *fa) ctx->fail_after = atoll(fa);
+  const char* fu = getenv("COLI_DECODE_FUSED");
+  if (fu && *fu) ctx->decode_fused = atoi(fu) != 0;
   ctx->h_table.assign(COLI_MAX_EXPERTS, ExpertDesc{});
   ctx->table_handles.assign(3 * COLI_MAX_EXPERTS, 0);
   void* p = nullptr;
   if ((e = cudaMalloc(&p, sizeof(ExpertDesc) * COLI_MAX_EXPERTS)) != cudaSuccess) goto fail;
   ctx->d_table = static_cast<ExpertDesc*>(p);
   if ((e = cudaMemset(ctx->d_table, 0, sizeof(ExpertDesc) * COLI_MAX_EXPERTS)) != cudaSuccess) goto fail;
-  if ((e = cudaMalloc(&p, 256)) != cudaSuccess) goto fail;
+  if ((e = cudaMalloc(&p, kStatusBytes)) != cudaSuccess) goto fail;
   ctx->d_status = static_cast<int*>(p);
-  if ((e = cudaMemset(ctx->d_status, 0, 256)) != cudaSuccess) goto fail;
+  if ((e = cudaMemset(ctx->d_status, 0, kStatusBytes)) != cudaSuccess) goto fail;
+  ctx->coop_mode = probe_coop_mode(ctx);
   *out = ctx;
   return COLI_OK;
 fail:
@@ -254,10 +257,13 @@ int coli_check_error(coli_ctx* ctx) {
   e = cudaMemcpy(&code, ctx->d_status, sizeof(int), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "coli_check_error: read error word");
   if (code != 0) {
-    e = cudaMemset(ctx->d_status, 0, sizeof(int));
+    // after a timed-out wait the synchronisation words may be left mid-count: clear them with the
+    // error word
+    e = cudaMemset(ctx->d_status, 0, code == COLI_E_TIMEOUT ? kStatusBytes : sizeof(int));
     if (e != cudaSuccess) return cuda_fail(ctx, e, "coli_check_error: clear error word");
     ctx->last_error = code == COLI_E_ROUTE ? "device: expert index out of range or unset table entry"
                       : code == COLI_E_NONFINITE ? "device: non-finite activation or router score"
+                      : code == COLI_E_TIMEOUT   ? "device: a bounded wait inside a kernel gave up"
                                                  : "device error";
   }
   return code;
@@ -296,9 +302,17 @@ int coli_profile_read(coli_ctx* ctx, int kind, double* total_ms, long long* laun
 int coli_reserve(coli_ctx* ctx, int max_S, int max_E, int max_K, int max_D, int max_I) {
   if (!ctx || max_S < 1 || max_E < 1 || max_K < 1 || max_D < 1 || max_I < 1) return COLI_E_INVAL;
   size_t router = align_up((size_t)max_S * max_E * 2 * sizeof(float), 256);
-  size_t experts = align_up((size_t)max_S * max_K * max_I * sizeof(float), 256) +
-                   align_up((size_t)max_S * max_K * max_D * sizeof(float), 256) + 4096 +
-                   align_up((size_t)(max_S + 1) * sizeof(int) * 4, 256);
+  const size_t routes = (size_t)max_S * max_K;
+  // grouped GEMV path: h, per-route rows (S > 1) or the fused kernel's partial rows (S == 1), plan
+  size_t experts = align_up(routes * max_I * sizeof(float), 256) +
+                   align_up((routes > (size_t)max_K * kFusedMaxSlices ? routes : (size_t)max_K * kFusedMaxSlices) *
+                                max_D * sizeof(float), 256) +
+                   4096 + align_up((size_t)(max_S + 1) * sizeof(int) * 4, 256);
+  // tensor-core path: grouped rows (each expert's block padded to 16) as bf16 x and h, f32 outputs
+  const size_t pf_rows = routes + 16 * (size_t)(max_E < COLI_MAX_EXPERTS ? max_E : COLI_MAX_EXPERTS) + 16;
+  const size_t prefill = pf_rows * ((size_t)max_D * 2 + (size_t)max_I * 2 + (size_t)max_D * 4 + 4) + routes * 4 +
+                         (size_t)max_E * 8 + (routes / 128 + max_E + 1) * 16 + 16 * 256;
+  if (prefill > experts) experts = prefill;
   cudaSetDevice(ctx->device);
   return ensure_workspace(ctx, router > experts ? router : experts);
 }

@@ -27,6 +27,16 @@ constexpr int kScaleBox = 16;
 constexpr int kTcRows = 128;
 constexpr int kTcWords = 32;
 
+// Device status words of a context: [0] error code, [1] router arrivals, [2..] the fused decode
+// kernel's synchronisation words (grid barrier at [2], [3]; row-range counters from
+// [2 + kSyncRanges]). All start at zero and are returned to zero by the kernels that use them.
+constexpr int kSyncBase = 2;
+constexpr int kSyncRanges = 64;   // offset of the range counters from kSyncBase
+constexpr int kMaxRanges = 4096;  // range counters
+constexpr size_t kStatusBytes = (size_t)(kSyncBase + kSyncRanges + kMaxRanges) * sizeof(int);
+// The fused decode kernel covers I <= 32 * 32 * kFusedMaxSlices (column slices of a down row).
+constexpr int kFusedMaxSlices = 4;
+
 // One uploaded int4 tensor as the kernels see it. Rows are padded to a whole number of 16-byte
 // chunks (32 columns each); padding nibbles hold 8, i.e. the value 0.
 struct TensorDesc {
@@ -88,8 +98,11 @@ struct coli_ctx {
   std::vector<coli::ExpertDesc> h_table;
   std::vector<uint64_t> table_handles;       // 3 per entry
   int table_D = 0, table_I = 0, table_count = 0;
-  // device status words: [0] error code, [1] router completion counter
-  int* d_status = nullptr;  // [0] device error word, [1] router arrivals
+  int* d_status = nullptr;  // kStatusBytes of device status words (see kSyncBase)
+  // decode (S == 1) expert FFN as one cooperative kernel: COLI_DECODE_FUSED=1 (default 0), and how
+  // this device launches it (2: cooperative + programmatic dependent launch, 1: cooperative, 0: no)
+  bool decode_fused = false;
+  int coop_mode = -1;  // -1: not probed yet
   coli::Workspace ws;
   // COLI_FAIL_AFTER test hook
   long long fail_after = -1;
@@ -141,6 +154,9 @@ int launch_router_noalloc(coli_ctx* ctx, const void* x, int x_dtype, int S, int 
                           int32_t* idx, float* w, int32_t* n_sel);
 int launch_expert_group(coli_ctx* ctx, const void* x, int x_dtype, int S, const int32_t* idx,
                         const float* w, const int32_t* n_sel, int K, const void* resid, void* y);
+// Which cooperative launch forms this device accepts (coli_ctx::coop_mode), found with an empty
+// kernel on a private stream.
+int probe_coop_mode(coli_ctx* ctx);
 
 }  // namespace coli
 

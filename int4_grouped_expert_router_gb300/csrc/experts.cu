@@ -278,12 +278,6 @@ struct GroupParams {
 };
 
 // ------------------------------------------------------------------------------------------
-// Batches of the gate/up work: kept routes x I row pairs, split into equal contiguous ranges over
-// the grid; a batch is up to RB consecutive row pairs of one route. Producer and consumers walk
-// the same sequence.
-// ------------------------------------------------------------------------------------------
-
-// ------------------------------------------------------------------------------------------
 // Shared pieces of the two streaming kernels
 //
 // Every consumer warp owns one 512-byte column slice (32 chunks of 16 bytes) of the weight rows
@@ -445,6 +439,14 @@ __device__ __forceinline__ void gateup_issue(const RouteSlot& rs, uint8_t* st, u
 // a multiple of kBoxRows, so batch q is (route q / Bpr, first row kBoxRows (q % Bpr)) in closed
 // form and a CTA owns a contiguous run of batches; segB batches (one row pair per thread of the
 // CTA, at most kSeg) form a finishing segment.
+//
+// FUSED (S == 1, cooperative launch): the same kernel then runs the down projection. Every warp
+// takes one (slot k, column slice) stream of a range of down rows; the ranges split D identically
+// for every stream. Its first down boxes are staged into the warp's ring (the gate/up ring, free by
+// then) before the grid-wide barrier that makes h complete, so the weight stream runs on while the
+// last gate/up rows finish. After the barrier each warp turns its slice of h_k into limbs, streams
+// its rows and writes per-row partial sums; the last of a range's streams to finish (a counter per
+// range) adds them up in slot order -- the same order and arithmetic as the two-kernel path.
 // ------------------------------------------------------------------------------------------
 
 #ifndef COLI_GU_STAGES
@@ -458,10 +460,29 @@ constexpr int kGUMinCtas = COLI_GU_MIN_CTAS; // CTAs per SM the register budget 
 
 __device__ const float kOneF = 1.0f;         // stand-in scale for unconditional loads
 
+__host__ __device__ constexpr uint32_t down_stage_bytes() { return kBoxRows * kSliceWords * 4 + kBoxRows * kScaleBox * 4; }
+
+// stages of the fused kernel's down ring: it reuses the warp's gate/up ring
+constexpr int kFDStages = (int)(kGUStages * (2u * kBoxRows * kSliceWords * 4 + 2u * kBoxRows * kScaleBox * 4) /
+                                down_stage_bytes());
+
 struct GateUpSmem {
   RouteSlot routes[kRouteCache];
   uint64_t bars[8][kGUStages];     // gate/up CTAs have at most 8 warps (D <= 8192)
   int e_spec[COLI_MAX_K];          // S == 1: the expert of each slot, read with n_sel
+  // FUSED only
+  uint64_t dbars[8][kFDStages];    // the warps' down rings
+  SlotTensor dn[COLI_MAX_K];       // down tensor of each kept slot
+  float wk[COLI_MAX_K];            // routing weight of each slot
+  int dn_ok[COLI_MAX_K];
+  int m;                           // kept slots
+};
+
+// Fused decode kernel: where the down phase keeps its cross-CTA state.
+struct FusedParams {
+  float* ypart;  // [K][nsl][D]: partial down rows of each (slot, column slice) stream
+  int* sync;     // [0..1]: the grid barrier's 64-bit arrival count; [kSyncRanges + r]: arrivals at row range r
+  int nsl;       // column slices of a down row: ceil(ceil(I / 32) / 32)
 };
 // followed in dynamic shared memory by the warps' rings, pg[W][kSeg], pu[W][kSeg], pre[S + 1]
 
@@ -484,8 +505,174 @@ inline size_t gateup_smem_bytes(int W, int S) {
          (size_t)(S + 1) * sizeof(int);
 }
 
-template <int MAXT>
-__global__ void __launch_bounds__(MAXT, MAXT <= 192 ? kGUMinCtas : 1) gateup_kernel(GroupParams P) {
+// Rows [d0, dend) of y, one row per lane at a time: residual + the sum over kept slots, in slot
+// order, of w_k (row scale x the sum of the slot's NSL column-slice partials). Every load of a
+// kRB-slot block is issued before its sums, from clamped (always valid) addresses, so the loads
+// overlap instead of paying one L2 round trip each.
+template <int NSL>
+__device__ __forceinline__ void fused_finish_rows(const GroupParams& P, const FusedParams& F, const GateUpSmem& sm,
+                                                  int m, int d0, int dend, int lane) {
+  constexpr int kRB = 8;
+  const int nsl = F.nsl;  // NSL >= nsl
+  for (int d = d0 + lane; d < dend; d += 32) {
+    float acc = 0.f;
+    for (int k0 = 0; k0 < m; k0 += kRB) {
+      float v[kRB][NSL], sv[kRB];
+#pragma unroll
+      for (int i = 0; i < kRB; i++) {
+        const int kk = min(k0 + i, m - 1);
+        const bool row_scale = sm.dn_ok[kk] && sm.dn[kk].mode == SCALE_ROW;
+#pragma unroll
+        for (int ss = 0; ss < NSL; ss++) v[i][ss] = __ldcg(F.ypart + ((size_t)kk * nsl + min(ss, nsl - 1)) * P.D + d);
+        sv[i] = __ldg((row_scale ? sm.dn[kk].s : F.ypart) + d);
+      }
+#pragma unroll
+      for (int i = 0; i < kRB; i++) {
+        const int kk = k0 + i;
+        if (kk < m && sm.dn_ok[kk]) {
+          float yk = 0.f;
+#pragma unroll
+          for (int ss = 0; ss < NSL; ss++)
+            if (ss < nsl) yk += v[i][ss];
+          const float rs = sm.dn[kk].mode == SCALE_ROW ? sv[i] : 1.f;
+          acc = fmaf(sm.wk[kk], yk * rs, acc);
+        }
+      }
+    }
+    float res = 0.f;
+    if (P.resid) res = load_act(P.resid, P.x_dtype, d);
+    if (P.resid) acc = res + acc;
+    if (P.x_dtype == COLI_DTYPE_F32)
+      static_cast<float*>(P.y)[d] = acc;
+    else
+      static_cast<uint16_t*>(P.y)[d] = f32_to_bf16_rn(acc);
+  }
+}
+
+// Down phase of the fused decode kernel. `ring` is this warp's gate/up ring (drained by now).
+__device__ __forceinline__ void fused_down_phase(const GroupParams& P, const FusedParams& F, GateUpSmem& sm,
+                                                 uint8_t* ring, int W) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t DSB = down_stage_bytes();
+  const int m = sm.m, nsl = F.nsl, T = m * nsl;  // streams: kept slots x column slices
+  if (T == 0) {  // no kept route (uniform across the grid): y = residual
+    for (int d = blockIdx.x * blockDim.x + tid; d < P.D; d += gridDim.x * blockDim.x) {
+      float acc = 0.f;
+      if (P.resid) acc = load_act(P.resid, P.x_dtype, d) + acc;
+      if (P.x_dtype == COLI_DTYPE_F32)
+        static_cast<float*>(P.y)[d] = acc;
+      else
+        static_cast<uint16_t*>(P.y)[d] = f32_to_bf16_rn(acc);
+    }
+    return;
+  }
+  // warp gw takes stream gw % T of row range gw / T; every stream splits D into the same NR ranges
+  const int NW = gridDim.x * W, gw = blockIdx.x * W + warp;
+  const int NR = min(NW / T, kMaxRanges);
+  const int NBd = (P.D + kBoxRows - 1) / kBoxRows;  // row batches of a down matrix
+  const int r = gw / T, pr = gw - r * T;
+  const int k = pr / nsl, slice = pr - k * nsl;
+  const bool task = r < NR;
+  const int b0 = task ? (int)((long long)r * NBd / NR) : 0;
+  const int b1 = task ? (int)((long long)(r + 1) * NBd / NR) : 0;
+  const bool warp_on = task && sm.dn_ok[k];  // uniform per warp
+  const SlotTensor& sl = sm.dn[warp_on ? k : 0];
+  uint64_t* bars = sm.dbars[warp];
+  const int CI = (P.I + 31) >> 5;
+  const int c = slice * 32 + lane;
+  const bool active = warp_on && c < CI;
+  const uint32_t nbat = (uint32_t)(b1 - b0);
+  uint32_t issued = 0;
+  auto issue_next = [&]() {
+    if (issued >= nbat) return;
+    const uint32_t s = issued % kFDStages;
+    uint8_t* st = ring + (size_t)s * DSB;
+    const int d0 = (b0 + (int)issued) * kBoxRows;
+    const uint32_t bytes = sl.box_rows * sl.box_w * 4 + (sl.box_s ? sl.box_rows * sl.box_s * 4 : 0);
+    mbar_arrive_expect_tx(&bars[s], bytes);
+    tma_load_2d(st, &sl.d->map_w, kSliceWords * slice, d0, &bars[s]);
+    if (sl.box_s) tma_load_2d(st + kBoxRows * kSliceWords * 4, &sl.d->map_s, sl.box_s * slice, d0, &bars[s]);
+    issued++;
+  };
+  __syncwarp();  // every lane is done with the gate/up ring
+  if (warp_on && lane == 0)
+    for (int s = 0; s < kFDStages; s++) issue_next();  // the down weights do not depend on h
+  bool stop = !grid_barrier(reinterpret_cast<unsigned long long*>(F.sync));  // every row of h is written
+  if (stop && tid == 0) set_error(P.err, COLI_E_TIMEOUT);
+
+  LaneTensor lt;
+  lane_tensor(lt, sl, c);
+  const int so = lt.cg - lt.box_s * slice;  // lane's scale within the staged box
+  float hv[32];
+  Limbs L;
+  load_chunk_f32(P.h, COLI_DTYPE_F32, (size_t)k * P.I, 32 * c, active ? P.I : 0, hv);
+  if (!make_limbs(hv, L) && active) set_error(P.err, COLI_E_NONFINITE);
+  float* yp = F.ypart + ((size_t)k * nsl + slice) * P.D;
+  for (uint32_t b = 0; b < nbat; b++) {
+    if (!warp_on || stop) break;
+    const int d0 = (b0 + (int)b) * kBoxRows;
+    const int n = min(kBoxRows, P.D - d0);
+    const uint32_t s = b % kFDStages;
+    const bool ok = mbar_wait(&bars[s], (b / kFDStages) & 1);
+    const uint8_t* st = ring + (size_t)s * DSB;
+    float acc[kBoxRows];
+    if (ok && active && lt.fast) {
+#pragma unroll
+      for (int u = 0; u < kBoxRows; u++) {
+        float d = 0.f;
+        if (u < n) {
+          d = chunk_dot(lds128(st + u * lt.rowB + 16 * lane), L);
+          if (lt.box_s) d *= lds32f(st + kBoxRows * kSliceWords * 4 + (u * lt.box_s + so) * 4);
+        }
+        acc[u] = d;
+      }
+    } else {
+      float tmp[kBoxRows];  // local memory: the rarely used slow path keeps code small
+#pragma unroll 1
+      for (int u = 0; u < kBoxRows; u++)
+        tmp[u] = (ok && active && u < n)
+                     ? chunk_dot_slow(lds128(st + u * lt.rowB + 16 * lane), L, lt, P.h, COLI_DTYPE_F32,
+                                      (size_t)k * P.I, d0 + u, c)
+                     : 0.f;
+#pragma unroll
+      for (int u = 0; u < kBoxRows; u++) acc[u] = tmp[u];
+    }
+    __syncwarp();
+    if (lane == 0 && ok) issue_next();
+    if (!ok) {
+      stop = true;
+      set_error(P.err, COLI_E_TIMEOUT);
+    }
+    // lane l ends with the warp total of row l / (32 / kBoxRows) of the batch
+    warp_transpose_reduce<kBoxRows>(acc, lane);
+    constexpr int kSpread = 32 / kBoxRows;
+    if ((lane & (kSpread - 1)) == 0 && (lane / kSpread) < n) yp[d0 + lane / kSpread] = acc[0];
+  }
+  if (warp_on && lane == 0)  // never leave with TMA loads in flight into the ring
+    for (uint32_t q = issued > kFDStages ? issued - kFDStages : 0; q < issued; q++)
+      (void)mbar_wait(&bars[q % kFDStages], (q / kFDStages) & 1);
+  if (!task) return;
+
+  // arrive at the range; the last of its T streams finishes its rows
+  __threadfence();
+  __syncwarp();
+  int* ctr = F.sync + kSyncRanges + r;
+  int last = 0;
+  if (lane == 0) last = atomicAdd(ctr, 1) == T - 1;
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  if (lane == 0) atomicExch(ctr, 0);  // ready for the next launch
+  __threadfence();
+  const int d0 = b0 * kBoxRows, dend = min(b1 * kBoxRows, P.D);
+  switch (nsl) {
+    case 1: fused_finish_rows<1>(P, F, sm, m, d0, dend, lane); break;
+    case 2: fused_finish_rows<2>(P, F, sm, m, d0, dend, lane); break;
+    default: fused_finish_rows<kFusedMaxSlices>(P, F, sm, m, d0, dend, lane); break;
+  }
+}
+
+template <bool FUSED>
+__device__ __forceinline__ void gateup_body(const GroupParams& P, const FusedParams& F) {
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem_raw = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 127) & ~uintptr_t(127));
   const int C = (P.D + 31) >> 5;
@@ -505,6 +692,8 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 192 ? kGUMinCtas : 1) gateup_ker
   uint64_t* bars = sm.bars[warp];
   if (lane == 0) {
     for (int s = 0; s < kGUStages; s++) mbar_init(&bars[s], 1);
+    if (FUSED)
+      for (int s = 0; s < kFDStages; s++) mbar_init(&sm.dbars[warp][s], 1);
     mbar_fence_init();
   }
   // prologue overlapping the router's tail: activation limbs of token 0
@@ -516,7 +705,11 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 192 ? kGUMinCtas : 1) gateup_ker
     if (!make_limbs(xv, L) && has_chunk) set_error(P.err, COLI_E_NONFINITE);
   }
   griddep_wait();
-  if (P.S == 1 && tid < P.K) sm.e_spec[tid] = ld_cg_i32(P.idx + tid);  // same round trip as n_sel
+  float w_slot = 0.f;
+  if (P.S == 1 && tid < P.K) {  // same round trip as n_sel
+    sm.e_spec[tid] = ld_cg_i32(P.idx + tid);
+    if (FUSED) w_slot = ld_cg_f32(P.w + tid);
+  }
   const int R = build_plan(P.n_sel, P.S, P.K, pre, scratch32);       // contains __syncthreads
   if (blockIdx.x == 0)
     for (int t = tid; t <= P.S; t += blockDim.x) P.plan[t] = pre[t];
@@ -527,14 +720,19 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 192 ? kGUMinCtas : 1) gateup_ker
   const long long NB = (long long)R * Bpr;
   const int qbeg = (int)((long long)blockIdx.x * NB / gridDim.x);
   const int qend = (int)((long long)(blockIdx.x + 1) * NB / gridDim.x);
-  if (qbeg >= qend) return;  // uniform across the CTA
   const int j_first = qbeg / Bpr;
-  const int n_routes = (qend - 1) / Bpr - j_first + 1;  // <= kRouteCache (launch sizing)
-  if (n_routes > kRouteCache) {  // uniform across the CTA; the launcher's grid rules this out
-    if (tid == 0) set_error(P.err, COLI_E_INVAL);
-    return;
+  const int n_routes = qbeg < qend ? (qend - 1) / Bpr - j_first + 1 : 0;  // <= kRouteCache (launch sizing)
+  if (n_routes > kRouteCache && tid == 0) set_error(P.err, COLI_E_INVAL);  // the launcher's grid rules this out
+  const bool gu = qbeg < qend && n_routes <= kRouteCache;                   // uniform across the CTA
+  if (FUSED && tid < P.K) {
+    const int e = sm.e_spec[tid];
+    const bool ok = tid < R && e >= 0 && e < COLI_MAX_EXPERTS && P.table[e].valid;
+    if (ok) fill_slot_tensor(sm.dn[tid], &P.table[e].t[T_DOWN]);
+    sm.dn_ok[tid] = ok;
+    sm.wk[tid] = ok ? w_slot : 0.f;
+    if (tid == 0) sm.m = R;
   }
-  if (tid < n_routes) {
+  if (gu && tid < n_routes) {
     const int j = j_first + tid;
     RouteSlot& rs = sm.routes[tid];
     if (P.S == 1) {
@@ -551,115 +749,129 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 192 ? kGUMinCtas : 1) gateup_ker
     if (!rs.ok) set_error(P.err, COLI_E_ROUTE);
   }
   __syncthreads();
-  // issue side of this warp's ring: kGUStages batches ahead of the compute (lane 0)
-  int iq = qbeg, ij = j_first, ii = (qbeg - j_first * Bpr) * kBoxRows, istage = 0, issued = 0;
-  auto issue_next = [&]() {
-    while (iq < qend) {
-      const int j = ij, i0 = ii;
-      iq++;
-      ii += kBoxRows;
-      if (ii >= Bpr * kBoxRows) {
-        ii = 0;
-        ij++;
+  if (gu) {
+    // issue side of this warp's ring: kGUStages batches ahead of the compute (lane 0)
+    int iq = qbeg, ij = j_first, ii = (qbeg - j_first * Bpr) * kBoxRows, istage = 0, issued = 0;
+    auto issue_next = [&]() {
+      while (iq < qend) {
+        const int j = ij, i0 = ii;
+        iq++;
+        ii += kBoxRows;
+        if (ii >= Bpr * kBoxRows) {
+          ii = 0;
+          ij++;
+        }
+        const RouteSlot& rs = sm.routes[j - j_first];
+        if (!rs.ok) continue;
+        gateup_issue(rs, ring + (size_t)istage * SB, &bars[istage], warp, i0);
+        istage = istage + 1 == kGUStages ? 0 : istage + 1;
+        issued++;
+        return;
       }
-      const RouteSlot& rs = sm.routes[j - j_first];
-      if (!rs.ok) continue;
-      gateup_issue(rs, ring + (size_t)istage * SB, &bars[istage], warp, i0);
-      istage = istage + 1 == kGUStages ? 0 : istage + 1;
-      issued++;
-      return;
-    }
-  };
-  if (lane == 0)
-    for (int s = 0; s < kGUStages; s++) issue_next();
+    };
+    if (lane == 0)
+      for (int s = 0; s < kGUStages; s++) issue_next();
 
-  // finaliser thread `tid` (< segB kBoxRows) of a segment: where its row pair goes and its row
-  // scales, loaded when the segment starts and consumed when it ends
-  float fg = 1.f, fu = 1.f;
-  size_t hdst = 0;
-  bool fin_ok = false;
-  auto prefetch_finaliser = [&](int q0) {
-    const int qq = q0 + tid / kBoxRows;
-    const int jj = qq / Bpr, i = (qq - jj * Bpr) * kBoxRows + tid % kBoxRows;
-    fin_ok = tid < segB * kBoxRows && qq < qend && i < P.I && sm.routes[jj - j_first].ok;
-    const RouteSlot& r = sm.routes[fin_ok ? jj - j_first : 0];
-    hdst = (size_t)jj * P.I + i;
-    fg = __ldg((fin_ok && r.ts[0].mode == SCALE_ROW) ? r.ts[0].s + i : &kOneF);
-    fu = __ldg((fin_ok && r.ts[1].mode == SCALE_ROW) ? r.ts[1].s + i : &kOneF);
-  };
+    // finaliser thread `tid` (< segB kBoxRows) of a segment: where its row pair goes and its row
+    // scales, loaded when the segment starts and consumed when it ends
+    float fg = 1.f, fu = 1.f;
+    size_t hdst = 0;
+    bool fin_ok = false;
+    auto prefetch_finaliser = [&](int q0) {
+      const int qq = q0 + tid / kBoxRows;
+      const int jj = qq / Bpr, i = (qq - jj * Bpr) * kBoxRows + tid % kBoxRows;
+      fin_ok = tid < segB * kBoxRows && qq < qend && i < P.I && sm.routes[jj - j_first].ok;
+      const RouteSlot& r = sm.routes[fin_ok ? jj - j_first : 0];
+      hdst = (size_t)jj * P.I + i;
+      fg = __ldg((fin_ok && r.ts[0].mode == SCALE_ROW) ? r.ts[0].s + i : &kOneF);
+      fu = __ldg((fin_ok && r.ts[1].mode == SCALE_ROW) ? r.ts[1].s + i : &kOneF);
+    };
 
-  // ---------------- compute ----------------
-  int cur_slot = -1;
-  LaneTensor tg, tu;
-  bool stop = false, row_scales = false;
-  int stage = 0;
-  uint32_t phase = 0;
-  int j = j_first, i0 = (qbeg - j_first * Bpr) * kBoxRows;
-  for (int qs = qbeg; qs < qend; qs += segB) {
-    const int qe = min(qs + segB, qend);
-    prefetch_finaliser(qs);
-    for (int q = qs; q < qe; q++) {
-      const int slot = j - j_first;
-      if (sm.routes[slot].ok) {
-        if (slot != cur_slot) {
-          cur_slot = slot;
-          const RouteSlot& rs = sm.routes[slot];
-          lane_tensor(tg, rs.ts[0], c);
-          lane_tensor(tu, rs.ts[1], c);
-          row_scales = tg.fast && tu.fast && !tg.box_s && !tu.box_s;
-          if (rs.t != cur_tok) {
-            cur_tok = rs.t;
-            float xv[32];
-            load_chunk_f32(P.x, P.x_dtype, (size_t)cur_tok * P.D, 32 * c, has_chunk ? P.D : 0, xv);
-            if (!make_limbs(xv, L) && has_chunk) set_error(P.err, COLI_E_NONFINITE);
+    // ---------------- compute ----------------
+    int cur_slot = -1;
+    LaneTensor tg, tu;
+    bool stop = false, row_scales = false;
+    int stage = 0;
+    uint32_t phase = 0;
+    int j = j_first, i0 = (qbeg - j_first * Bpr) * kBoxRows;
+    for (int qs = qbeg; qs < qend; qs += segB) {
+      const int qe = min(qs + segB, qend);
+      prefetch_finaliser(qs);
+      for (int q = qs; q < qe; q++) {
+        const int slot = j - j_first;
+        if (sm.routes[slot].ok) {
+          if (slot != cur_slot) {
+            cur_slot = slot;
+            const RouteSlot& rs = sm.routes[slot];
+            lane_tensor(tg, rs.ts[0], c);
+            lane_tensor(tu, rs.ts[1], c);
+            row_scales = tg.fast && tu.fast && !tg.box_s && !tu.box_s;
+            if (rs.t != cur_tok) {
+              cur_tok = rs.t;
+              float xv[32];
+              load_chunk_f32(P.x, P.x_dtype, (size_t)cur_tok * P.D, 32 * c, has_chunk ? P.D : 0, xv);
+              if (!make_limbs(xv, L) && has_chunk) set_error(P.err, COLI_E_NONFINITE);
+            }
+          }
+          const bool ok = !stop && mbar_wait(&bars[stage], phase);
+          const uint8_t* st = ring + (size_t)stage * SB + 16 * lane;
+          float acc[2 * kBoxRows];  // gate rows 0..3, then up rows 0..3
+          gateup_batch(acc, ok, has_chunk, row_scales, tg, tu, st, ring + (size_t)stage * SB + kScaleOff, warp, L, P,
+                       cur_tok, i0, min(kBoxRows, P.I - i0), c);
+          __syncwarp();
+          if (lane == 0 && ok) issue_next();  // refill the stage just consumed
+          if (!ok && !stop) {
+            stop = true;
+            set_error(P.err, COLI_E_TIMEOUT);
+          }
+          if (++stage == kGUStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          // lane l ends with the warp total of value l / 4: gate row v (v < 4) or up row v - 4.
+          // Box rows at and beyond I (zero-filled by TMA) give values that are never read back.
+          warp_transpose_reduce<2 * kBoxRows>(acc, lane);
+          if ((lane & 3) == 0) {
+            const int v = lane >> 2;
+            (v < kBoxRows ? pg : pu)[warp * kSeg + (q - qs) * kBoxRows + (v & (kBoxRows - 1))] = acc[0];
           }
         }
-        const bool ok = !stop && mbar_wait(&bars[stage], phase);
-        const uint8_t* st = ring + (size_t)stage * SB + 16 * lane;
-        float acc[2 * kBoxRows];  // gate rows 0..3, then up rows 0..3
-        gateup_batch(acc, ok, has_chunk, row_scales, tg, tu, st, ring + (size_t)stage * SB + kScaleOff, warp, L, P,
-                     cur_tok, i0, min(kBoxRows, P.I - i0), c);
-        __syncwarp();
-        if (lane == 0 && ok) issue_next();  // refill the stage just consumed
-        if (!ok && !stop) {
-          stop = true;
-          set_error(P.err, COLI_E_TIMEOUT);
-        }
-        if (++stage == kGUStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-        // lane l ends with the warp total of value l / 4: gate row v (v < 4) or up row v - 4.
-        // Box rows at and beyond I (zero-filled by TMA) give values that are never read back.
-        warp_transpose_reduce<2 * kBoxRows>(acc, lane);
-        if ((lane & 3) == 0) {
-          const int v = lane >> 2;
-          (v < kBoxRows ? pg : pu)[warp * kSeg + (q - qs) * kBoxRows + (v & (kBoxRows - 1))] = acc[0];
+        i0 += kBoxRows;
+        if (i0 >= Bpr * kBoxRows) {
+          i0 = 0;
+          j++;
         }
       }
-      i0 += kBoxRows;
-      if (i0 >= Bpr * kBoxRows) {
-        i0 = 0;
-        j++;
+      // segment end: finish its rows
+      const bool any_stop = named_sync_or(1, W * 32, stop);
+      if (!any_stop && fin_ok) {
+        float g = 0.f, u = 0.f;
+        for (int wi = 0; wi < W; wi++) {
+          g += pg[wi * kSeg + tid];
+          u += pu[wi * kSeg + tid];
+        }
+        P.h[hdst] = silu_mul(g * fg, u * fu);
       }
+      named_sync(1, W * 32);  // the partial buffers are reused by the next segment
+      if (any_stop) stop = true;
     }
-    // segment end: finish its rows
-    const bool any_stop = named_sync_or(1, W * 32, stop);
-    if (!any_stop && fin_ok) {
-      float g = 0.f, u = 0.f;
-      for (int wi = 0; wi < W; wi++) {
-        g += pg[wi * kSeg + tid];
-        u += pu[wi * kSeg + tid];
-      }
-      P.h[hdst] = silu_mul(g * fg, u * fu);
-    }
-    named_sync(1, W * 32);  // the partial buffers are reused by the next segment
-    if (any_stop) stop = true;
-  }
-  // never leave with TMA loads in flight into this warp's ring (the last issued phases)
-  if (lane == 0)
-    for (int q = issued > kGUStages ? issued - kGUStages : 0; q < issued; q++)
-      (void)mbar_wait(&bars[q % kGUStages], (q / kGUStages) & 1);
+    // never leave with TMA loads in flight into this warp's ring (the last issued phases)
+    if (lane == 0)
+      for (int q = issued > kGUStages ? issued - kGUStages : 0; q < issued; q++)
+        (void)mbar_wait(&bars[q % kGUStages], (q / kGUStages) & 1);
+  }  // gu
+  if constexpr (FUSED) fused_down_phase(P, F, sm, rings + (size_t)warp * kGUStages * SB, W);
+}
+
+template <int MAXT>
+__global__ void __launch_bounds__(MAXT, MAXT <= 192 ? kGUMinCtas : 1) gateup_kernel(GroupParams P) {
+  gateup_body<false>(P, FusedParams{});
+}
+
+// S == 1: the whole expert FFN (gate/up, down, weighting and the reduce) in one cooperative launch.
+template <int MAXT>
+__global__ void __launch_bounds__(MAXT, MAXT <= 192 ? kGUMinCtas : 1) decode_ffn_kernel(GroupParams P, FusedParams F) {
+  gateup_body<true>(P, F);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -678,7 +890,6 @@ struct DownSmem {
   int ok[COLI_MAX_K];
 };
 
-__host__ __device__ constexpr uint32_t down_stage_bytes() { return kBoxRows * kSliceWords * 4 + kBoxRows * kScaleBox * 4; }
 constexpr size_t kDCtrlBytes = (sizeof(DownSmem) + 127) / 128 * 128;
 static_assert(down_stage_bytes() % 128 == 0, "down stage must keep 128-byte alignment");
 
@@ -687,7 +898,7 @@ inline size_t down_smem_bytes(int nwarps) {
 }
 
 template <int MAXT>
-__global__ void __launch_bounds__(MAXT, 1) down_fused_kernel(GroupParams P, int TPE) {
+__global__ void __launch_bounds__(MAXT, 1) down_reduce_kernel(GroupParams P, int TPE) {
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem_raw = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 127) & ~uintptr_t(127));
   DownSmem& sm = *reinterpret_cast<DownSmem*>(smem_raw);
@@ -840,9 +1051,6 @@ __global__ void __launch_bounds__(MAXT, 1) down_fused_kernel(GroupParams P, int 
 
 constexpr int kDU = 4;  // rows per batch of the route-parallel down kernel
 
-// ------------------------------------------------------------------------------------------
-// ------------------------------------------------------------------------------------------
-
 template <int MAXT>
 __global__ void __launch_bounds__(MAXT) down_routes_kernel(GroupParams P) {
   __shared__ float red[2][32][kDU];
@@ -950,21 +1158,57 @@ __global__ void combine_kernel(GroupParams P) {
 
 
 // Launch with programmatic stream serialisation (the kernel may start while its predecessor in
-// the stream finishes; it calls griddepcontrol.wait before reading that predecessor's output).
+// the stream finishes; it calls griddepcontrol.wait before reading that predecessor's output) and,
+// when `coop`, as a cooperative launch (every CTA resident at once, or the launch fails).
 template <typename... KArgs, typename... Args>
 static cudaError_t launch_k(void (*kern)(KArgs...), int grid, int block, size_t smem, cudaStream_t st, bool pdl,
-                            Args... args) {
+                            bool coop, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(block);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    na++;
+  }
+  if (coop) {
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na].val.cooperative = 1;
+    na++;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+__global__ void coop_probe_kernel(int* p) {
+  if (p) *p = 0;
+}
+
+int probe_coop_mode(coli_ctx* ctx) {
+  int coop = 0;
+  if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, ctx->device) != cudaSuccess || !coop) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  cudaStream_t st;
+  if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  int mode = 0;
+  for (int m = 2; m >= 1 && mode == 0; m--) {
+    cudaError_t e = launch_k(coop_probe_kernel, 1, 32, 0, st, m == 2, true, (int*)nullptr);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) mode = m;
+    (void)cudaGetLastError();
+  }
+  cudaStreamDestroy(st);
+  return mode;
 }
 
 int launch_expert_group(coli_ctx* ctx, const void* x, int x_dtype, int S, const int32_t* idx, const float* w,
@@ -973,11 +1217,37 @@ int launch_expert_group(coli_ctx* ctx, const void* x, int x_dtype, int S, const 
   if (S > COLI_MAX_GROUP_TOKENS) return fail(ctx, COLI_E_INVAL, "expert_group: S above COLI_MAX_GROUP_TOKENS");
   const int D = ctx->table_D, I = ctx->table_I;
   if (D > COLI_MAX_GROUP_DIM) return fail(ctx, COLI_E_INVAL, "expert_group: D above COLI_MAX_GROUP_DIM");
+  const int CD = (D + 31) / 32, CI = (I + 31) / 32;
+  const int W = (CD + 31) / 32;  // gate/up warps per CTA
+  const int nt_gu = W * 32;
+  const size_t gu_smem = gateup_smem_bytes(W, S);
+  cudaError_t e;
+  // S == 1: gate/up and down in one cooperative kernel, when its whole grid fits on the device
+  const int nsl = (CI + 31) / 32;
+  bool fused = false;
+  int fused_grid = 0;
+  if (S == 1 && ctx->decode_fused && ctx->coop_mode > 0 && nsl <= kFusedMaxSlices) {
+    auto kern = nt_gu <= 192 ? decode_ffn_kernel<192> : decode_ffn_kernel<256>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gu_smem)) != cudaSuccess)
+      return cuda_fail(ctx, e, "fused decode smem attribute");
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, nt_gu, gu_smem) != cudaSuccess) {
+      (void)cudaGetLastError();
+      occ = 0;
+    }
+    fused_grid = ctx->num_sms * occ;
+    fused = occ > 0 && (long long)fused_grid * W >= (long long)K * nsl;
+  }
+  // otherwise the down projection: S == 1 with all slots' threads in one CTA (down_reduce_kernel),
+  // else per-route rows into yr and a combine
+  const int TPE = (CI + 31) / 32 * 32;
+  const bool down_reduce = S == 1 && K * TPE <= 1024 && down_smem_bytes(K * TPE / 32) <= 220 * 1024;
   const size_t R = (size_t)S * K;
   const size_t h_bytes = align_up(R * I * sizeof(float), 256);
-  const size_t yr_bytes = S > 1 ? align_up(R * D * sizeof(float), 256) : 0;
+  const size_t yr_bytes = (!fused && !down_reduce) ? align_up(R * D * sizeof(float), 256) : 0;
+  const size_t yp_bytes = fused ? align_up((size_t)K * nsl * D * sizeof(float), 256) : 0;
   const size_t plan_bytes = align_up((size_t)(S + 1) * sizeof(int), 256);
-  int rc = ensure_workspace(ctx, h_bytes + yr_bytes + plan_bytes);
+  int rc = ensure_workspace(ctx, h_bytes + yr_bytes + yp_bytes + plan_bytes);
   if (rc != COLI_OK) return rc;
   GroupParams P;
   P.x = x;
@@ -994,39 +1264,44 @@ int launch_expert_group(coli_ctx* ctx, const void* x, int x_dtype, int S, const 
   P.y = y;
   P.h = reinterpret_cast<float*>(ctx->ws.base);
   P.yr = reinterpret_cast<float*>(ctx->ws.base + h_bytes);
-  P.plan = reinterpret_cast<int*>(ctx->ws.base + h_bytes + yr_bytes);
+  P.plan = reinterpret_cast<int*>(ctx->ws.base + h_bytes + yr_bytes + yp_bytes);
   P.err = ctx->d_status;
 
-  const int CD = (D + 31) / 32, CI = (I + 31) / 32;
-  cudaError_t e;
+  if (fused) {
+    FusedParams F;
+    F.ypart = reinterpret_cast<float*>(ctx->ws.base + h_bytes + yr_bytes);
+    F.sync = ctx->d_status + kSyncBase;
+    F.nsl = nsl;
+    auto kern = nt_gu <= 192 ? decode_ffn_kernel<192> : decode_ffn_kernel<256>;
+    ProfScope prof(ctx, COLI_KERNEL_GATEUP);
+    e = launch_k(kern, fused_grid, nt_gu, gu_smem, ctx->stream, ctx->coop_mode == 2, true, P, F);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "fused decode launch");
+    return COLI_OK;
+  }
   {
-    const int W = (CD + 31) / 32;
-    const int nt = W * 32;
-    const size_t smem = gateup_smem_bytes(W, S);
-    auto kern = nt <= 192 ? gateup_kernel<192> : gateup_kernel<256>;
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+    auto kern = nt_gu <= 192 ? gateup_kernel<192> : gateup_kernel<256>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gu_smem)) != cudaSuccess)
       return cuda_fail(ctx, e, "gate/up smem attribute");
     int occ = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, nt, smem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, nt_gu, gu_smem);
     // every CTA's range spans at most kRouteCache routes: (R I / grid) <= (kRouteCache - 2) I
     long long grid = (long long)ctx->num_sms * (occ > 0 ? occ : 1);
     const long long min_grid = ((long long)S * K + kRouteCache - 3) / (kRouteCache - 2);
     if (grid < min_grid) grid = min_grid;
     ProfScope prof(ctx, COLI_KERNEL_GATEUP);
-    e = launch_k(kern, (int)grid, nt, smem, ctx->stream, true, P);
+    e = launch_k(kern, (int)grid, nt_gu, gu_smem, ctx->stream, true, false, P);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "gate/up launch");
   }
-  const int TPE = (CI + 31) / 32 * 32;
-  if (S == 1 && K * TPE <= 1024 && down_smem_bytes(K * TPE / 32) <= 220 * 1024) {
+  if (down_reduce) {
     const int nt = K * TPE;
     const size_t smem = down_smem_bytes(nt / 32);
-    auto kern = nt <= 256 ? down_fused_kernel<256> : (nt <= 512 ? down_fused_kernel<512> : down_fused_kernel<1024>);
+    auto kern = nt <= 256 ? down_reduce_kernel<256> : (nt <= 512 ? down_reduce_kernel<512> : down_reduce_kernel<1024>);
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
       return cuda_fail(ctx, e, "down smem attribute");
     int grid = ctx->num_sms;
     if (grid > D) grid = D;
     ProfScope prof(ctx, COLI_KERNEL_DOWN);
-    e = launch_k(kern, grid, nt, smem, ctx->stream, true, P, TPE);
+    e = launch_k(kern, grid, nt, smem, ctx->stream, true, false, P, TPE);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "down launch");
   } else {
     auto kern = TPE <= 256 ? down_routes_kernel<256> : (TPE <= 512 ? down_routes_kernel<512> : down_routes_kernel<1024>);

@@ -1,8 +1,9 @@
 // Device helpers for streaming kernels on sm_100-family GPUs: mbarriers, bulk asynchronous copies
 // (TMA) global -> shared memory, and programmatic dependent launch controls.
-// Every wait is bounded: a waiting thread sleeps in mbarrier.try_wait (woken when the phase
-// completes) and gives up after kWaitLimitNs of wall-clock time; the caller then records
-// COLI_E_TIMEOUT in the context's error word instead of hanging.
+// Every wait is bounded: a waiting thread polls its mbarrier phase (or, with COLI_WAIT_SPIN=0,
+// sleeps in mbarrier.try_wait until the phase completes) and gives up after kWaitLimitNs of
+// wall-clock time; the caller then records COLI_E_TIMEOUT in the context's error word instead of
+// hanging.
 #pragma once
 
 #include <stdint.h>
@@ -63,13 +64,41 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+#ifndef COLI_WAIT_SPIN
+#define COLI_WAIT_SPIN 1
+#endif
+
 // Wait until the phase with the given parity has completed; false after kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+#if COLI_WAIT_SPIN
+  // poll the non-blocking test: the thread sees the phase complete within a few hundred cycles
+  // (a suspended try_wait can resume well after the phase completed)
+  for (int i = 0; i < 64; i++)
+    if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_test_wait(bar, parity)) {
+    __nanosleep(32);
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+#else
   if (mbar_try_wait_sleep(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait_sleep(bar, parity))
     if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
   return true;
+#endif
 }
 
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from global to shared
@@ -137,7 +166,7 @@ __device__ __forceinline__ void prefetch_l2_line(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
-// Programmatic dependent launch: wait for the preceding grid's completion and memory flush /// Programmatic dependent launch: wait for the preceding grid's completion and memory flush /
+// Programmatic dependent launch: wait for the preceding grid's completion and memory flush /
 // allow the next grid in the stream to start launching.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
@@ -186,6 +215,51 @@ __device__ __forceinline__ float ld_cg_f32(const float* p) {
   float v;
   asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
   return v;
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Barrier over every CTA of a cooperative launch (all CTAs are resident). `count` only grows: CTA
+// arrivals of this and every earlier use of the same word, G = gridDim.x per use, so this use is
+// complete when the count reaches the next multiple of G above the value this CTA saw. Nothing is
+// reset, and the last CTA to arrive leaves at once. Every thread's global writes before the call
+// are visible to every thread after it. Returns false (the wait gave up after kWaitLimitNs)
+// uniformly across the CTA.
+__device__ __forceinline__ bool grid_barrier(unsigned long long* count) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    const unsigned long long G = gridDim.x;
+    unsigned long long old;
+    asm volatile("atom.add.release.gpu.u64 %0, [%1], 1;" : "=l"(old) : "l"(count) : "memory");
+    const unsigned long long target = (old / G + 1) * G;
+    if (old + 1 != target) {
+      const uint64_t t0 = globaltimer_ns();
+      for (;;) {
+        unsigned long long now;
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(now) : "l"(count) : "memory");
+        if (now >= target) break;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          ok = 0;
+          break;
+        }
+      }
+    } else {
+      asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    }
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
 }
 
 }  // namespace coli
