@@ -37,7 +37,6 @@ namespace coli {
 constexpr int kPfRows = COLI_PF_ROWS;  // tokens (GEMM N) per work entry
 constexpr int kPfPad = 16;      // per-entry token blocks are padded to a multiple of 16
 constexpr int kPfKTile = 64;    // K columns per pipeline stage
-constexpr int kPfStages = 3;
 constexpr int kPfConvWarps = COLI_PF_CONV_WARPS;  // warps 3.. convert; warps 4..7 also drain the accumulator
 constexpr int kPfThreads = (3 + kPfConvWarps) * 32;  // + the two producer warps and the MMA warp
 constexpr uint32_t kPfTileBytes = kTcRows * 128;       // one bf16 operand tile: 128 rows x 128 bytes
@@ -301,25 +300,9 @@ inline size_t pf_smem_bytes() {
   return 1024 + 1024 + PfLayout<DUAL>::kBytes;
 }
 
-#ifndef COLI_PF_POLL
-#define COLI_PF_POLL 0
-#endif
-// Wait for a ring barrier; COLI_PF_POLL polls try_wait without a suspend-time hint.
-__device__ __forceinline__ bool pf_mbar_wait(uint64_t* bar, uint32_t parity) {
-#if COLI_PF_POLL
-  if (mbar_test_parity(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_test_parity(bar, parity))
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-  return true;
-#else
-  return mbar_wait(bar, parity);
-#endif
-}
-
 __device__ __forceinline__ bool pf_wait(PfCtrl& c, uint64_t* bar, uint32_t parity, int* err) {
   if (ld_volatile_int(&c.stop)) return false;
-  if (pf_mbar_wait(bar, parity)) return true;
+  if (mbar_wait(bar, parity)) return true;
   set_error(err, COLI_E_TIMEOUT);
   *reinterpret_cast<volatile int*>(&c.stop) = 1;
   return false;

@@ -14,7 +14,14 @@
 
 namespace coli {
 
-constexpr int kRouterThreads = 256;
+#ifndef COLI_ROUTER_THREADS
+#define COLI_ROUTER_THREADS 256
+#endif
+#ifndef COLI_ROUTER_UNROLL
+#define COLI_ROUTER_UNROLL 4
+#endif
+constexpr int kRouterThreads = COLI_ROUTER_THREADS;
+constexpr int kRouterUnroll = COLI_ROUTER_UNROLL;  // float4 loads of one thread in flight together
 #ifndef COLI_ROUTER_ROWS
 #define COLI_ROUTER_ROWS 1
 #endif
@@ -148,7 +155,7 @@ __device__ __forceinline__ void router_body(const void* __restrict__ x, int x_dt
     for (int r = 0; r < kRowsPerCta; r++) acc[r] = 0.f;
     if (VEC4 && x_dtype == COLI_DTYPE_F32) {
       const float4* x4 = reinterpret_cast<const float4*>(static_cast<const float*>(x) + (size_t)t * D);
-#pragma unroll 4
+#pragma unroll kRouterUnroll
       for (int j = tid; j < D / 4; j += kRouterThreads) {
         const float4 b = __ldg(x4 + j);
 #pragma unroll
