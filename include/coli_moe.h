@@ -63,6 +63,7 @@ extern "C" {
 #define COLI_MAX_TOKENS 65536   /* S for coli_router_select */
 #define COLI_MAX_GROUP_TOKENS 1024  /* S for coli_expert_group */
 #define COLI_MAX_GROUP_DIM 8192     /* D (model width) for coli_expert_group */
+#define COLI_MAX_ISSUES 16          /* pending coli_expert_group_issue calls per round */
 
 typedef struct coli_ctx coli_ctx;
 
@@ -189,6 +190,31 @@ COLI_API int coli_expert_table_set(coli_ctx *ctx, int e, uint64_t gate, uint64_t
 COLI_API int coli_expert_group(coli_ctx *ctx, const void *x_rows, int x_dtype, int S,
                       const int32_t *idx, const float *w, const int32_t *n_sel, int K,
                       const void *resid, void *y);
+
+/*
+ * Resident issue/take, [resid] "What": the expert groups of one layer are issued one by one and
+ * their results stay on the device; one take joins them to the residual. Nothing is copied to the
+ * host and nothing synchronises, so a whole decode layer (router, issues, take) can be captured in
+ * one CUDA graph.
+ *
+ * coli_expert_group_issue: the routes (x_rows, idx, w, n_sel, K as for coli_expert_group) are one
+ * group; its weighted, slot-ordered sum  p_j[s,:] = sum_{k < n_sel[s]} w[s,k] * y_k  (no residual)
+ * goes into the context's partial-sum slot j, kept in f32 whatever x_dtype is. Returns j >= 0, the
+ * issue index of this round, or a negative COLI_E_* code. Every issue of a round must have the
+ * same S, x_dtype and table D (COLI_E_INVAL otherwise), and at most COLI_MAX_ISSUES may be pending.
+ * The first issue of a round sizes the slot pool (COLI_MAX_ISSUES x S x D floats; it may allocate
+ * and wait for the stream): call coli_reserve first, or run one round, before any stream capture.
+ *
+ * coli_expert_group_take: y[s,:] = resid[s,:] + (p_0 + p_1 + ... + p_{n-1})[s,:], the partial sums
+ * added in issue order in binary32 and then added to the residual (resid NULL: no residual); resid
+ * and y are [S x D] in the round's x_dtype, device pointers. The round ends and the next issue
+ * starts a new one. COLI_E_INVAL if nothing was issued; on a launch failure the round is kept.
+ * With one issue holding all of a token's routes, y is bit-identical to coli_expert_group's.
+ * The take is profiled as COLI_KERNEL_COMBINE.
+ */
+COLI_API int coli_expert_group_issue(coli_ctx *ctx, const void *x_rows, int x_dtype, int S,
+                            const int32_t *idx, const float *w, const int32_t *n_sel, int K);
+COLI_API int coli_expert_group_take(coli_ctx *ctx, const void *resid, void *y);
 
 #ifdef __cplusplus
 }

@@ -41,6 +41,7 @@ COLI_DTYPE_F32 = _C["COLI_DTYPE_F32"]
 COLI_DTYPE_BF16 = _C["COLI_DTYPE_BF16"]
 COLI_MAX_EXPERTS = _C["COLI_MAX_EXPERTS"]
 COLI_MAX_K = _C["COLI_MAX_K"]
+COLI_MAX_ISSUES = _C["COLI_MAX_ISSUES"]
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -61,6 +62,8 @@ SIGNATURES = {
     "coli_expert_free": (_I, [_P, _U64]),
     "coli_expert_table_set": (_I, [_P, _I, _U64, _U64, _U64]),
     "coli_expert_group": (_I, [_P, _P, _I, _I, _P, _P, _P, _I, _P, _P]),
+    "coli_expert_group_issue": (_I, [_P, _P, _I, _I, _P, _P, _P, _I]),
+    "coli_expert_group_take": (_I, [_P, _P, _P]),
     "coli_profile_enable": (_I, [_P, _I]),
     "coli_profile_read": (_I, [_P, _I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong)]),
 }
@@ -232,6 +235,30 @@ def coli_expert_group(ctx, x_rows, idx, w, n_sel, K, resid, y):
     rc = library().coli_expert_group(ctx, _ptr(x_rows), act_dtype(x_rows), S, _ptr(idx), _ptr(w), _ptr(n_sel), K,
                                      _ptr(resid), _ptr(y))
     return _check(ctx, rc, "coli_expert_group")
+
+
+def coli_expert_group_issue(ctx, x_rows, idx, w, n_sel, K):
+    """Issue one group of routes; returns its issue index in the current round."""
+    S = x_rows.shape[0]
+    _dev(x_rows, name="x_rows")
+    _dev(idx, torch.int32, "idx")
+    _dev(w, torch.float32, "w")
+    _dev(n_sel, torch.int32, "n_sel")
+    if idx.numel() != S * K or w.numel() != S * K or (n_sel is not None and n_sel.numel() != S):
+        raise ValueError("expert_group_issue: inconsistent shapes")
+    rc = library().coli_expert_group_issue(ctx, _ptr(x_rows), act_dtype(x_rows), S, _ptr(idx), _ptr(w), _ptr(n_sel), K)
+    if rc < 0:
+        raise ColiError(rc, f"coli_expert_group_issue: {coli_last_error(ctx)}")
+    return rc
+
+
+def coli_expert_group_take(ctx, resid, y):
+    """Join the round's issued partial sums, in issue order, to the residual: y = resid + sum."""
+    _dev(resid, y.dtype, "resid")
+    _dev(y, name="y")
+    if resid is not None and resid.shape != y.shape:
+        raise ValueError("expert_group_take: inconsistent shapes")
+    return _check(ctx, library().coli_expert_group_take(ctx, _ptr(resid), _ptr(y)), "coli_expert_group_take")
 
 
 def coli_profile_enable(ctx, on):

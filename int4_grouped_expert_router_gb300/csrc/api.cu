@@ -53,6 +53,26 @@ int ensure_workspace(coli_ctx* ctx, size_t bytes) {
   return COLI_OK;
 }
 
+// The issue/take slot pool. It only grows at the first issue of a round (or in coli_reserve), when no
+// slot holds a pending partial sum; the old pool is freed after the stream has drained.
+int ensure_slots(coli_ctx* ctx, size_t bytes) {
+  bytes = align_up(bytes < 256 ? 256 : bytes, 256);
+  if (bytes <= ctx->slot_bytes) return COLI_OK;
+  if (ctx->slots) {
+    cudaError_t e = cudaStreamSynchronize(ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "slot pool grow: stream sync");
+    cudaFree(ctx->slots);
+    ctx->slots = nullptr;
+    ctx->slot_bytes = 0;
+  }
+  void* p = nullptr;
+  cudaError_t e = cudaMalloc(&p, bytes);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "slot pool cudaMalloc");
+  ctx->slots = static_cast<float*>(p);
+  ctx->slot_bytes = bytes;
+  return COLI_OK;
+}
+
 static cudaEvent_t prof_event(coli_ctx* ctx) {
   if (!ctx->prof_free.empty()) {
     cudaEvent_t e = ctx->prof_free.back();
@@ -229,6 +249,7 @@ void coli_destroy(coli_ctx* ctx) {
   if (ctx->d_table) cudaFree(ctx->d_table);
   if (ctx->d_status) cudaFree(ctx->d_status);
   if (ctx->ws.base) cudaFree(ctx->ws.base);
+  if (ctx->slots) cudaFree(ctx->slots);
   for (auto& r : ctx->prof_pending) {
     cudaEventDestroy(r.a);
     cudaEventDestroy(r.b);
@@ -313,7 +334,10 @@ int coli_reserve(coli_ctx* ctx, int max_S, int max_E, int max_K, int max_D, int 
   const size_t prefill = pf_rows * ((size_t)max_D * 2 + (size_t)max_I * 2 + (size_t)max_D * 4 + 4) + routes * 4 +
                          (size_t)max_E * 8 + (routes / 128 + max_E + 1) * 16 + 16 * 256;
   if (prefill > experts) experts = prefill;
+  const size_t slots = (size_t)COLI_MAX_ISSUES * max_S * max_D * sizeof(float);
   cudaSetDevice(ctx->device);
+  int rc = ensure_slots(ctx, slots);
+  if (rc != COLI_OK) return rc;
   return ensure_workspace(ctx, router > experts ? router : experts);
 }
 
@@ -476,9 +500,49 @@ int coli_expert_group(coli_ctx* ctx, const void* x_rows, int x_dtype, int S, con
   if (ctx->table_count == 0) return fail(ctx, COLI_E_INVAL, "expert_group: expert table is empty");
   if (injected(ctx)) return COLI_E_INJECTED;
   cudaSetDevice(ctx->device);
-  int rc = launch_expert_group(ctx, x_rows, x_dtype, S, idx, w, n_sel, K, resid, y);
+  int rc = launch_expert_group(ctx, x_rows, x_dtype, S, idx, w, n_sel, K, resid, y, x_dtype);
   if (rc == COLI_OK) ctx->compute_calls++;
   return rc;
+}
+
+int coli_expert_group_issue(coli_ctx* ctx, const void* x_rows, int x_dtype, int S, const int32_t* idx,
+                            const float* w, const int32_t* n_sel, int K) {
+  if (!ctx) return COLI_E_INVAL;
+  if (!x_rows || !idx || !w) return fail(ctx, COLI_E_INVAL, "issue: NULL pointer");
+  if (x_dtype != COLI_DTYPE_F32 && x_dtype != COLI_DTYPE_BF16) return fail(ctx, COLI_E_INVAL, "issue: dtype");
+  if (S < 1 || S > COLI_MAX_TOKENS || K < 1 || K > COLI_MAX_K) return fail(ctx, COLI_E_INVAL, "issue: size out of range");
+  if (ctx->table_count == 0) return fail(ctx, COLI_E_INVAL, "issue: expert table is empty");
+  if (ctx->n_issued >= COLI_MAX_ISSUES) return fail(ctx, COLI_E_INVAL, "issue: COLI_MAX_ISSUES issues already pending");
+  if (ctx->n_issued > 0 && (S != ctx->round_S || x_dtype != ctx->round_dtype || ctx->table_D != ctx->round_D))
+    return fail(ctx, COLI_E_INVAL, "issue: S, dtype and D must match the round's first issue");
+  if (injected(ctx)) return COLI_E_INJECTED;
+  cudaSetDevice(ctx->device);
+  const int D = ctx->table_D;
+  if (ctx->n_issued == 0) {
+    int rc = ensure_slots(ctx, (size_t)COLI_MAX_ISSUES * S * D * sizeof(float));
+    if (rc != COLI_OK) return rc;
+    ctx->round_S = S;
+    ctx->round_D = D;
+    ctx->round_dtype = x_dtype;
+  }
+  float* slot = ctx->slots + (size_t)ctx->n_issued * S * D;
+  int rc = launch_expert_group(ctx, x_rows, x_dtype, S, idx, w, n_sel, K, nullptr, slot, COLI_DTYPE_F32);
+  if (rc != COLI_OK) return rc;
+  ctx->compute_calls++;
+  return ctx->n_issued++;
+}
+
+int coli_expert_group_take(coli_ctx* ctx, const void* resid, void* y) {
+  if (!ctx) return COLI_E_INVAL;
+  if (!y) return fail(ctx, COLI_E_INVAL, "take: NULL pointer");
+  if (ctx->n_issued == 0) return fail(ctx, COLI_E_INVAL, "take: nothing issued");
+  if (injected(ctx)) return COLI_E_INJECTED;
+  cudaSetDevice(ctx->device);
+  int rc = launch_take(ctx, ctx->round_S, ctx->round_D, ctx->n_issued, resid, ctx->round_dtype, y);
+  if (rc != COLI_OK) return rc;
+  ctx->compute_calls++;
+  ctx->n_issued = 0;
+  return COLI_OK;
 }
 
 }  // extern "C"

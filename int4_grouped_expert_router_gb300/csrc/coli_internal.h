@@ -104,6 +104,10 @@ struct coli_ctx {
   bool decode_fused = false;
   int coop_mode = -1;  // -1: not probed yet
   coli::Workspace ws;
+  // resident issue/take: f32 partial sums [COLI_MAX_ISSUES][S x D] of the current round's issues
+  float* slots = nullptr;
+  size_t slot_bytes = 0;
+  int n_issued = 0, round_S = 0, round_D = 0, round_dtype = 0;
   // COLI_FAIL_AFTER test hook
   long long fail_after = -1;
   long long compute_calls = 0;
@@ -125,6 +129,7 @@ int fail(coli_ctx* ctx, int code, const std::string& msg);
 int cuda_fail(coli_ctx* ctx, cudaError_t e, const char* what);
 bool injected(coli_ctx* ctx);  // COLI_FAIL_AFTER: true if this compute call must fail
 int ensure_workspace(coli_ctx* ctx, size_t bytes);
+int ensure_slots(coli_ctx* ctx, size_t bytes);
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -144,7 +149,7 @@ int launch_router(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const
 // Tensor-core (prefill) path of coli_expert_group: bf16 activations, many routed rows per expert.
 bool prefill_eligible(const coli_ctx* ctx, const void* x, int S, int K, int x_dtype);
 int launch_prefill(coli_ctx* ctx, const void* x, int S, const int32_t* idx, const float* w, const int32_t* n_sel,
-                   int K, const void* resid, void* y);
+                   int K, const void* resid, void* y, int y_dtype);
 // TMA map over a row-major bf16 matrix [rows x cols] read in 16-row x 64-column boxes with the
 // 128-byte swizzle (cols a multiple of 8).
 int encode_bf16_rows_map(coli_ctx* ctx, CUtensorMap* map, void* base, long long rows, int cols);
@@ -152,8 +157,11 @@ int encode_bf16_rows_map(coli_ctx* ctx, CUtensorMap* map, void* base, long long 
 int launch_router_noalloc(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr,
                           const float* bias, int E, int K, float topp, int norm_topk, float routed_scale,
                           int32_t* idx, float* w, int32_t* n_sel);
+// y is written in y_dtype (x_dtype for coli_expert_group; f32 for an issued partial sum); resid is read in x_dtype.
 int launch_expert_group(coli_ctx* ctx, const void* x, int x_dtype, int S, const int32_t* idx,
-                        const float* w, const int32_t* n_sel, int K, const void* resid, void* y);
+                        const float* w, const int32_t* n_sel, int K, const void* resid, void* y, int y_dtype);
+// y [S x D] (dtype) = resid + the n issued partial sums [S x D] f32, added in issue order.
+int launch_take(coli_ctx* ctx, int S, int D, int n, const void* resid, int dtype, void* y);
 // Which cooperative launch forms this device accepts (coli_ctx::coop_mode), found with an empty
 // kernel on a private stream.
 int probe_coop_mode(coli_ctx* ctx);

@@ -263,7 +263,8 @@ __device__ __forceinline__ int route_token(const int* pre, int S, int j) {
 
 struct GroupParams {
   const void* x;
-  int x_dtype;
+  int x_dtype;     // dtype of x and resid
+  int y_dtype;     // dtype of y (x_dtype, or f32 for an issued partial sum)
   int S, D, I, K;
   const int32_t* idx;
   const float* w;
@@ -542,7 +543,7 @@ __device__ __forceinline__ void fused_finish_rows(const GroupParams& P, const Fu
     float res = 0.f;
     if (P.resid) res = load_act(P.resid, P.x_dtype, d);
     if (P.resid) acc = res + acc;
-    if (P.x_dtype == COLI_DTYPE_F32)
+    if (P.y_dtype == COLI_DTYPE_F32)
       static_cast<float*>(P.y)[d] = acc;
     else
       static_cast<uint16_t*>(P.y)[d] = f32_to_bf16_rn(acc);
@@ -559,7 +560,7 @@ __device__ __forceinline__ void fused_down_phase(const GroupParams& P, const Fus
     for (int d = blockIdx.x * blockDim.x + tid; d < P.D; d += gridDim.x * blockDim.x) {
       float acc = 0.f;
       if (P.resid) acc = load_act(P.resid, P.x_dtype, d) + acc;
-      if (P.x_dtype == COLI_DTYPE_F32)
+      if (P.y_dtype == COLI_DTYPE_F32)
         static_cast<float*>(P.y)[d] = acc;
       else
         static_cast<uint16_t*>(P.y)[d] = f32_to_bf16_rn(acc);
@@ -1032,7 +1033,7 @@ __global__ void __launch_bounds__(MAXT, 1) down_reduce_kernel(GroupParams P, int
         acc = fmaf(sm.wk[kk], yk * sm.rscale[kk][tid], acc);
       }
       if (P.resid) acc = res + acc;
-      if (P.x_dtype == COLI_DTYPE_F32)
+      if (P.y_dtype == COLI_DTYPE_F32)
         static_cast<float*>(P.y)[d] = acc;
       else
         static_cast<uint16_t*>(P.y)[d] = f32_to_bf16_rn(acc);
@@ -1145,11 +1146,40 @@ __global__ void combine_kernel(GroupParams P) {
     float acc = 0.f;
     for (int k = 0; k < m; k++) acc = fmaf(__ldg(P.w + (size_t)t * P.K + k), P.yr[(size_t)(j0 + k) * P.D + d], acc);
     if (P.resid) acc = load_act(P.resid, P.x_dtype, i) + acc;
-    if (P.x_dtype == COLI_DTYPE_F32)
+    if (P.y_dtype == COLI_DTYPE_F32)
       static_cast<float*>(P.y)[i] = acc;
     else
       static_cast<uint16_t*>(P.y)[i] = f32_to_bf16_rn(acc);
   }
+}
+
+// ------------------------------------------------------------------------------------------
+// Resident take: the issued groups' partial sums, in issue order, joined to the residual.
+// ------------------------------------------------------------------------------------------
+
+__global__ void take_kernel(const float* __restrict__ slots, int n, long long cells, const void* resid, int dtype,
+                            void* y) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < cells; i += (long long)gridDim.x * blockDim.x) {
+    float acc = __ldcg(slots + i);
+    for (int j = 1; j < n; j++) acc = __fadd_rn(acc, __ldcg(slots + (size_t)j * cells + i));
+    if (resid) acc = load_act(resid, dtype, i) + acc;
+    if (dtype == COLI_DTYPE_F32)
+      static_cast<float*>(y)[i] = acc;
+    else
+      static_cast<uint16_t*>(y)[i] = f32_to_bf16_rn(acc);
+  }
+}
+
+int launch_take(coli_ctx* ctx, int S, int D, int n, const void* resid, int dtype, void* y) {
+  const long long cells = (long long)S * D;
+  int grid = (int)((cells + 255) / 256);
+  if (grid > 4 * ctx->num_sms) grid = 4 * ctx->num_sms;
+  {
+    ProfScope prof(ctx, COLI_KERNEL_COMBINE);
+    take_kernel<<<grid, 256, 0, ctx->stream>>>(ctx->slots, n, cells, resid, dtype, y);
+  }
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? COLI_OK : cuda_fail(ctx, e, "take launch");
 }
 
 // ------------------------------------------------------------------------------------------
@@ -1212,8 +1242,8 @@ int probe_coop_mode(coli_ctx* ctx) {
 }
 
 int launch_expert_group(coli_ctx* ctx, const void* x, int x_dtype, int S, const int32_t* idx, const float* w,
-                        const int32_t* n_sel, int K, const void* resid, void* y) {
-  if (prefill_eligible(ctx, x, S, K, x_dtype)) return launch_prefill(ctx, x, S, idx, w, n_sel, K, resid, y);
+                        const int32_t* n_sel, int K, const void* resid, void* y, int y_dtype) {
+  if (prefill_eligible(ctx, x, S, K, x_dtype)) return launch_prefill(ctx, x, S, idx, w, n_sel, K, resid, y, y_dtype);
   if (S > COLI_MAX_GROUP_TOKENS) return fail(ctx, COLI_E_INVAL, "expert_group: S above COLI_MAX_GROUP_TOKENS");
   const int D = ctx->table_D, I = ctx->table_I;
   if (D > COLI_MAX_GROUP_DIM) return fail(ctx, COLI_E_INVAL, "expert_group: D above COLI_MAX_GROUP_DIM");
@@ -1252,6 +1282,7 @@ int launch_expert_group(coli_ctx* ctx, const void* x, int x_dtype, int S, const 
   GroupParams P;
   P.x = x;
   P.x_dtype = x_dtype;
+  P.y_dtype = y_dtype;
   P.S = S;
   P.D = D;
   P.I = I;

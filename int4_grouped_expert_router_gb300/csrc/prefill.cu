@@ -577,7 +577,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(PfGemmParams P, 
 
 __global__ void pf_combine_kernel(const float* __restrict__ yr, const int* __restrict__ pos, const float* __restrict__ w,
                                   const int32_t* __restrict__ n_sel, int S, int K, int D, const void* resid, int dtype,
-                                  void* y, int* err) {
+                                  void* y, int y_dtype, int* err) {
   const long long n = (long long)S * D;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
     const int t = (int)(i / D), d = (int)(i - (long long)t * D);
@@ -593,7 +593,7 @@ __global__ void pf_combine_kernel(const float* __restrict__ yr, const int* __res
       acc = fmaf(__ldg(w + t * K + k), __ldg(yr + (size_t)p * D + d), acc);
     }
     if (resid) acc = load_act(resid, dtype, (size_t)t * D + d) + acc;
-    if (dtype == COLI_DTYPE_F32)
+    if (y_dtype == COLI_DTYPE_F32)
       static_cast<float*>(y)[(size_t)t * D + d] = acc;
     else
       static_cast<uint16_t*>(y)[(size_t)t * D + d] = f32_to_bf16_rn(acc);
@@ -620,7 +620,7 @@ bool prefill_eligible(const coli_ctx* ctx, const void* x, int S, int K, int x_dt
 }
 
 int launch_prefill(coli_ctx* ctx, const void* x, int S, const int32_t* idx, const float* w, const int32_t* n_sel,
-                   int K, const void* resid, void* y) {
+                   int K, const void* resid, void* y, int y_dtype) {
   const int D = ctx->table_D, I = ctx->table_I;
   int E = 0, n_valid = 0;
   for (int e = 0; e < COLI_MAX_EXPERTS; e++)
@@ -711,7 +711,8 @@ int launch_prefill(coli_ctx* ctx, const void* x, int S, const int32_t* idx, cons
     int grid = (int)((n + 255) / 256);
     if (grid > 8 * ctx->num_sms) grid = 8 * ctx->num_sms;
     ProfScope prof(ctx, COLI_KERNEL_COMBINE);
-    pf_combine_kernel<<<grid, 256, 0, ctx->stream>>>(yr, pos, w, n_sel, S, K, D, resid, COLI_DTYPE_BF16, y, ctx->d_status);
+    pf_combine_kernel<<<grid, 256, 0, ctx->stream>>>(yr, pos, w, n_sel, S, K, D, resid, COLI_DTYPE_BF16, y, y_dtype,
+                                                     ctx->d_status);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(ctx, e, "prefill combine launch");
   }
   return COLI_OK;
