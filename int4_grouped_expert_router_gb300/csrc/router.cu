@@ -34,6 +34,10 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+__device__ void select_finish(int mine, float wmine, int K, float topp, int norm_topk, float routed_scale,
+                              int32_t* __restrict__ idx_out, float* __restrict__ w_out, int32_t* __restrict__ nsel_out,
+                              const ExpertDesc* table);
+
 // One warp selects for one token. Lane l owns experts e = l + 32 * i (i < EPL). Each round, every
 // lane finds its best not-yet-chosen expert by a strict '>' scan in increasing e (so its first,
 // lowest index wins a local tie); the warp maximum of the order keys and then the minimum index
@@ -87,7 +91,15 @@ __device__ void select_token(const float2* __restrict__ sc_row, int E, int K, fl
       wmine = ws;
     }
   }
-  // weights from the raw (bias-free) score; every sum in slot order in binary32, no contraction
+  select_finish(mine, wmine, K, topp, norm_topk, routed_scale, idx_out, w_out, nsel_out, table);
+}
+
+// Lane k holds the expert of slot k (mine) and its raw score (wmine): weights from the raw
+// (bias-free) score, top-p, norm and scale; every sum in slot order in binary32, no contraction.
+__device__ void select_finish(int mine, float wmine, int K, float topp, int norm_topk, float routed_scale,
+                              int32_t* __restrict__ idx_out, float* __restrict__ w_out, int32_t* __restrict__ nsel_out,
+                              const ExpertDesc* table) {
+  const int lane = threadIdx.x & 31;
   int m = K;
   float denom = 1.f;
   float total = 0.f;
@@ -120,13 +132,73 @@ __device__ void select_token(const float2* __restrict__ sc_row, int E, int K, fl
       prefetch_l2_line(reinterpret_cast<const char*>(table + mine) + 128 * l);
 }
 
+// Selection for 1024 < E <= COLI_MAX_EXPERTS (more than 32 experts per lane): the same rules and
+// reductions as select_token, but each round re-reads the lane's (score, choice) pairs through L2
+// instead of holding them in registers, and the chosen set is a 128-bit mask per lane.
+__device__ void select_token_large(const float2* __restrict__ sc_row, int E, int K, float topp, int norm_topk,
+                                   float routed_scale, int32_t* __restrict__ idx_out, float* __restrict__ w_out,
+                                   int32_t* __restrict__ nsel_out, int* err, const ExpertDesc* table) {
+  const int lane = threadIdx.x & 31;
+  const int epl = (E + 31) >> 5;           // <= 128
+  uint32_t taken[4] = {0u, 0u, 0u, 0u};   // bit i: expert lane + 32 i already chosen (or absent)
+  bool bad = false;
+  for (int i = 0; i < epl; i++) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      const float2 v = __ldcg(sc_row + e);
+      if (!isfinite(v.x) || !isfinite(v.y)) bad = true;
+    } else {
+      taken[i >> 5] |= 1u << (i & 31);
+    }
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) set_error(err, COLI_E_NONFINITE);
+  int mine = -1;
+  float wmine = 0.f;
+  for (int k = 0; k < K; k++) {
+    uint32_t bk = 0;
+    int bi = -1;
+    float bs = 0.f;
+    for (int i = 0; i < epl; i++) {
+      if (taken[i >> 5] & (1u << (i & 31))) continue;
+      const float2 v = __ldcg(sc_row + lane + 32 * i);
+      const uint32_t key = order_key(v.y);
+      if (bi < 0 || key > bk) {
+        bk = key;
+        bi = i;
+        bs = v.x;
+      }
+    }
+    const uint32_t best = __reduce_max_sync(0xffffffffu, bi >= 0 ? bk : 0u);
+    const uint32_t cand = (bi >= 0 && bk == best) ? (uint32_t)(lane + 32 * bi) : 0xffffffffu;
+    const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+    const float ws = __shfl_sync(0xffffffffu, bs, win & 31);
+    if ((int)(win & 31) == lane) taken[(win >> 5) >> 5] |= 1u << ((win >> 5) & 31);
+    if (lane == k) {
+      mine = (int)win;
+      wmine = ws;
+    }
+  }
+  select_finish(mine, wmine, K, topp, norm_topk, routed_scale, idx_out, w_out, nsel_out, table);
+}
+
+// EPL = experts per lane (a power of two up to 32); EPL = 0: the large-E selection.
+template <int EPL>
+__device__ __forceinline__ void select_token_any(const float2* sc_row, int E, int K, float topp, int norm_topk,
+                                                 float routed_scale, int32_t* idx_out, float* w_out, int32_t* nsel_out,
+                                                 int* err, const ExpertDesc* table) {
+  if constexpr (EPL == 0)
+    select_token_large(sc_row, E, K, topp, norm_topk, routed_scale, idx_out, w_out, nsel_out, err, table);
+  else
+    select_token<EPL>(sc_row, E, K, topp, norm_topk, routed_scale, idx_out, w_out, nsel_out, err, table);
+}
+
 template <int EPL>
 __device__ void select_all(const float2* sc, int S, int E, int K, float topp, int norm_topk, float routed_scale,
                            int32_t* idx, float* w, int32_t* n_sel, int* err, const ExpertDesc* table) {
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   for (int t = warp; t < S; t += nwarps)
-    select_token<EPL>(sc + (size_t)t * E, E, K, topp, norm_topk, routed_scale, idx + (size_t)t * K, w + (size_t)t * K,
-                      n_sel ? n_sel + t : nullptr, err, table);
+    select_token_any<EPL>(sc + (size_t)t * E, E, K, topp, norm_topk, routed_scale, idx + (size_t)t * K,
+                          w + (size_t)t * K, n_sel ? n_sel + t : nullptr, err, table);
 }
 
 // Logits GEMV: CTA b computes rows e = b * kRowsPerCta + r (r < kRowsPerCta) for every token;
@@ -211,7 +283,8 @@ __device__ __forceinline__ void router_body(const void* __restrict__ x, int x_dt
     case 4: select_all<4>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
     case 8: select_all<8>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
     case 16: select_all<16>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
-    default: select_all<32>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
+    case 32: select_all<32>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
+    default: select_all<0>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
   }
   __syncthreads();
   if (tid == 0) atomicExch(arrivals, 0u);
@@ -320,8 +393,8 @@ __global__ void router_select_kernel(const float2* sc, int S, int E, int K, floa
                                      const ExpertDesc* table) {
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= S) return;  // uniform per warp
-  select_token<EPL>(sc + (size_t)t * E, E, K, topp, norm_topk, routed_scale, idx + (size_t)t * K, w + (size_t)t * K,
-                    n_sel ? n_sel + t : nullptr, err, table);
+  select_token_any<EPL>(sc + (size_t)t * E, E, K, topp, norm_topk, routed_scale, idx + (size_t)t * K,
+                        w + (size_t)t * K, n_sel ? n_sel + t : nullptr, err, table);
 }
 
 // sc_ws: S E (score, choice) pairs; part: kRSplit S E floats
@@ -350,9 +423,10 @@ static int launch_router_batched(coli_ctx* ctx, const void* x, int x_dtype, int 
     COLI_SELECT_CASE(4)
     COLI_SELECT_CASE(8)
     COLI_SELECT_CASE(16)
-    default:
-      router_select_kernel<32><<<sg, 256, 0, ctx->stream>>>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel,
-                                                             ctx->d_status, table);
+    COLI_SELECT_CASE(32)
+    default:  // more than 1024 experts
+      router_select_kernel<0><<<sg, 256, 0, ctx->stream>>>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel,
+                                                            ctx->d_status, table);
 #undef COLI_SELECT_CASE
   }
   cudaError_t e = cudaGetLastError();

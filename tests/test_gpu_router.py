@@ -92,6 +92,35 @@ def test_many_tokens(ctx):
     assert near <= 1
 
 
+@pytest.mark.parametrize("E,K,S", [(1024, 8, 1), (1025, 32, 1), (1500, 8, 3), (4096, 32, 1), (4096, 8, 20), (2048, 16, 17)])
+def test_expert_counts_up_to_the_limit(ctx, E, K, S):
+    """E up to COLI_MAX_EXPERTS: more than 32 experts per selecting lane above E = 1024 (the decode
+    router for S < 16, the batched router's selection kernel for S >= 16)."""
+    assert E <= B.COLI_MAX_EXPERTS and K <= B.COLI_MAX_K
+    x, Wr, bias = synth.router_inputs(synth.stream_seed(synth.BASE_SEED, "router-large-e", E * 100 + K), S, 256, E)
+    idx, w, n = run_router(ctx, x, Wr, bias, K, 0.9 if S > 1 else 0.0, True, 2.5)
+    near, _ = check_router(idx, w, n, x, Wr, bias, K, 0.9 if S > 1 else 0.0, True, 2.5)
+    assert near <= 1
+    assert (idx[:, 0] >= 1024).any() or E == 1024 or S == 1  # experts past the first 1024 do get chosen
+
+
+def test_high_index_expert_wins(ctx):
+    """The top expert is the last one of E = 4096: only a selection that sees every lane's 128
+    experts finds it first."""
+    E, D, K = 4096, 64, 4
+    x = np.zeros((1, D), np.float32)
+    x[0, 0] = 1.0
+    Wr = np.zeros((E, D), np.float32)
+    Wr[E - 1, 0] = 3.0
+    Wr[E - 2, 0] = 2.0
+    Wr[1500, 0] = 1.0
+    Wr[7, 0] = 0.5
+    idx, w, n = run_router(ctx, x, Wr, None, K, 0.0, False, 1.0)
+    assert idx[0].tolist() == [E - 1, E - 2, 1500, 7]
+    near, _ = check_router(idx, w, n, x, Wr, None, K, 0.0, False, 1.0)
+    assert near == 0
+
+
 def test_nonfinite_activation_reported(ctx):
     x, Wr, bias = synth.router_inputs(12, 1, 128, 16)
     x[0, 5] = np.nan
