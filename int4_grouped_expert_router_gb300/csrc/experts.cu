@@ -1022,17 +1022,22 @@ __global__ void __launch_bounds__(MAXT, 1) down_reduce_kernel(GroupParams P, int
       b++;
     }
     if (rsk >= 0) sm.rscale[rsk][rsr] = rsv;
+    // blocks with fewer threads than K nseg scale cells or nseg rows (K ceil(I/1024) 32 < 64) take the rest in strides
+    for (int i = tid + NC; i < P.K * nseg; i += NC) {
+      const int kk = i / nseg, r = i - kk * nseg;
+      sm.rscale[kk][r] = (kk < m && sm.ok[kk] && sm.st[kk].mode == SCALE_ROW) ? __ldg(sm.st[kk].s + s0 + r) : 1.f;
+    }
     const bool any_stop = named_sync_or(1, NC, stop);
-    if (!any_stop && tid < nseg) {
-      const int d = s0 + tid;
+    for (int r = tid; !any_stop && r < nseg; r += NC) {
+      const int d = s0 + r;
       float acc = 0.f;
       for (int kk = 0; kk < m; kk++) {
         if (!sm.ok[kk]) continue;
         float yk = 0.f;
-        for (int wi = kk * wpe; wi < (kk + 1) * wpe; wi++) yk += sm.part[wi][tid];
-        acc = fmaf(sm.wk[kk], yk * sm.rscale[kk][tid], acc);
+        for (int wi = kk * wpe; wi < (kk + 1) * wpe; wi++) yk += sm.part[wi][r];
+        acc = fmaf(sm.wk[kk], yk * sm.rscale[kk][r], acc);
       }
-      if (P.resid) acc = res + acc;
+      if (P.resid) acc = (r == tid ? res : load_act(P.resid, P.x_dtype, d)) + acc;
       if (P.y_dtype == COLI_DTYPE_F32)
         static_cast<float*>(P.y)[d] = acc;
       else

@@ -1,0 +1,58 @@
+"""The grouped expert FFN at the header's size limits, against the oracle.
+
+- D = COLI_MAX_GROUP_DIM (8192): eight warps per gate/up CTA, one CTA per SM.
+- D = 7000 (ragged, 219 column chunks) with 64-column groups and a 24-column tail group.
+- I = 32768 (COLI_MAX_DIM): 1024 threads per down row, the route-parallel down kernel.
+- S = COLI_MAX_GROUP_TOKENS (1024) tokens on the GEMV path.
+- K = E = 32 (COLI_MAX_K): every expert chosen by every token.
+- Down kernels whose block (K ceil(I/1024) 32 threads) is smaller than a 64-row segment or its row-scale cells.
+"""
+import pytest
+
+from int4_grouped_expert_router_gb300 import binding as B
+from int4_grouped_expert_router_gb300.workload import DeviceLayer, LayerConfig, router_host_inputs
+from gpu_util import BF16_RTOL, F32_RTOL, Ctx, assert_close, bf16_atol, check_router, f32_atol, ffn_reference, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ctx():
+    c = Ctx()
+    yield c.ctx
+    c.close()
+
+
+LIMITS = [
+    LayerConfig("D8192-f32", D=8192, I=128, E=8, K=4),
+    LayerConfig("D8192-S2-bf16", D=8192, I=128, E=8, K=4, S=2, x_dtype="bf16"),
+    LayerConfig("D7000-g64-tail", D=7000, I=200, E=8, K=3, gs=64),
+    LayerConfig("I32768", D=64, I=32768, E=4, K=2),
+    LayerConfig("S1024", D=128, I=64, E=16, K=8, S=1024, topp=0.9),
+    LayerConfig("K32-E32", D=128, I=64, E=32, K=32, S=2, gs="mixed:32"),
+    # one slot of 32 threads per down row range of 40 rows, and 4 slots of 32 threads for 54 rows: the down
+    # kernel's block is smaller than a segment's rows (and its row-scale cells)
+    LayerConfig("K1-D6144-I128", D=6144, I=128, E=4, K=1),
+    LayerConfig("K4-D6144-I1024", D=6144, I=1024, E=8, K=4, gs="mixed:64"),
+]
+
+
+@pytest.mark.parametrize("cfg", LIMITS, ids=lambda c: c.name)
+def test_limits_match_oracle(ctx, cfg):
+    assert cfg.D <= 8192 and cfg.I <= 32768 and cfg.S <= 1024 and cfg.K <= B.COLI_MAX_K
+    layer = DeviceLayer(ctx, cfg)
+    try:
+        x, Wr, bias, resid = router_host_inputs(cfg)
+        out = layer.outputs()
+        xt, rt = layer.act_tensor(x), layer.act_tensor(resid)
+        layer.step(xt, rt, out)
+        assert B.coli_check_error(ctx) == 0, B.coli_last_error(ctx)
+        idx, w, n, y = (to_np(out[k]) for k in ("idx", "w", "n_sel", "y"))
+        xw, rw = to_np(xt), to_np(rt)
+        near, _ = check_router(idx, w, n, xw, Wr, bias, cfg.K, cfg.topp, cfg.norm_topk, cfg.routed_scale)
+        assert near <= 1
+        ref = ffn_reference(cfg, xw, idx, w, n, rw)
+        rtol, atol = (BF16_RTOL, bf16_atol(ref)) if cfg.x_dtype == "bf16" else (F32_RTOL, f32_atol(ref))
+        print(cfg.name, assert_close(y, ref, rtol, atol, cfg.name))
+    finally:
+        layer.free()
