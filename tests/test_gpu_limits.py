@@ -6,6 +6,7 @@
 - S = COLI_MAX_GROUP_TOKENS (1024) tokens on the GEMV path.
 - K = E = 32 (COLI_MAX_K): every expert chosen by every token.
 - Down kernels whose block (K ceil(I/1024) 32 threads) is smaller than a 64-row segment or its row-scale cells.
+- bf16 rows that are not 16-byte aligned, and the tensor-core path at D = 8192 (checked with its tolerance).
 """
 import pytest
 
@@ -34,6 +35,11 @@ LIMITS = [
     # kernel's block is smaller than a segment's rows (and its row-scale cells)
     LayerConfig("K1-D6144-I128", D=6144, I=128, E=4, K=1),
     LayerConfig("K4-D6144-I1024", D=6144, I=1024, E=8, K=4, gs="mixed:64"),
+    # bf16 rows of 200 columns (400 bytes: not 16-byte aligned after row 0), one and several tokens
+    LayerConfig("bf16-D200-S1", D=200, I=136, E=12, K=3, x_dtype="bf16"),
+    LayerConfig("bf16-D200-S3", D=200, I=136, E=12, K=3, S=3, x_dtype="bf16"),
+    # the tensor-core path at D = 8192: 128 K tiles of gate/up, 64 row tiles of down
+    LayerConfig("tc-D8192", D=8192, I=256, E=8, K=4, S=64, gs=64, x_dtype="bf16", zipf=True),
 ]
 
 
@@ -52,7 +58,13 @@ def test_limits_match_oracle(ctx, cfg):
         near, _ = check_router(idx, w, n, xw, Wr, bias, cfg.K, cfg.topp, cfg.norm_topk, cfg.routed_scale)
         assert near <= 1
         ref = ffn_reference(cfg, xw, idx, w, n, rw)
-        rtol, atol = (BF16_RTOL, bf16_atol(ref)) if cfg.x_dtype == "bf16" else (F32_RTOL, f32_atol(ref))
-        print(cfg.name, assert_close(y, ref, rtol, atol, cfg.name))
+        if cfg.name.startswith("tc-"):
+            from test_gpu_prefill import TC_NORM, TC_RTOL, tc_atol
+            stats = assert_close(y, ref, TC_RTOL, tc_atol(ref), cfg.name)
+            assert stats["norm_rel"] < TC_NORM, stats
+        else:
+            rtol, atol = (BF16_RTOL, bf16_atol(ref)) if cfg.x_dtype == "bf16" else (F32_RTOL, f32_atol(ref))
+            stats = assert_close(y, ref, rtol, atol, cfg.name)
+        print(cfg.name, stats)
     finally:
         layer.free()

@@ -121,6 +121,16 @@ def test_high_index_expert_wins(ctx):
     assert near == 0
 
 
+@pytest.mark.parametrize("S", [15, 16, 65536])
+def test_token_counts(ctx, S):
+    """Both sides of the switch to the many-token router (S = 16), and S = COLI_MAX_TOKENS."""
+    x, Wr, bias = synth.router_inputs(synth.stream_seed(synth.BASE_SEED, "router-tokens", S), S, 64, 16)
+    idx, w, n = run_router(ctx, x, Wr, bias, 4, 0.8, True, 2.5)
+    near, _ = check_router(idx, w, n, x, Wr, bias, 4, 0.8, True, 2.5)  # every other token exact
+    print(f"S={S}: near-tie tokens {near}")
+    assert near <= S // 1000 + 1
+
+
 def test_nonfinite_activation_reported(ctx):
     x, Wr, bias = synth.router_inputs(12, 1, 128, 16)
     x[0, 5] = np.nan
