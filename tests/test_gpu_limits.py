@@ -68,3 +68,29 @@ def test_limits_match_oracle(ctx, cfg):
         print(cfg.name, stats)
     finally:
         layer.free()
+
+
+@pytest.mark.parametrize("cfg", [
+    LayerConfig("drop-all-S3", D=256, I=128, E=16, K=4, S=3),
+    LayerConfig("drop-all-tc-S64", D=256, I=128, E=16, K=4, S=64, gs=64, x_dtype="bf16"),
+], ids=lambda c: c.name)
+def test_every_slot_dropped_gives_the_residual(ctx, cfg):
+    """n_sel = 0 for every token: no route is kept, y = resid exactly (GEMV and tensor-core paths)."""
+    import torch
+    layer = DeviceLayer(ctx, cfg)
+    try:
+        x, _, _, resid = router_host_inputs(cfg)
+        xt, rt = layer.act_tensor(x), layer.act_tensor(resid)
+        idx = torch.randint(0, cfg.E, (cfg.S, cfg.K), dtype=torch.int32, device="cuda")
+        w = torch.rand(cfg.S, cfg.K, device="cuda")
+        n = torch.zeros(cfg.S, dtype=torch.int32, device="cuda")
+        y = torch.full_like(xt, 7.0)
+        B.coli_expert_group(ctx, xt, idx, w, n, cfg.K, rt, y)
+        assert B.coli_check_error(ctx) == 0, B.coli_last_error(ctx)
+        assert torch.equal(y, rt)
+        y0 = torch.full_like(xt, 7.0)
+        B.coli_expert_group(ctx, xt, idx, w, n, cfg.K, None, y0)  # no residual: zeros
+        assert B.coli_check_error(ctx) == 0
+        assert not y0.abs().sum().item()
+    finally:
+        layer.free()

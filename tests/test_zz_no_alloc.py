@@ -33,6 +33,8 @@ CASES = [
     (4, 6144, 256, 8, 0.9, True, 2.5, torch.bfloat16),
     (3, 200, 100, 5, 0.7, False, 1.0, torch.float32),
     (256, 512, 256, 8, 0.0, True, 2.5, torch.float32),  # S * E exactly at the limit
+    (1, 256, 4096, 32, 0.0, True, 2.5, torch.float32),   # more than 1024 experts: the large-E selection
+    (16, 128, 4096, 8, 0.9, True, 2.5, torch.float32),   # ... in the many-token router, S * E at the limit
 ]
 
 
