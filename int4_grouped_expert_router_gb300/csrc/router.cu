@@ -34,9 +34,10 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ void select_finish(int mine, float wmine, int K, float topp, int norm_topk, float routed_scale,
-                              int32_t* __restrict__ idx_out, float* __restrict__ w_out, int32_t* __restrict__ nsel_out,
-                              const ExpertDesc* table);
+__device__ __forceinline__ void select_finish(int mine, float wmine, int K, float topp, int norm_topk,
+                                              float routed_scale, int32_t* __restrict__ idx_out,
+                                              float* __restrict__ w_out, int32_t* __restrict__ nsel_out,
+                                              const ExpertDesc* table);
 
 // One warp selects for one token. Lane l owns experts e = l + 32 * i (i < EPL). Each round, every
 // lane finds its best not-yet-chosen expert by a strict '>' scan in increasing e (so its first,
@@ -96,9 +97,10 @@ __device__ void select_token(const float2* __restrict__ sc_row, int E, int K, fl
 
 // Lane k holds the expert of slot k (mine) and its raw score (wmine): weights from the raw
 // (bias-free) score, top-p, norm and scale; every sum in slot order in binary32, no contraction.
-__device__ void select_finish(int mine, float wmine, int K, float topp, int norm_topk, float routed_scale,
-                              int32_t* __restrict__ idx_out, float* __restrict__ w_out, int32_t* __restrict__ nsel_out,
-                              const ExpertDesc* table) {
+__device__ __forceinline__ void select_finish(int mine, float wmine, int K, float topp, int norm_topk,
+                                              float routed_scale, int32_t* __restrict__ idx_out,
+                                              float* __restrict__ w_out, int32_t* __restrict__ nsel_out,
+                                              const ExpertDesc* table) {
   const int lane = threadIdx.x & 31;
   int m = K;
   float denom = 1.f;
@@ -283,8 +285,7 @@ __device__ __forceinline__ void router_body(const void* __restrict__ x, int x_dt
     case 4: select_all<4>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
     case 8: select_all<8>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
     case 16: select_all<16>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
-    case 32: select_all<32>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
-    default: select_all<0>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
+    default: select_all<32>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
   }
   __syncthreads();
   if (tid == 0) atomicExch(arrivals, 0u);
@@ -317,6 +318,9 @@ __global__ void __launch_bounds__(kRouterThreads) router_fixed_kernel(
 // ------------------------------------------------------------------------------------------
 
 constexpr int kBatchedS = 16;
+// The decode router's last-CTA selection holds at most 32 experts per lane (E <= 1024); larger E
+// takes the many-token path, whose separate selection kernel also has the large-E form.
+constexpr int kDecodeMaxE = 1024;
 constexpr int kRT = 64;     // tokens and experts per tile
 constexpr int kRBK = 32;    // columns of D per step
 constexpr int kRSplit = 8;  // column ranges of D
@@ -437,7 +441,7 @@ static int launch_router_batched(coli_ctx* ctx, const void* x, int x_dtype, int 
 int launch_router(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr, const float* bias,
                   int E, int K, float topp, int norm_topk, float routed_scale, int32_t* idx, float* w,
                   int32_t* n_sel) {
-  if (S >= kBatchedS) {
+  if (S >= kBatchedS || E > kDecodeMaxE) {
     const size_t sc_bytes = align_up((size_t)S * E * sizeof(float2), 256);
     int rc = ensure_workspace(ctx, sc_bytes + (size_t)kRSplit * S * E * sizeof(float));
     if (rc != COLI_OK) return rc;
@@ -524,7 +528,7 @@ int launch_router_noalloc(coli_ctx* ctx, const void* x, int x_dtype, int S, int 
   }
   unsigned* arrivals = reinterpret_cast<unsigned*>(base);
   float2* sc_ws = reinterpret_cast<float2*>(base + kFixedPairsOff);
-  if (S >= kBatchedS)  // the many-token path, as coli_router_select takes it (no arrival counter)
+  if (S >= kBatchedS || E > kDecodeMaxE)  // the many-token path, as coli_router_select takes it (no arrival counter)
     return launch_router_batched(ctx, x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk, routed_scale, idx, w, n_sel,
                                  sc_ws, reinterpret_cast<float*>(base + kFixedPartOff));
   cudaError_t e = cudaMemsetAsync(arrivals, 0, sizeof(unsigned), ctx->stream);
