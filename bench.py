@@ -438,29 +438,28 @@ def gpu_arm(args, rank, world, local):
     traffic = load_traffic(top_kernel, source_hash())
 
     # ---- end to end through the C ABI with host buffers: H2D inputs, D2H result per step ----
-    hx = [torch.empty_like(xs[s], device="cpu").pin_memory() for s in range(n_tok)]
-    hr = [torch.empty_like(rs[s], device="cpu").pin_memory() for s in range(n_tok)]
+    # each step's x and resid sit side by side in one pinned host buffer and travel in one copy
+    hxr = [torch.empty((2,) + tuple(xs[s].shape), dtype=xs[s].dtype, device="cpu").pin_memory() for s in range(n_tok)]
     hy = [torch.empty_like(outs[s]["y"], device="cpu").pin_memory() for s in range(n_tok)]
     for s in range(n_tok):
-        hx[s].copy_(xs[s])
-        hr[s].copy_(rs[s])
-    dx = [torch.empty_like(xs[s]) for s in range(n_tok)]
-    dr = [torch.empty_like(rs[s]) for s in range(n_tok)]
+        hxr[s][0].copy_(xs[s])
+        hxr[s][1].copy_(rs[s])
+    dxr = [torch.empty((2,) + tuple(xs[s].shape), dtype=xs[s].dtype, device="cuda") for s in range(n_tok)]
+
+    def e2e_step(s):
+        dxr[s].copy_(hxr[s], non_blocking=True)
+        layer.step(dxr[s][0], dxr[s][1], outs[s])
+        hy[s].copy_(outs[s]["y"], non_blocking=True)
+
     for s in range(args.warmup):
         flush.zero_()
-        dx[s].copy_(hx[s], non_blocking=True)
-        dr[s].copy_(hr[s], non_blocking=True)
-        layer.step(dx[s], dr[s], outs[s])
-        hy[s].copy_(outs[s]["y"], non_blocking=True)
+        e2e_step(s)
     barrier()
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_tok)]
     for s in range(args.warmup, n_tok):
         flush.zero_()
         e2e_ev[s][0].record(stream)
-        dx[s].copy_(hx[s], non_blocking=True)
-        dr[s].copy_(hr[s], non_blocking=True)
-        layer.step(dx[s], dr[s], outs[s])
-        hy[s].copy_(outs[s]["y"], non_blocking=True)
+        e2e_step(s)
         e2e_ev[s][1].record(stream)
     barrier()
     e2e_ms = max_over_ranks(sum(e2e_ev[s][0].elapsed_time(e2e_ev[s][1]) for s in range(args.warmup, n_tok)), dist, "cuda")

@@ -13,8 +13,12 @@
 // scale, n the stored nibble); activations and SiLU(g) * u as bf16; products are accumulated in
 // f32 in tensor memory; the combine sums the slots in slot order in f32.
 //
-// GEMM orientation. The weight rows are the MMA's M side (tiles of 128 rows) and an expert's
-// tokens are its N side (16..128 columns), so the accumulator is D^T = W X^T in tensor memory.
+// GEMM orientation. An expert's tokens are the MMA's M side (128 rows; rows past the entry's tokens
+// are ignored) and a 256-row block of weights is its N side: the gate and the up tile of the same
+// 128 rows, or two consecutive 128-row tiles of the down matrix. The accumulator D = X W^T sits in
+// tensor memory with a token per lane and a weight row per column. Four MMAs of K = 16 cover a
+// 64-column K tile whatever the number of tokens (the single issuing thread spends a roughly fixed
+// time per MMA instruction, so fewer, wider instructions are what sets the K-tile rate).
 // Both operands are K-major bf16 tiles of 64 columns in the 128-byte-swizzled layout: the
 // activations are staged by TMA; the weights are staged packed by TMA and dequantised into that
 // layout by converter warps. Within every 8-column group the dequantiser emits the columns in the
@@ -42,9 +46,6 @@ constexpr int kPfThreads = (3 + kPfConvWarps) * 32;  // + the two producer warps
 constexpr uint32_t kPfTileBytes = kTcRows * 128;       // one bf16 operand tile: 128 rows x 128 bytes
 constexpr uint32_t kPfPackedBytes = kTcRows * kTcWords * 4;  // one packed int4 weight tile (4 K tiles)
 constexpr int kPfSuper = kTcWords * 8 / kPfKTile;            // K tiles per packed tile
-
-// position of column c (0..7) of an 8-column group in the tensor-core K order
-__host__ __device__ constexpr int pf_perm8(int c) { return c < 4 ? 2 * c : 2 * (c - 4) + 1; }
 
 struct PfEntry {
   int e;     // expert
@@ -236,21 +237,24 @@ __device__ __forceinline__ uint4 pf_dequant8(uint32_t w, uint32_t s2) {
 //   packed ring (kPkStages): packed int4 tiles, staged by TMA far ahead of their use;
 //   act ring (kActStages): 128-byte-swizzled bf16 activation tiles, staged by TMA;
 //   operand ring (kOpStages): bf16 weight tiles written by the converter warps.
+// A converter warp releases a packed stage only after the words it loaded from it are consumed (its
+// dequantised stores done): released right after the shared-memory loads were issued, the copy engine
+// could refill the stage before every load had read it, under the tensor core's operand traffic.
 // warp 0 stages packed tiles; warp 1 owns tensor memory, its lane 0 issues the MMAs; warp 2 stages
 // activation tiles (each producer has a warp of its own, so neither waits while the other sleeps
 // in a barrier wait); warps 3.. convert; warps 4..7 also read the accumulators (warp w reads
-// tensor-memory lanes 32 (w % 4) ..). Work units are (entry, 128-row weight tile), strided over
+// tensor-memory lanes 32 (w % 4) ..: tokens). Work units are (entry, 256-row weight block), strided over
 // the persistent grid; every role walks the same units and K tiles.
 // ------------------------------------------------------------------------------------------
 
 #ifndef COLI_PF_PK_STAGES
-#define COLI_PF_PK_STAGES 3
+#define COLI_PF_PK_STAGES 2
 #endif
 #ifndef COLI_PF_ACT_STAGES
 #define COLI_PF_ACT_STAGES 3
 #endif
 #ifndef COLI_PF_OP_STAGES
-#define COLI_PF_OP_STAGES 2
+#define COLI_PF_OP_STAGES 3
 #endif
 constexpr int kPkStages = COLI_PF_PK_STAGES;
 constexpr int kActStages = COLI_PF_ACT_STAGES;
@@ -260,7 +264,7 @@ struct PfGemmParams {
   const ExpertDesc* table;
   const PfEntry* entries;
   const int* n_entries;
-  int tiles;   // weight row tiles per entry: ceil(rows / 128)
+  int tiles;   // 256-row weight blocks per entry: ceil(rows / 128) (DUAL) or ceil(rows / 256)
   int rows;    // weight rows (I for gate/up, D for down)
   int K;       // reduction length (D for gate/up, I for down)
   int t0, t1;  // tensor indices in the expert descriptor (t1 < 0: single)
@@ -270,7 +274,7 @@ struct PfGemmParams {
 
 template <bool DUAL>
 struct PfLayout {
-  static constexpr int kT = DUAL ? 2 : 1;
+  static constexpr int kT = 2;  // 128-row weight tiles per block (the two halves of the MMA's N)
   static constexpr uint32_t kOpStage = kT * kPfTileBytes;            // bf16 weight tiles
   static constexpr uint32_t kActStage = kPfRows * 128;               // <= kPfRows rows x 128 bytes
   static constexpr uint32_t kPkStage = kT * kPfPackedBytes;          // packed tiles
@@ -377,11 +381,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(PfGemmParams P, 
         if (!pf_wait(c, &emptyb[rp.s], rp.ph ^ 1u, P.err)) break;
         if (packed) {
           uint8_t* st = sm + Lay::kPk + (size_t)rp.s * Lay::kPkStage;
+          // the second tile of a down block may lie wholly past the last row: TMA fills it with
+          // zeros and still delivers its bytes
           mbar_arrive_expect_tx(&fullb[rp.s], Lay::kPkStage);
-          tma_load_2d_hint(st, &ed.t[P.t0].map_tc, (kt / kPfSuper) * kTcWords, t * kTcRows, &fullb[rp.s], policy);
-          if (DUAL)
-            tma_load_2d_hint(st + kPfPackedBytes, &ed.t[P.t1].map_tc, (kt / kPfSuper) * kTcWords, t * kTcRows,
-                             &fullb[rp.s], policy);
+          const int kx = (kt / kPfSuper) * kTcWords;
+          tma_load_2d_hint(st, &ed.t[P.t0].map_tc, kx, (DUAL ? t : 2 * t) * kTcRows, &fullb[rp.s], policy);
+          tma_load_2d_hint(st + kPfPackedBytes, &ed.t[DUAL ? P.t1 : P.t0].map_tc, kx, (DUAL ? t : 2 * t + 1) * kTcRows,
+                           &fullb[rp.s], policy);
         } else {
           uint8_t* st = sm + Lay::kAct + (size_t)rp.s * Lay::kActStage;
           mbar_arrive_expect_tx(&fullb[rp.s], (uint32_t)en.npad * 128u);
@@ -403,8 +409,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(PfGemmParams P, 
       RingPos ra, ro;
       int lu = 0;
       for (int u = blockIdx.x; u < n_units && !ld_volatile_int(&c.stop); u += gridDim.x, lu++) {
-        const PfEntry en = P.entries[u / P.tiles];
-        const uint32_t idesc = bf16_f32_idesc(128, (uint32_t)en.npad);
+        const uint32_t idesc = bf16_f32_idesc(kPfRows, Lay::kT * kTcRows);  // M = tokens, N = weight rows
         if (!pf_wait(c, &c.acc_empty, ((uint32_t)lu & 1u) ^ 1u, P.err)) break;
         tc_fence_after_sync();
         bool ok = true;
@@ -414,15 +419,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(PfGemmParams P, 
             break;
           }
           tc_fence_after_sync();
-          const uint64_t bdesc = sw128_kmajor_desc(sm + Lay::kAct + (size_t)ra.s * Lay::kActStage);
+          const uint64_t adesc = sw128_kmajor_desc(sm + Lay::kAct + (size_t)ra.s * Lay::kActStage);
+          const uint64_t bdesc = sw128_kmajor_desc(sm + Lay::kOp + (size_t)ro.s * Lay::kOpStage);  // both tiles
 #pragma unroll
-          for (int x = 0; x < Lay::kT; x++) {
-            const uint64_t adesc = sw128_kmajor_desc(sm + Lay::kOp + (size_t)ro.s * Lay::kOpStage + x * kPfTileBytes);
-            const uint32_t dcol = tmem + (uint32_t)(x * kPfRows);
-#pragma unroll
-            for (int ks = 0; ks < kPfKTile / 16; ks++)
-              tc_mma_bf16(dcol, adesc + 2 * ks, bdesc + 2 * ks, idesc, kt > 0 || ks > 0);
-          }
+          for (int ks = 0; ks < kPfKTile / 16; ks++)
+            tc_mma_bf16(tmem, adesc + 2 * ks, bdesc + 2 * ks, idesc, kt > 0 || ks > 0);
           tc_commit(&c.act_empty[ra.s]);
           tc_commit(&c.op_empty[ro.s]);
           ra.next(kActStages);
@@ -443,7 +444,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(PfGemmParams P, 
     constexpr int kW = 8 / kParts;  // words of a 64-column K tile (8 words per row) per thread
     static_assert(kParts * kW == 8 && kW >= 2, "converter split");
     const int r = ct & (kTcRows - 1);
-    const int x = DUAL ? ct / (kTcRows * kParts) : 0;
+    const int x = ct / (kTcRows * kParts);   // weight tile of the block
     const int w0 = ((ct / kTcRows) % kParts) * kW;
     const bool epi = warp >= 4 && warp < 8;
     const int q = warp & 3;                  // tensor-memory lane quarter of an epilogue warp
@@ -453,8 +454,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(PfGemmParams P, 
     for (int u = blockIdx.x; u < n_units && !ld_volatile_int(&c.stop); u += gridDim.x, lu++) {
       const PfEntry en = P.entries[u / P.tiles];
       const int t = u % P.tiles;
-      const TensorDesc& td = P.table[en.e].t[x == 0 ? P.t0 : P.t1];
-      const int gs = td.gs, row = t * kTcRows + r;
+      const TensorDesc& td = P.table[en.e].t[(DUAL && x == 1) ? P.t1 : P.t0];
+      const int gs = td.gs, row = (DUAL ? t : 2 * t + x) * kTcRows + r;
       const bool row_ok = row < P.rows;
       const float* srow = row_ok ? td.s + (gs == 0 ? (size_t)row : (size_t)row * td.G) : nullptr;
       // this thread's 32-column half of every K tile: columns c0 + 8 w0 .. + 8 kW - 1 (gs is 0 or a
@@ -477,7 +478,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(PfGemmParams P, 
         s_next0 = s_next1;
         s_next1 = kt + 2 < nkt ? scale_of((kt + 2) * kPfKTile + hoff) : 0.f;
         const int sub = kt % kPfSuper;  // K tile within the packed tile
-        if ((sub == 0 && !pf_wait(c, &c.pk_full[rp.s], rp.ph, P.err)) || !pf_wait(c, &c.op_empty[ro.s], ro.ph ^ 1u, P.err)) {
+        if ((sub == 0 && !pf_wait(c, &c.pk_full[rp.s], rp.ph, P.err)) ||
+            !pf_wait(c, &c.op_empty[ro.s], ro.ph ^ 1u, P.err)) {
           ok = false;
           break;
         }
@@ -506,8 +508,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(PfGemmParams P, 
           wv[kW - 1] = v.y;
         }
         const bool last_sub = sub == kPfSuper - 1 || kt + 1 == nkt;
-        __syncwarp();
-        if (last_sub && lane == 0) mbar_arrive(&c.pk_empty[rp.s]);  // the packed tile's words are all read
         const int c0 = kt * kPfKTile + hoff;
         if (row_ok && c0 + 8 * kW <= P.K) {  // whole half inside the matrix
 #pragma unroll
@@ -523,39 +523,54 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(PfGemmParams P, 
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&c.op_full[ro.s]);
+        if (lane == 0) {
+          if (last_sub) mbar_arrive(&c.pk_empty[rp.s]);  // the packed words are consumed
+          mbar_arrive(&c.op_full[ro.s]);
+        }
         if (last_sub) rp.next(kPkStages);
         ro.next(kOpStages);
       }
       if (!ok) break;
       if (epi) {
-        // ---------------- epilogue of this unit ----------------
+        // ---------------- epilogue of this unit: lane = token, column = weight row ----------------
         if (!pf_wait(c, &c.acc_full, (uint32_t)lu & 1u, P.err)) break;
         tc_fence_after_sync();
-        const int orow = t * kTcRows + q * 32 + lane;  // weight row this lane holds
+        const int m = q * 32 + lane;  // token of the entry this lane holds
+        const bool tok = m < en.n;
         const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
-        for (int n0 = 0; n0 < en.npad; n0 += 16) {
-          float a[16];
-          tmem_ld16(tl + (uint32_t)n0, a);
-          if (DUAL) {
-            float b[16];
-            tmem_ld16(tl + (uint32_t)kPfRows + (uint32_t)n0, b);
-            if (orow < P.rows) {
-              uint16_t* h = static_cast<uint16_t*>(P.out);
-              const int pcol = (orow & ~7) + pf_perm8(orow & 7);
+        if (DUAL) {
+          // h = SiLU(g) u for weight rows i of the tile, stored in the tensor-core column order:
+          // within each group of 8, word p holds columns p and p + 4
+          uint16_t* hrow = static_cast<uint16_t*>(P.out) + (size_t)(en.row0 + m) * P.rows;
+          for (int j0 = 0; j0 < kTcRows; j0 += 16) {
+            float g[16], uu[16];
+            tmem_ld16(tl + (uint32_t)j0, g);
+            tmem_ld16(tl + (uint32_t)(kTcRows + j0), uu);
 #pragma unroll
-              for (int j = 0; j < 16; j++) {
-                const int n = n0 + j;
-                float v = 0.f;
-                if (n < en.n) v = a[j] / (1.f + expf(-a[j])) * b[j];
-                h[(size_t)(en.row0 + n) * P.rows + pcol] = f32_to_bf16_rn(v);
+            for (int half = 0; half < 2; half++) {
+              const int i8 = t * kTcRows + j0 + 8 * half;
+              if (!tok || i8 >= P.rows) continue;
+              uint32_t wv[4];
+#pragma unroll
+              for (int p = 0; p < 4; p++) {
+                const float a0 = g[8 * half + p], a1 = g[8 * half + p + 4];
+                const float v0 = a0 / (1.f + expf(-a0)) * uu[8 * half + p];
+                const float v1 = a1 / (1.f + expf(-a1)) * uu[8 * half + p + 4];
+                wv[p] = (uint32_t)f32_to_bf16_rn(v0) | ((uint32_t)f32_to_bf16_rn(v1) << 16);
               }
+              *reinterpret_cast<uint4*>(hrow + i8) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
             }
-          } else if (orow < P.rows) {
-            float* yr = static_cast<float*>(P.out);
+          }
+        } else {
+          float* yrow = static_cast<float*>(P.out) + (size_t)(en.row0 + m) * P.rows;
+          for (int j0 = 0; j0 < Lay::kT * kTcRows; j0 += 16) {
+            float a[16];
+            tmem_ld16(tl + (uint32_t)j0, a);
+            const int d0 = 2 * t * kTcRows + j0;
 #pragma unroll
-            for (int j = 0; j < 16; j++)
-              if (n0 + j < en.n) yr[(size_t)(en.row0 + n0 + j) * P.rows + orow] = a[j];
+            for (int v = 0; v < 4; v++)
+              if (tok && d0 + 4 * v < P.rows)
+                *reinterpret_cast<float4*>(yrow + d0 + 4 * v) = make_float4(a[4 * v], a[4 * v + 1], a[4 * v + 2], a[4 * v + 3]);
           }
         }
         tc_fence_before_sync();
@@ -696,7 +711,7 @@ int launch_prefill(coli_ctx* ctx, const void* x, int S, const int32_t* idx, cons
     if ((e = cudaFuncSetAttribute(pf_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
         cudaSuccess)
       return cuda_fail(ctx, e, "prefill down smem attribute");
-    G.tiles = (D + kTcRows - 1) / kTcRows;
+    G.tiles = (D + 2 * kTcRows - 1) / (2 * kTcRows);
     G.rows = D;
     G.K = I;
     G.t0 = T_DOWN;
