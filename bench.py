@@ -67,7 +67,7 @@ def bf16_peak():
 
 
 def prefill_leg(ctx, stream, flush, steps=10, warmup=3):
-    """Config-5 prefill layer (S=512, g64 int4, bf16, Zipf routing) on the tensor-core path:
+    """The prefill layer (S=512, g64 int4, bf16, Zipf routing) on the tensor-core path:
     graph-replayed steps with a cold L2, TFLOP/s and HBM bytes of the touched experts."""
     import numpy as np
     import torch
