@@ -9,6 +9,9 @@
  *   [fixes]  c/backend_cuda.cu commit history, commit "Three vendor-neutral fixes to backend_cuda.cu"
  *   [pipe]   c/backend_cuda.cu commit history, commit "GPU resident pipeline ..."
  *   [resid]  PR #434 "COLI_CUDA_RESID=1", section "What"
+ *   [attn]   c/backend_cuda.cu commit history, commit "CUDA batch MLA attention, kv_b head-sharding,
+ *            fused o_proj, expert-group dispatch, W4A16 kernels"
+ *   [q651]   PR #651, comment "Follow-up decode experiments" (Nsight kernel shares)
  *
  * Conventions shared by every call:
  *  - Return value: COLI_OK (0) or a negative COLI_E_* code. A failed call leaves no CUDA error
@@ -94,12 +97,13 @@ COLI_API int coli_reserve(coli_ctx *ctx, int max_S, int max_E, int max_K, int ma
 
 /* Per-kernel timing: when on, every kernel launch of this context is bracketed by two CUDA events
  * recorded on the context's stream (off by default). Kinds: COLI_KERNEL_ROUTER, _GATEUP, _DOWN,
- * _COMBINE. coli_profile_read synchronises the stream and returns, for one kind, the summed event
+ * _COMBINE, _LINEAR. coli_profile_read synchronises the stream and returns, for one kind, the summed event
  * time in milliseconds and the number of launches since the previous read of that kind. */
 #define COLI_KERNEL_ROUTER 0
 #define COLI_KERNEL_GATEUP 1
 #define COLI_KERNEL_DOWN 2
 #define COLI_KERNEL_COMBINE 3
+#define COLI_KERNEL_LINEAR 4
 COLI_API int coli_profile_enable(coli_ctx *ctx, int on);
 COLI_API int coli_profile_read(coli_ctx *ctx, int kind, double *total_ms, long long *launches);
 
@@ -161,6 +165,10 @@ COLI_API int coli_router_select_noalloc(coli_ctx *ctx, const void *x, int x_dtyp
 COLI_API uint64_t coli_expert_upload(coli_ctx *ctx, const uint8_t *packed, const float *scales, int O,
                             int I, int gs);
 
+/* Shape of an uploaded tensor: O rows, I columns and its group size gs (any output pointer may be
+ * NULL). COLI_E_INVAL for an unknown handle. */
+COLI_API int coli_tensor_shape(coli_ctx *ctx, uint64_t handle, int *O, int *I, int *gs);
+
 /* Free an uploaded tensor. It must not be referenced by the expert table (COLI_E_INVAL). */
 COLI_API int coli_expert_free(coli_ctx *ctx, uint64_t handle);
 
@@ -215,6 +223,26 @@ COLI_API int coli_expert_group(coli_ctx *ctx, const void *x_rows, int x_dtype, i
 COLI_API int coli_expert_group_issue(coli_ctx *ctx, const void *x_rows, int x_dtype, int S,
                             const int32_t *idx, const float *w, const int32_t *n_sel, int K);
 COLI_API int coli_expert_group_take(coli_ctx *ctx, const void *resid, void *y);
+
+/*
+ * Dense int4 projection: the one-tensor int4 matmul that [tcgate] names quant_matmul and that
+ * [q651] measures as the largest kernel share of a decode step. For S tokens,
+ *   y[t, o] = resid[t, o] + sum_i W[o, i] x[t, i]
+ * with W an uploaded tensor [O x I] (coli_expert_upload; it may also be in the expert table) and
+ * the same int4 x activation dot product as coli_expert_group (f32 results; bf16 activations are
+ * widened exactly and y is rounded to bf16 once). x [S x I], resid [S x O] or NULL, y [S x O]:
+ * row-major in x_dtype, device pointers. y may be resid (in place) but must not overlap x.
+ * 1 <= S <= COLI_MAX_TOKENS. Every weight byte is read from HBM once per call for the first token;
+ * the other tokens' passes over W mostly hit L2. COLI_E_INVAL for a bad handle, pointer, dtype or
+ * S. Profiled as COLI_KERNEL_LINEAR.
+ *
+ * A shared expert ([attn] runs it on the device, [pipe] keeps it beside the residual adds) is an
+ * always-chosen expert with weight 1. With the same shape as the routed experts it is one more
+ * table entry outside the router's E ids, issued as its own group (idx = its id for every token,
+ * w = 1, K = 1, n_sel NULL) with coli_expert_group_issue next to the routed group, before the take.
+ */
+COLI_API int coli_w4_linear(coli_ctx *ctx, uint64_t W, const void *x, int x_dtype, int S, const void *resid,
+                            void *y);
 
 #ifdef __cplusplus
 }

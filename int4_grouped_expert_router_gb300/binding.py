@@ -60,6 +60,9 @@ SIGNATURES = {
     "coli_router_select_noalloc": (_I, [_P, _P, _I, _I, _I, _P, _P, _I, _I, _F, _I, _F, _P, _P, _P]),
     "coli_expert_upload": (_U64, [_P, _P, _P, _I, _I, _I]),
     "coli_expert_free": (_I, [_P, _U64]),
+    "coli_tensor_shape": (_I, [_P, _U64, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
+                              ctypes.POINTER(ctypes.c_int)]),
+    "coli_w4_linear": (_I, [_P, _U64, _P, _I, _I, _P, _P]),
     "coli_expert_table_set": (_I, [_P, _I, _U64, _U64, _U64]),
     "coli_expert_group": (_I, [_P, _P, _I, _I, _P, _P, _P, _I, _P, _P]),
     "coli_expert_group_issue": (_I, [_P, _P, _I, _I, _P, _P, _P, _I]),
@@ -72,6 +75,7 @@ COLI_KERNEL_ROUTER = _C["COLI_KERNEL_ROUTER"]
 COLI_KERNEL_GATEUP = _C["COLI_KERNEL_GATEUP"]
 COLI_KERNEL_DOWN = _C["COLI_KERNEL_DOWN"]
 COLI_KERNEL_COMBINE = _C["COLI_KERNEL_COMBINE"]
+COLI_KERNEL_LINEAR = _C["COLI_KERNEL_LINEAR"]
 
 
 class ColiError(RuntimeError):
@@ -215,6 +219,27 @@ def coli_expert_upload(ctx, packed, scales, O, I, gs):
 
 def coli_expert_free(ctx, handle):
     return _check(ctx, library().coli_expert_free(ctx, handle), "coli_expert_free")
+
+
+def coli_tensor_shape(ctx, handle):
+    """(O, I, gs) of an uploaded tensor."""
+    O, I, gs = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(ctx, library().coli_tensor_shape(ctx, handle, ctypes.byref(O), ctypes.byref(I), ctypes.byref(gs)),
+           "coli_tensor_shape")
+    return O.value, I.value, gs.value
+
+
+def coli_w4_linear(ctx, W, x, resid, y):
+    """y = resid + W x for every row of x ([S x I] -> [S x O]); resid may be None."""
+    O, I, _ = coli_tensor_shape(ctx, W)
+    _dev(x, name="x")
+    _dev(resid, x.dtype, "resid")
+    _dev(y, x.dtype, "y")
+    S = x.shape[0]
+    if x.dim() != 2 or x.shape[1] != I or tuple(y.shape) != (S, O) or (resid is not None and resid.shape != y.shape):
+        raise ValueError("w4_linear: x must be [S x I] and y, resid [S x O] for the tensor's O and I")
+    rc = library().coli_w4_linear(ctx, W, _ptr(x), act_dtype(x), S, _ptr(resid), _ptr(y))
+    return _check(ctx, rc, "coli_w4_linear")
 
 
 def coli_expert_table_set(ctx, e, gate, up, down):

@@ -297,7 +297,7 @@ int coli_profile_enable(coli_ctx* ctx, int on) {
 }
 
 int coli_profile_read(coli_ctx* ctx, int kind, double* total_ms, long long* launches) {
-  if (!ctx || kind < 0 || kind > 3 || !total_ms || !launches) return COLI_E_INVAL;
+  if (!ctx || kind < 0 || kind > COLI_KERNEL_LINEAR || !total_ms || !launches) return COLI_E_INVAL;
   cudaSetDevice(ctx->device);
   cudaError_t e = cudaStreamSynchronize(ctx->stream);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "coli_profile_read: stream sync");
@@ -395,6 +395,16 @@ uint64_t coli_expert_upload(coli_ctx* ctx, const uint8_t* packed, const float* s
   t.live = true;
   ctx->tensors.push_back(t);
   return (uint64_t)ctx->tensors.size();
+}
+
+int coli_tensor_shape(coli_ctx* ctx, uint64_t handle, int* O, int* I, int* gs) {
+  if (!ctx) return COLI_E_INVAL;
+  if (!valid_handle(ctx, handle)) return fail(ctx, COLI_E_INVAL, "tensor_shape: unknown tensor handle");
+  const HostTensor& t = ctx->tensors[handle - 1];
+  if (O) *O = t.O;
+  if (I) *I = t.I;
+  if (gs) *gs = t.gs;
+  return COLI_OK;
 }
 
 int coli_expert_free(coli_ctx* ctx, uint64_t handle) {
@@ -501,6 +511,19 @@ int coli_expert_group(coli_ctx* ctx, const void* x_rows, int x_dtype, int S, con
   if (injected(ctx)) return COLI_E_INJECTED;
   cudaSetDevice(ctx->device);
   int rc = launch_expert_group(ctx, x_rows, x_dtype, S, idx, w, n_sel, K, resid, y, x_dtype);
+  if (rc == COLI_OK) ctx->compute_calls++;
+  return rc;
+}
+
+int coli_w4_linear(coli_ctx* ctx, uint64_t W, const void* x, int x_dtype, int S, const void* resid, void* y) {
+  if (!ctx) return COLI_E_INVAL;
+  if (!x || !y) return fail(ctx, COLI_E_INVAL, "w4_linear: NULL pointer");
+  if (x_dtype != COLI_DTYPE_F32 && x_dtype != COLI_DTYPE_BF16) return fail(ctx, COLI_E_INVAL, "w4_linear: dtype");
+  if (S < 1 || S > COLI_MAX_TOKENS) return fail(ctx, COLI_E_INVAL, "w4_linear: S out of range");
+  if (!valid_handle(ctx, W)) return fail(ctx, COLI_E_INVAL, "w4_linear: unknown tensor handle");
+  if (injected(ctx)) return COLI_E_INJECTED;
+  cudaSetDevice(ctx->device);
+  int rc = launch_linear(ctx, ctx->tensors[W - 1].desc, x, x_dtype, S, resid, y);
   if (rc == COLI_OK) ctx->compute_calls++;
   return rc;
 }

@@ -119,8 +119,8 @@ struct coli_ctx {
   };
   std::vector<ProfRec> prof_pending;
   std::vector<cudaEvent_t> prof_free;
-  double prof_ms[4] = {0, 0, 0, 0};
-  long long prof_n[4] = {0, 0, 0, 0};
+  double prof_ms[5] = {0, 0, 0, 0, 0};
+  long long prof_n[5] = {0, 0, 0, 0, 0};
 };
 
 namespace coli {
@@ -160,6 +160,8 @@ int launch_router_noalloc(coli_ctx* ctx, const void* x, int x_dtype, int S, int 
 // y is written in y_dtype (x_dtype for coli_expert_group; f32 for an issued partial sum); resid is read in x_dtype.
 int launch_expert_group(coli_ctx* ctx, const void* x, int x_dtype, int S, const int32_t* idx,
                         const float* w, const int32_t* n_sel, int K, const void* resid, void* y, int y_dtype);
+// y [S x O] = resid + W x for S tokens of the uploaded tensor T [O x I] (coli_w4_linear).
+int launch_linear(coli_ctx* ctx, const TensorDesc& T, const void* x, int x_dtype, int S, const void* resid, void* y);
 // y [S x D] (dtype) = resid + the n issued partial sums [S x D] f32, added in issue order.
 int launch_take(coli_ctx* ctx, int S, int D, int n, const void* resid, int dtype, void* y);
 // Which cooperative launch forms this device accepts (coli_ctx::coop_mode), found with an empty

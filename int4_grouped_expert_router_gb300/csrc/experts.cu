@@ -1159,6 +1159,105 @@ __global__ void combine_kernel(GroupParams P) {
 }
 
 // ------------------------------------------------------------------------------------------
+// Dense int4 projection: y[t, o] = resid[t, o] + sum_i W[o, i] x[t, i] for S tokens.
+//
+// The same block-fixed-point dot product as the expert kernels. A thread owns one 16-byte chunk
+// (32 columns) of every row; a CTA takes a contiguous range of (token, 4-row batch) items, the
+// items ordered token-major so a token's limbs are computed once per CTA. Each batch loads its
+// four rows' chunks from HBM (streaming loads, the next batch's issued before the current batch's
+// products), reduces them across the warp and parks the warp totals in shared memory; every
+// kLinSeg batches the CTA adds the warps' totals in warp order and writes the finished rows.
+// ------------------------------------------------------------------------------------------
+
+struct LinearParams {
+  const void* x;      // [S x I], x_dtype
+  const void* resid;  // [S x O], x_dtype, or NULL
+  void* y;            // [S x O], x_dtype
+  int x_dtype;
+  int S, O, I;
+  int* err;
+};
+
+constexpr int kLinSeg = 16;  // batches of kDU rows finished together
+
+template <int MAXT>
+__global__ void __launch_bounds__(MAXT) linear_kernel(LinearParams P, const __grid_constant__ TensorDesc T) {
+  __shared__ float red[MAXT / 32][kLinSeg * kDU];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  const int CI = (P.I + 31) >> 5;
+  const int c = tid;
+  const bool has_chunk = c < CI;
+  const int Bo = (P.O + kDU - 1) / kDU;  // row batches per token
+  const long long NB = (long long)P.S * Bo;
+  const long long q0 = (long long)blockIdx.x * NB / gridDim.x;
+  const long long q1 = (long long)(blockIdx.x + 1) * NB / gridDim.x;
+  const uint4 zero_w = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);  // nibbles 8: value 0
+  auto load_batch = [&](long long q, uint4 (&wv)[kDU]) {
+    const int t = (int)(q / Bo);
+    const int o0 = (int)(q - (long long)t * Bo) * kDU;
+#pragma unroll
+    for (int u = 0; u < kDU; u++)
+      wv[u] = (has_chunk && q < q1 && o0 + u < P.O) ? ldg_stream(T.w + (size_t)(o0 + u) * T.pitch + 16 * c) : zero_w;
+  };
+  Limbs L;
+  int cur_t = -1;
+  uint4 wnext[kDU];
+  load_batch(q0, wnext);
+  for (long long qs = q0; qs < q1; qs += kLinSeg) {
+    const int nq = (int)min((long long)kLinSeg, q1 - qs);
+    for (int b = 0; b < nq; b++) {
+      const long long q = qs + b;
+      const int t = (int)(q / Bo);
+      const int o0 = (int)(q - (long long)t * Bo) * kDU;
+      uint4 wv[kDU];
+#pragma unroll
+      for (int u = 0; u < kDU; u++) wv[u] = wnext[u];
+      load_batch(q + 1, wnext);
+      if (t != cur_t) {  // uniform across the CTA
+        cur_t = t;
+        float xv[32];
+        load_chunk_f32(P.x, P.x_dtype, (size_t)t * P.I, 32 * c, has_chunk ? P.I : 0, xv);
+        if (!make_limbs(xv, L) && has_chunk) set_error(P.err, COLI_E_NONFINITE);
+      }
+      float part[kDU];
+#pragma unroll
+      for (int u = 0; u < kDU; u++) {
+        float d = 0.f;
+        if (has_chunk && o0 + u < P.O) {
+          if (T.mode == SCALE_GENERIC) {
+            d = chunk_dot_generic(wv[u], P.x, P.x_dtype, (size_t)t * P.I, &T, o0 + u, c);
+          } else {
+            d = chunk_dot(wv[u], L);
+            if (T.mode == SCALE_CHUNK) d *= __ldg(T.s + (size_t)(o0 + u) * T.G + (32 * c) / T.gs);
+          }
+        }
+        part[u] = d;
+      }
+      // lane l ends with the warp total of row l / (32 / kDU) of the batch
+      warp_transpose_reduce<kDU>(part, lane);
+      if ((lane & (32 / kDU - 1)) == 0) red[warp][b * kDU + lane / (32 / kDU)] = part[0];
+    }
+    __syncthreads();
+    for (int r = tid; r < nq * kDU; r += blockDim.x) {
+      const long long q = qs + r / kDU;
+      const int t = (int)(q / Bo);
+      const int o = (int)(q - (long long)t * Bo) * kDU + r % kDU;
+      if (o >= P.O) continue;
+      float acc = 0.f;
+      for (int wi = 0; wi < nwarps; wi++) acc += red[wi][r];
+      if (T.mode == SCALE_ROW) acc *= __ldg(T.s + o);
+      const size_t i = (size_t)t * P.O + o;
+      if (P.resid) acc = load_act(P.resid, P.x_dtype, i) + acc;
+      if (P.x_dtype == COLI_DTYPE_F32)
+        static_cast<float*>(P.y)[i] = acc;
+      else
+        static_cast<uint16_t*>(P.y)[i] = f32_to_bf16_rn(acc);
+    }
+    __syncthreads();  // red is reused by the next segment
+  }
+}
+
+// ------------------------------------------------------------------------------------------
 // Resident take: the issued groups' partial sums, in issue order, joined to the residual.
 // ------------------------------------------------------------------------------------------
 
@@ -1355,6 +1454,36 @@ int launch_expert_group(coli_ctx* ctx, const void* x, int x_dtype, int S, const 
     combine_kernel<<<grid, 256, 0, ctx->stream>>>(P);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(ctx, e, "down/combine launch");
+  return COLI_OK;
+}
+
+int launch_linear(coli_ctx* ctx, const TensorDesc& T, const void* x, int x_dtype, int S, const void* resid, void* y) {
+  LinearParams P;
+  P.x = x;
+  P.resid = resid;
+  P.y = y;
+  P.x_dtype = x_dtype;
+  P.S = S;
+  P.O = T.rows;
+  P.I = T.cols;
+  P.err = ctx->d_status;
+  const int CI = (T.cols + 31) / 32;
+  const int nt = (CI + 31) / 32 * 32;
+  auto kern = nt <= 256 ? linear_kernel<256> : (nt <= 512 ? linear_kernel<512> : linear_kernel<1024>);
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, nt, 0) != cudaSuccess) {
+    (void)cudaGetLastError();
+    occ = 1;
+  }
+  // at least four row batches per CTA: a CTA computes its token's limbs once per range
+  const long long NB = (long long)S * ((T.rows + kDU - 1) / kDU);
+  long long grid = (long long)ctx->num_sms * (occ > 0 ? occ : 1);
+  if (grid > (NB + 3) / 4) grid = (NB + 3) / 4;
+  if (grid < 1) grid = 1;
+  ProfScope prof(ctx, COLI_KERNEL_LINEAR);
+  kern<<<(int)grid, nt, 0, ctx->stream>>>(P, T);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "linear launch");
   return COLI_OK;
 }
 

@@ -17,6 +17,11 @@ Sources (web pages about the "colibri" int4 MoE engine; cited by page and sectio
             (grouped 3-launch path: dual gate/up GEMV, SiLU, down GEMV)
   [resid]   PR #434 "COLI_CUDA_RESID=1", section "What"
             (per-expert weighting + fixed-order reduce, joined to the residual)
+  [attn]    c/backend_cuda.cu commit history, commit "CUDA batch MLA attention, kv_b head-sharding,
+            fused o_proj, expert-group dispatch, W4A16 kernels" (the shared expert on the device)
+  [pipe]    c/backend_cuda.cu commit history, commit "GPU resident pipeline ..." (the shared-expert
+            MLP beside the residual adds)
+  [q651]    PR #651, comment "Follow-up decode experiments" (the generic quant_matmul's kernel share)
 
 Precision: weights are dequantised exactly (float64) and every dot product, SiLU and
 the weighted reduce run in float64. The router's decisions (top-K, top-p) are taken in
@@ -266,3 +271,33 @@ def expert_group(x, experts, idx, w, n_sel=None, resid=None) -> np.ndarray:
             acc = acc + float(w[t, k]) * expert_ffn(x[t], gate, up, down)
         y[t] = acc if resid is None else np.asarray(resid[t], dtype=np.float64) + acc
     return y
+
+
+# ------------------------------------------------------------------------------------------
+# Dense int4 projection and the shared expert [tcgate], [q651], [attn], [pipe]
+# ------------------------------------------------------------------------------------------
+
+def w4_linear(x, W: Tensor, resid=None) -> np.ndarray:
+    """y[t] = resid[t] + W x[t] for every token t, float64: the one-tensor int4 matmul that
+    [tcgate] calls quant_matmul (the per-expert fallback) and [q651] measures as the largest
+    kernel share of a decode step. W is dequantised exactly as in [g4]."""
+    x = np.atleast_2d(np.asarray(x, dtype=np.float64))
+    y = x @ W.dense().T
+    return y if resid is None else np.asarray(resid, dtype=np.float64) + y
+
+
+def moe_block_with_shared(x, experts, idx, w, n_sel, shared, resid=None) -> np.ndarray:
+    """y[t] = resid[t] + (routed[t] + E_shared(x[t])), float64.
+
+    routed[t] is the slot-ordered weighted sum of :func:`expert_group` (no residual); the
+    shared expert is a (gate, up, down) triple applied to every token with weight 1 ([attn]
+    runs it on the device, [pipe] beside the residual adds). Reading: the pages give no
+    formula; we take the usual one, an always-chosen expert whose output is added unscaled
+    (no routing weight, no routed scale), and sum routed then shared before the residual.
+    """
+    x = np.atleast_2d(np.asarray(x, dtype=np.float64))
+    routed = expert_group(x, experts, idx, w, n_sel, None)
+    gate, up, down = shared
+    sh = np.stack([expert_ffn(x[t], gate, up, down) for t in range(x.shape[0])])
+    y = routed + sh
+    return y if resid is None else np.asarray(resid, dtype=np.float64) + y

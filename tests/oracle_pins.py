@@ -304,4 +304,70 @@ def pin_reduce_properties(o):
     assert np.array_equal(yz, resid.astype(np.float64))               # no slot: residual only
 
 
+def pin_linear_bruteforce(o):
+    """w4_linear against element-by-element sums over the packed nibbles, every scale layout."""
+    O, I, S = 7, 12, 3
+    for trial, gs in enumerate([0, 2, 4, 6, 12]):
+        p, sc = synth.expert_tensor(synth.stream_seed(60 + trial, "W"), O, I, gs)
+        T = o.Tensor(p, sc, O, I, gs)
+        x = synth.normal(synth.stream_seed(60 + trial, "x"), S * I).reshape(S, I)
+        resid = synth.normal(synth.stream_seed(60 + trial, "r"), S * O).reshape(S, O)
+        y0 = o.w4_linear(x, T)
+        y1 = o.w4_linear(x, T, resid)
+        for t in range(S):
+            ref = _matvec_brute(T, x[t])
+            assert np.allclose(y0[t], ref, rtol=1e-12, atol=1e-12), (trial, t)
+            assert np.allclose(y1[t], [float(resid[t, r]) + ref[r] for r in range(O)], rtol=1e-12, atol=1e-12), (trial, t)
+
+
+def pin_linear_exact_and_transposed(o):
+    """Integer x and power-of-two scales give exact integers; a one-hot x reads out a column."""
+    O, I = 5, 8
+    q = ((synth.u64(synth.stream_seed(70, "q"), O * I) % np.uint64(16)).astype(np.int16) - 8).reshape(O, I)
+    sc = np.array([2.0 ** (r - 2) for r in range(O)], np.float32)
+    T = _tensor_from_q(o, q, sc)
+    xi = np.array([3, -1, 0, 2, -4, 1, 1, -2], np.int64)
+    got = o.w4_linear(xi.astype(np.float64).reshape(1, I), T)[0]
+    assert got.tolist() == [sum(int(q[r, j]) * int(xi[j]) for j in range(I)) * 2.0 ** (r - 2) for r in range(O)]
+    for j in range(I):
+        e = np.zeros((1, I))
+        e[0, j] = 1.0
+        col = o.w4_linear(e, T)[0]
+        assert col.tolist() == [int(q[r, j]) * 2.0 ** (r - 2) for r in range(O)], j
+
+
+def pin_shared_expert_bruteforce(o):
+    """Routed slots plus an always-chosen shared expert of weight 1, by hand-written loops."""
+    D, I, E, S = 8, 6, 4, 2
+    def trip(tag):
+        out = []
+        for which, (r, c, gs) in zip("gud", ((I, D, 2), (I, D, 0), (D, I, 6))):
+            p, sc = synth.expert_tensor(synth.stream_seed(80, tag, which), r, c, gs)
+            out.append(o.Tensor(p, sc, r, c, gs))
+        return tuple(out)
+    experts = {e: trip(e) for e in range(E)}
+    shared = trip("shared")
+    x = synth.normal(synth.stream_seed(81, "x"), S * D).reshape(S, D)
+    resid = synth.normal(synth.stream_seed(81, "r"), S * D).reshape(S, D)
+    idx = np.array([[1, 3], [2, 0]], np.int32)
+    w = np.array([[0.6, 0.4], [1.25, 0.5]], np.float32)
+    n_sel = np.array([2, 1], np.int32)
+    y = o.moe_block_with_shared(x, experts, idx, w, n_sel, shared, resid)
+    y0 = o.moe_block_with_shared(x, experts, idx, w, np.array([0, 0], np.int32), shared, None)
+
+    def ffn(trip_, v):
+        G, U, Dn = trip_
+        g, u = _matvec_brute(G, v), _matvec_brute(U, v)
+        return _matvec_brute(Dn, [g[i] / (1.0 + math.exp(-g[i])) * u[i] for i in range(I)])
+    for t in range(S):
+        sh = ffn(shared, x[t])
+        acc = [0.0] * D
+        for k in range(int(n_sel[t])):
+            yk = ffn(experts[int(idx[t, k])], x[t])
+            acc = [acc[d] + float(w[t, k]) * yk[d] for d in range(D)]
+        want = [float(resid[t, d]) + (acc[d] + sh[d]) for d in range(D)]
+        assert np.allclose(y[t], want, rtol=1e-12, atol=1e-12), t
+        assert np.allclose(y0[t], sh, rtol=1e-12, atol=1e-12), t  # no routed slot: the shared expert alone
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

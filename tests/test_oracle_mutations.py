@@ -156,9 +156,32 @@ def gate_up_swapped(o):
     o.expert_ffn = lambda x_row, gate, up, down: orig(x_row, up, gate, down)
 
 
+def linear_drops_residual(o):
+    orig = o.w4_linear
+    o.w4_linear = lambda x, W, resid=None: orig(x, W, None)
+
+
+def linear_reads_columns_reversed(o):
+    orig = o.w4_linear
+    o.w4_linear = lambda x, W, resid=None: orig(np.atleast_2d(np.asarray(x))[:, ::-1], W, resid)
+
+
+def shared_weighted_like_slot0(o):
+    orig = o.moe_block_with_shared
+
+    def bad(x, experts, idx, w, n_sel, shared, resid=None):
+        routed = orig(x, experts, idx, w, n_sel, shared, None) - orig(x, experts, idx, w, np.zeros(len(idx), np.int32),
+                                                                        shared, None)
+        sh = orig(x, experts, idx, w, np.zeros(len(idx), np.int32), shared, None)
+        y = routed + np.asarray(w, np.float64)[:, :1] * sh
+        return y if resid is None else np.asarray(resid, np.float64) + y
+    o.moe_block_with_shared = bad
+
+
 MUTATIONS = [swap_nibble_order, offset_seven, tie_to_higher_index, weights_from_choice, scale_before_norm,
              topp_drops_reaching_slot, norm_over_all_slots, sigmoid_sign, silu_on_up, drop_residual,
-             group_scales_column_major, group_index_by_byte, down_transposed_roles, gate_up_swapped]
+             group_scales_column_major, group_index_by_byte, down_transposed_roles, gate_up_swapped,
+             linear_drops_residual, linear_reads_columns_reversed, shared_weighted_like_slot0]
 
 
 @pytest.mark.parametrize("mutate", MUTATIONS, ids=[m.__name__ for m in MUTATIONS])
