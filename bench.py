@@ -37,7 +37,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--no-clocks", action="store_true")
-    ap.add_argument("--no-prefill", action="store_true", help="skip the tensor-core prefill figure")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill, shared-expert and dense-projection figures")
     ap.add_argument("--cpu-worker", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -64,6 +64,107 @@ def bf16_peak():
         with open(path) as f:
             return float(json.load(f)["bf16_tflops"]), "measured"
     return 1900.0, "fallback"
+
+
+def linear_leg(ctx, stream, flush, D, steps=20, warmup=3):
+    """The dense int4 projection (coli_w4_linear) of one decode token through a D x D per-row-scaled
+    tensor: event-timed launches with a cold L2, HBM bytes per launch and the fraction of the peak."""
+    import numpy as np
+    import torch
+
+    from int4_grouped_expert_router_gb300 import binding as B
+    from int4_grouped_expert_router_gb300 import synth
+
+    p, sc = synth.expert_tensor_torch(synth.stream_seed(900, "dense"), D, D, 0, "cuda")
+    h = B.coli_expert_upload(ctx, p.contiguous(), sc.contiguous(), D, D, 0)
+    del p, sc
+    n = warmup + steps
+    xs = [torch.from_numpy(synth.normal(synth.stream_seed(901, s), D).reshape(1, D)).cuda() for s in range(n)]
+    rs = [torch.from_numpy(synth.normal(synth.stream_seed(902, s), D).reshape(1, D)).cuda() for s in range(n)]
+    ys = [torch.empty(1, D, device="cuda") for _ in range(n)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for s in range(n):
+            flush.zero_()
+            ev[s][0].record(stream)
+            B.coli_w4_linear(ctx, h, xs[s], rs[s], ys[s])
+            ev[s][1].record(stream)
+    torch.cuda.synchronize()
+    assert B.coli_check_error(ctx) == 0, B.coli_last_error(ctx)
+    B.coli_expert_free(ctx, h)
+    us = statistics.mean(ev[s][0].elapsed_time(ev[s][1]) for s in range(warmup, n)) * 1000.0
+    nbytes = D * (D // 2) + 4 * D + 3 * 4 * D  # packed weights, row scales, x, resid, y
+    hpeak, hkind = peaks()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"workload": f"dense int4 projection O={D} I={D} gs=0, S=1, f32, residual", "us": us, "steps": steps,
+            "launch": "one C-ABI call per step", "l2": "flushed between steps", "bytes": nbytes, "hbm_gbs": gbs,
+            "hbm_frac": gbs / hpeak, "peak_kind": f"{hkind} hbm_gbs"}
+
+
+def shared_expert_leg(ctx, stream, flush, layer, xs, rs, steps=20, warmup=3):
+    """The decode layer with an always-chosen shared expert (weight 1, the routed experts' shape): the
+    router appends it after the kept slots and one grouped call runs all K + 1 experts, as one CUDA
+    graph per step."""
+    import numpy as np
+    import torch
+
+    from int4_grouped_expert_router_gb300 import binding as B
+    from int4_grouped_expert_router_gb300 import synth
+    from int4_grouped_expert_router_gb300.workload import tensor_seed
+
+    cfg = layer.cfg
+    e_sh = cfg.E  # outside the router's ids
+    hs = []
+    for which, (rows, cols) in (("gate", (cfg.I, cfg.D)), ("up", (cfg.I, cfg.D)), ("down", (cfg.D, cfg.I))):
+        p, sc = synth.expert_tensor_torch(tensor_seed(cfg, e_sh, which), rows, cols, cfg.gs_of(e_sh), "cuda")
+        hs.append(B.coli_expert_upload(ctx, p.contiguous(), sc.contiguous(), rows, cols, cfg.gs_of(e_sh)))
+        del p, sc
+    B.coli_expert_table_set(ctx, e_sh, *hs)
+    xin, rin, yout = torch.empty_like(xs[0]), torch.empty_like(rs[0]), torch.empty_like(rs[0])
+    r = dict(idx=torch.empty(cfg.S, cfg.K + 1, dtype=torch.int32, device="cuda"),
+             w=torch.empty(cfg.S, cfg.K + 1, device="cuda"), n_sel=torch.empty(cfg.S, dtype=torch.int32, device="cuda"))
+
+    def body():  # the router appends the shared slot; one grouped call runs the K + 1 experts
+        B.coli_router_select_shared(ctx, xin, layer.Wr, layer.bias, cfg.K, cfg.topp, cfg.norm_topk, cfg.routed_scale,
+                                    e_sh, r["idx"], r["w"], r["n_sel"])
+        B.coli_expert_group(ctx, xin, r["idx"], r["w"], r["n_sel"], cfg.K + 1, rin, yout)
+
+    n = min(len(xs), warmup + steps)
+    with torch.cuda.stream(stream):
+        xin.copy_(xs[0])
+        rin.copy_(rs[0])
+        body()  # eager once: the workspace is sized before capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        body()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    routed_bytes = []
+    with torch.cuda.stream(stream):
+        for s in range(n):
+            xin.copy_(xs[s])
+            rin.copy_(rs[s])
+            flush.zero_()
+            ev[s][0].record(stream)
+            g.replay()
+            ev[s][1].record(stream)
+            if s >= warmup:
+                idx = r["idx"].cpu().numpy()
+                routed_bytes.append(sum(cfg.expert_bytes(int(e)) for e in np.unique(idx[(idx >= 0) & (idx != e_sh)])))
+    torch.cuda.synchronize()
+    assert B.coli_check_error(ctx) == 0, B.coli_last_error(ctx)
+    del g
+    B.coli_expert_table_set(ctx, e_sh, 0, 0, 0)
+    for h in hs:
+        B.coli_expert_free(ctx, h)
+    us = statistics.mean(ev[s][0].elapsed_time(ev[s][1]) for s in range(warmup, n)) * 1000.0
+    nbytes = statistics.mean(routed_bytes) + cfg.expert_bytes(e_sh)
+    hpeak, hkind = peaks()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"workload": f"decode layer + 1 shared expert (D={cfg.D} I={cfg.I}), K={cfg.K} routed of E={cfg.E}",
+            "us_per_layer": us, "steps": n - warmup, "launch": "router with the shared slot + one grouped call of K+1 slots, one CUDA graph per step",
+            "l2": "flushed between steps", "expert_bytes": nbytes, "hbm_gbs": gbs, "hbm_frac": gbs / hpeak,
+            "peak_kind": f"{hkind} hbm_gbs"}
 
 
 def prefill_leg(ctx, stream, flush, steps=10, warmup=3):
@@ -502,6 +603,14 @@ def gpu_arm(args, rank, world, local):
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clock_info,
         }
+    extra = {}
+    if rank == 0 and not args.no_prefill:
+        for name, leg in (("shared_expert", lambda: shared_expert_leg(ctx, stream, flush, layer, xs, rs)),
+                          ("dense_projection", lambda: linear_leg(ctx, stream, flush, cfg.D))):
+            try:
+                extra[name] = leg()
+            except Exception as exc:  # these figures must not hide the decode number
+                extra[name] = {"error": f"{exc}"[:300]}
     layer.free()
     prefill = None
     if rank == 0 and not args.no_prefill:
@@ -511,6 +620,7 @@ def gpu_arm(args, rank, world, local):
             prefill = {"error": f"{exc}"[:300]}
     if result is not None:
         result["prefill"] = prefill
+        result.update(extra)
     B.coli_destroy(ctx)
     if dist is not None:
         dist.destroy_process_group()

@@ -130,6 +130,21 @@ COLI_API int coli_router_select(coli_ctx *ctx, const void *x, int x_dtype, int S
                        int norm_topk, float routed_scale, int32_t *idx, float *w, int32_t *n_sel);
 
 /*
+ * coli_router_select with a shared expert ([attn], [pipe]): the same selection and weights, and
+ * then the shared expert `shared` (a table id, 0 <= shared < COLI_MAX_EXPERTS, normally >= E so it
+ * is never also routed) is placed right after each token's kept slots as one more kept slot with
+ * weight exactly 1 (no normalisation, no routed scale). Outputs: idx [S x (K+1)], w [S x (K+1)],
+ * n_sel [S] = kept routed slots + 1; the slots after the shared one hold idx = -1 and w = 0.
+ * coli_expert_group with K + 1 then runs the routed experts and the shared expert in the same
+ * launches and adds the shared expert's output after the routed ones, in slot order.
+ * Limits as coli_router_select, with K + 1 <= COLI_MAX_K.
+ */
+COLI_API int coli_router_select_shared(coli_ctx *ctx, const void *x, int x_dtype, int S, int D,
+                              const float *Wr, const float *bias, int E, int K, float topp,
+                              int norm_topk, float routed_scale, int shared, int32_t *idx, float *w,
+                              int32_t *n_sel);
+
+/*
  * Same computation, arguments, outputs and error behaviour as coli_router_select, but the call
  * allocates nothing: no cudaMalloc or cudaFree and no allocating library call, whatever the size.
  * The router's pages have no counterpart for this entry; it serves callers that cannot let a call
@@ -235,11 +250,6 @@ COLI_API int coli_expert_group_take(coli_ctx *ctx, const void *resid, void *y);
  * 1 <= S <= COLI_MAX_TOKENS. Every weight byte is read from HBM once per call for the first token;
  * the other tokens' passes over W mostly hit L2. COLI_E_INVAL for a bad handle, pointer, dtype or
  * S. Profiled as COLI_KERNEL_LINEAR.
- *
- * A shared expert ([attn] runs it on the device, [pipe] keeps it beside the residual adds) is an
- * always-chosen expert with weight 1. With the same shape as the routed experts it is one more
- * table entry outside the router's E ids, issued as its own group (idx = its id for every token,
- * w = 1, K = 1, n_sel NULL) with coli_expert_group_issue next to the routed group, before the take.
  */
 COLI_API int coli_w4_linear(coli_ctx *ctx, uint64_t W, const void *x, int x_dtype, int S, const void *resid,
                             void *y);

@@ -58,6 +58,7 @@ SIGNATURES = {
     "coli_reserve": (_I, [_P, _I, _I, _I, _I, _I]),
     "coli_router_select": (_I, [_P, _P, _I, _I, _I, _P, _P, _I, _I, _F, _I, _F, _P, _P, _P]),
     "coli_router_select_noalloc": (_I, [_P, _P, _I, _I, _I, _P, _P, _I, _I, _F, _I, _F, _P, _P, _P]),
+    "coli_router_select_shared": (_I, [_P, _P, _I, _I, _I, _P, _P, _I, _I, _F, _I, _F, _I, _P, _P, _P]),
     "coli_expert_upload": (_U64, [_P, _P, _P, _I, _I, _I]),
     "coli_expert_free": (_I, [_P, _U64]),
     "coli_tensor_shape": (_I, [_P, _U64, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
@@ -168,8 +169,9 @@ def coli_reserve(ctx, max_S, max_E, max_K, max_D, max_I):
     return _check(ctx, library().coli_reserve(ctx, max_S, max_E, max_K, max_D, max_I), "coli_reserve")
 
 
-def _router_args(x, Wr, bias, K, idx, w, n_sel):
+def _router_args(x, Wr, bias, K, idx, w, n_sel, slots=None):
     S, D = x.shape
+    slots = K if slots is None else slots
     E = Wr.shape[0]
     _dev(x, name="x")
     _dev(Wr, torch.float32, "Wr")
@@ -177,7 +179,8 @@ def _router_args(x, Wr, bias, K, idx, w, n_sel):
     _dev(idx, torch.int32, "idx")
     _dev(w, torch.float32, "w")
     _dev(n_sel, torch.int32, "n_sel")
-    if Wr.shape[1] != D or idx.numel() != S * K or w.numel() != S * K or (n_sel is not None and n_sel.numel() != S):
+    if Wr.shape[1] != D or idx.numel() != S * slots or w.numel() != S * slots or \
+            (n_sel is not None and n_sel.numel() != S):
         raise ValueError("router_select: inconsistent shapes")
     if bias is not None and bias.numel() != E:
         raise ValueError("router_select: bias must have E entries")
@@ -189,6 +192,16 @@ def coli_router_select(ctx, x, Wr, bias, K, topp, norm_topk, routed_scale, idx, 
     rc = library().coli_router_select(ctx, _ptr(x), act_dtype(x), S, D, _ptr(Wr), _ptr(bias), E, K, float(topp),
                                       int(bool(norm_topk)), float(routed_scale), _ptr(idx), _ptr(w), _ptr(n_sel))
     return _check(ctx, rc, "coli_router_select")
+
+
+def coli_router_select_shared(ctx, x, Wr, bias, K, topp, norm_topk, routed_scale, shared, idx, w, n_sel=None):
+    """coli_router_select plus the shared expert ``shared`` after each token's kept slots (weight 1):
+    idx and w are [S x (K+1)]."""
+    S, D, E = _router_args(x, Wr, bias, K, idx, w, n_sel, slots=K + 1)
+    rc = library().coli_router_select_shared(ctx, _ptr(x), act_dtype(x), S, D, _ptr(Wr), _ptr(bias), E, K, float(topp),
+                                             int(bool(norm_topk)), float(routed_scale), int(shared), _ptr(idx), _ptr(w),
+                                             _ptr(n_sel))
+    return _check(ctx, rc, "coli_router_select_shared")
 
 
 def coli_router_select_noalloc(ctx, x, Wr, bias, K, topp, norm_topk, routed_scale, idx, w, n_sel=None):

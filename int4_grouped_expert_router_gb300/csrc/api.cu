@@ -478,7 +478,23 @@ int coli_router_select(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, 
     return fail(ctx, COLI_E_INVAL, "router: size out of range");
   if (injected(ctx)) return COLI_E_INJECTED;
   cudaSetDevice(ctx->device);
-  int rc = launch_router(ctx, x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk, routed_scale, idx, w, n_sel);
+  int rc = launch_router(ctx, x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk, routed_scale, -1, idx, w, n_sel);
+  if (rc == COLI_OK) ctx->compute_calls++;
+  return rc;
+}
+
+int coli_router_select_shared(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr,
+                              const float* bias, int E, int K, float topp, int norm_topk, float routed_scale,
+                              int shared, int32_t* idx, float* w, int32_t* n_sel) {
+  if (!ctx) return COLI_E_INVAL;
+  if (!x || !Wr || !idx || !w) return fail(ctx, COLI_E_INVAL, "router_shared: NULL pointer");
+  if (x_dtype != COLI_DTYPE_F32 && x_dtype != COLI_DTYPE_BF16) return fail(ctx, COLI_E_INVAL, "router_shared: dtype");
+  if (S < 1 || S > COLI_MAX_TOKENS || D < 1 || D > COLI_MAX_DIM || E < 1 || E > COLI_MAX_EXPERTS || K < 1 ||
+      K + 1 > COLI_MAX_K || K > E || shared < 0 || shared >= COLI_MAX_EXPERTS)
+    return fail(ctx, COLI_E_INVAL, "router_shared: size or shared id out of range");
+  if (injected(ctx)) return COLI_E_INJECTED;
+  cudaSetDevice(ctx->device);
+  int rc = launch_router(ctx, x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk, routed_scale, shared, idx, w, n_sel);
   if (rc == COLI_OK) ctx->compute_calls++;
   return rc;
 }
@@ -494,7 +510,8 @@ int coli_router_select_noalloc(coli_ctx* ctx, const void* x, int x_dtype, int S,
     return fail(ctx, COLI_E_INVAL, "router_noalloc: size out of range");
   if (injected(ctx)) return COLI_E_INJECTED;
   cudaSetDevice(ctx->device);
-  int rc = launch_router_noalloc(ctx, x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk, routed_scale, idx, w, n_sel);
+  int rc = launch_router_noalloc(ctx, x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk, routed_scale, -1, idx, w,
+                                  n_sel);
   if (rc == COLI_OK) ctx->compute_calls++;
   return rc;
 }

@@ -143,8 +143,9 @@ struct ProfScope {
 };
 
 // Launchers (defined in router.cu / experts.cu). Arguments already validated.
+// shared >= 0: every token's row gets K + 1 slots, the shared expert placed after the kept ones.
 int launch_router(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr,
-                  const float* bias, int E, int K, float topp, int norm_topk, float routed_scale,
+                  const float* bias, int E, int K, float topp, int norm_topk, float routed_scale, int shared,
                   int32_t* idx, float* w, int32_t* n_sel);
 // Tensor-core (prefill) path of coli_expert_group: bf16 activations, many routed rows per expert.
 bool prefill_eligible(const coli_ctx* ctx, const void* x, int S, int K, int x_dtype);
@@ -155,7 +156,7 @@ int launch_prefill(coli_ctx* ctx, const void* x, int S, const int32_t* idx, cons
 int encode_bf16_rows_map(coli_ctx* ctx, CUtensorMap* map, void* base, long long rows, int cols);
 
 int launch_router_noalloc(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr,
-                          const float* bias, int E, int K, float topp, int norm_topk, float routed_scale,
+                          const float* bias, int E, int K, float topp, int norm_topk, float routed_scale, int shared,
                           int32_t* idx, float* w, int32_t* n_sel);
 // y is written in y_dtype (x_dtype for coli_expert_group; f32 for an issued partial sum); resid is read in x_dtype.
 int launch_expert_group(coli_ctx* ctx, const void* x, int x_dtype, int S, const int32_t* idx,

@@ -1162,11 +1162,12 @@ __global__ void combine_kernel(GroupParams P) {
 // Dense int4 projection: y[t, o] = resid[t, o] + sum_i W[o, i] x[t, i] for S tokens.
 //
 // The same block-fixed-point dot product as the expert kernels. A thread owns one 16-byte chunk
-// (32 columns) of every row; a CTA takes a contiguous range of (token, 4-row batch) items, the
-// items ordered token-major so a token's limbs are computed once per CTA. Each batch loads its
-// four rows' chunks from HBM (streaming loads, the next batch's issued before the current batch's
-// products), reduces them across the warp and parks the warp totals in shared memory; every
-// kLinSeg batches the CTA adds the warps' totals in warp order and writes the finished rows.
+// (32 columns) of every row; a CTA takes a contiguous range of (token, kLinRows-row batch) items,
+// ordered token-major so a token's limbs are computed once per CTA. Each batch's rows are loaded
+// from HBM with streaming loads, the next batch's issued before the current batch's products, so a
+// CTA of two batches has all its rows in flight in one round trip. The products are reduced
+// across the warp and the warp totals parked in shared memory; every kLinSeg batches the CTA adds
+// the warps' totals in warp order and writes the finished rows.
 // ------------------------------------------------------------------------------------------
 
 struct LinearParams {
@@ -1178,50 +1179,68 @@ struct LinearParams {
   int* err;
 };
 
-constexpr int kLinSeg = 16;  // batches of kDU rows finished together
+constexpr int kLinRows = 8;  // rows per batch
+constexpr int kLinSeg = 8;   // batches finished together
+
+// Position of a (token, row batch) item, advanced one item at a time (no divisions in the loops).
+struct LinPos {
+  int t, ob;  // token, row batch within the token
+  __device__ __forceinline__ void next(int Bo) {
+    if (++ob == Bo) {
+      ob = 0;
+      ++t;
+    }
+  }
+};
 
 template <int MAXT>
 __global__ void __launch_bounds__(MAXT) linear_kernel(LinearParams P, const __grid_constant__ TensorDesc T) {
-  __shared__ float red[MAXT / 32][kLinSeg * kDU];
+  __shared__ float red[MAXT / 32][kLinSeg * kLinRows];
+  __shared__ int row_of[kLinSeg][2];  // (token, first row) of each batch of the segment
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
   const int CI = (P.I + 31) >> 5;
   const int c = tid;
   const bool has_chunk = c < CI;
-  const int Bo = (P.O + kDU - 1) / kDU;  // row batches per token
-  const long long NB = (long long)P.S * Bo;
-  const long long q0 = (long long)blockIdx.x * NB / gridDim.x;
-  const long long q1 = (long long)(blockIdx.x + 1) * NB / gridDim.x;
+  const int Bo = (P.O + kLinRows - 1) / kLinRows;  // row batches per token
+  const long long NB = (long long)P.S * Bo;        // < 2^31 (S <= 65536, O <= 32768)
+  const int q0 = (int)((long long)blockIdx.x * NB / gridDim.x);
+  const int q1 = (int)((long long)(blockIdx.x + 1) * NB / gridDim.x);
   const uint4 zero_w = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);  // nibbles 8: value 0
-  auto load_batch = [&](long long q, uint4 (&wv)[kDU]) {
-    const int t = (int)(q / Bo);
-    const int o0 = (int)(q - (long long)t * Bo) * kDU;
+  auto load_batch = [&](bool live, const LinPos& ps, uint4 (&wv)[kLinRows]) {
+    const int o0 = ps.ob * kLinRows;
 #pragma unroll
-    for (int u = 0; u < kDU; u++)
-      wv[u] = (has_chunk && q < q1 && o0 + u < P.O) ? ldg_stream(T.w + (size_t)(o0 + u) * T.pitch + 16 * c) : zero_w;
+    for (int u = 0; u < kLinRows; u++)
+      wv[u] = (has_chunk && live && o0 + u < P.O) ? ldg_stream(T.w + (size_t)(o0 + u) * T.pitch + 16 * c) : zero_w;
   };
+  LinPos pos{q0 / Bo, q0 % Bo};  // the batch being computed
+  LinPos ahead = pos;            // the batch whose rows are loaded next
   Limbs L;
   int cur_t = -1;
-  uint4 wnext[kDU];
-  load_batch(q0, wnext);
-  for (long long qs = q0; qs < q1; qs += kLinSeg) {
-    const int nq = (int)min((long long)kLinSeg, q1 - qs);
+  uint4 wnext[kLinRows];
+  load_batch(q0 < q1, ahead, wnext);
+  ahead.next(Bo);
+  for (int qs = q0; qs < q1; qs += kLinSeg) {
+    const int nq = min(kLinSeg, q1 - qs);
     for (int b = 0; b < nq; b++) {
-      const long long q = qs + b;
-      const int t = (int)(q / Bo);
-      const int o0 = (int)(q - (long long)t * Bo) * kDU;
-      uint4 wv[kDU];
+      const int t = pos.t, o0 = pos.ob * kLinRows;
+      if (tid == 0) {
+        row_of[b][0] = t;
+        row_of[b][1] = o0;
+      }
+      uint4 wv[kLinRows];
 #pragma unroll
-      for (int u = 0; u < kDU; u++) wv[u] = wnext[u];
-      load_batch(q + 1, wnext);
+      for (int u = 0; u < kLinRows; u++) wv[u] = wnext[u];
+      load_batch(qs + b + 1 < q1, ahead, wnext);
+      ahead.next(Bo);
       if (t != cur_t) {  // uniform across the CTA
         cur_t = t;
         float xv[32];
         load_chunk_f32(P.x, P.x_dtype, (size_t)t * P.I, 32 * c, has_chunk ? P.I : 0, xv);
         if (!make_limbs(xv, L) && has_chunk) set_error(P.err, COLI_E_NONFINITE);
       }
-      float part[kDU];
+      float part[kLinRows];
 #pragma unroll
-      for (int u = 0; u < kDU; u++) {
+      for (int u = 0; u < kLinRows; u++) {
         float d = 0.f;
         if (has_chunk && o0 + u < P.O) {
           if (T.mode == SCALE_GENERIC) {
@@ -1233,15 +1252,15 @@ __global__ void __launch_bounds__(MAXT) linear_kernel(LinearParams P, const __gr
         }
         part[u] = d;
       }
-      // lane l ends with the warp total of row l / (32 / kDU) of the batch
-      warp_transpose_reduce<kDU>(part, lane);
-      if ((lane & (32 / kDU - 1)) == 0) red[warp][b * kDU + lane / (32 / kDU)] = part[0];
+      // lane l ends with the warp total of row l / (32 / kLinRows) of the batch
+      warp_transpose_reduce<kLinRows>(part, lane);
+      if ((lane & (32 / kLinRows - 1)) == 0) red[warp][b * kLinRows + lane / (32 / kLinRows)] = part[0];
+      pos.next(Bo);
     }
     __syncthreads();
-    for (int r = tid; r < nq * kDU; r += blockDim.x) {
-      const long long q = qs + r / kDU;
-      const int t = (int)(q / Bo);
-      const int o = (int)(q - (long long)t * Bo) * kDU + r % kDU;
+    for (int r = tid; r < nq * kLinRows; r += blockDim.x) {
+      const int t = row_of[r / kLinRows][0];
+      const int o = row_of[r / kLinRows][1] + r % kLinRows;
       if (o >= P.O) continue;
       float acc = 0.f;
       for (int wi = 0; wi < nwarps; wi++) acc += red[wi][r];
@@ -1253,7 +1272,7 @@ __global__ void __launch_bounds__(MAXT) linear_kernel(LinearParams P, const __gr
       else
         static_cast<uint16_t*>(P.y)[i] = f32_to_bf16_rn(acc);
     }
-    __syncthreads();  // red is reused by the next segment
+    __syncthreads();  // red and row_of are reused by the next segment
   }
 }
 
@@ -1430,7 +1449,12 @@ int launch_expert_group(coli_ctx* ctx, const void* x, int x_dtype, int S, const 
   if (down_reduce) {
     const int nt = K * TPE;
     const size_t smem = down_smem_bytes(nt / 32);
-    auto kern = nt <= 256 ? down_reduce_kernel<256> : (nt <= 512 ? down_reduce_kernel<512> : down_reduce_kernel<1024>);
+    // block sizes between 512 and 1024 (K = 9..12 slots of 64 threads) get their own register budgets
+    auto kern = nt <= 256   ? down_reduce_kernel<256>
+                : nt <= 512 ? down_reduce_kernel<512>
+                : nt <= 640 ? down_reduce_kernel<640>
+                : nt <= 768 ? down_reduce_kernel<768>
+                            : down_reduce_kernel<1024>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
       return cuda_fail(ctx, e, "down smem attribute");
     int grid = ctx->num_sms;
@@ -1475,10 +1499,10 @@ int launch_linear(coli_ctx* ctx, const TensorDesc& T, const void* x, int x_dtype
     (void)cudaGetLastError();
     occ = 1;
   }
-  // at least four row batches per CTA: a CTA computes its token's limbs once per range
-  const long long NB = (long long)S * ((T.rows + kDU - 1) / kDU);
+  // at least two row batches per CTA: a CTA computes its token's limbs once per range
+  const long long NB = (long long)S * ((T.rows + kLinRows - 1) / kLinRows);
   long long grid = (long long)ctx->num_sms * (occ > 0 ? occ : 1);
-  if (grid > (NB + 3) / 4) grid = (NB + 3) / 4;
+  if (grid > (NB + 1) / 2) grid = (NB + 1) / 2;
   if (grid < 1) grid = 1;
   ProfScope prof(ctx, COLI_KERNEL_LINEAR);
   kern<<<(int)grid, nt, 0, ctx->stream>>>(P, T);

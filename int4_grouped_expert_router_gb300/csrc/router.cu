@@ -35,7 +35,7 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 __device__ __forceinline__ void select_finish(int mine, float wmine, int K, float topp, int norm_topk,
-                                              float routed_scale, int32_t* __restrict__ idx_out,
+                                              float routed_scale, int shared, int32_t* __restrict__ idx_out,
                                               float* __restrict__ w_out, int32_t* __restrict__ nsel_out,
                                               const ExpertDesc* table);
 
@@ -46,7 +46,7 @@ __device__ __forceinline__ void select_finish(int mine, float wmine, int K, floa
 // goes to the lower index. The chosen expert's raw score travels with it.
 template <int EPL>
 __device__ void select_token(const float2* __restrict__ sc_row, int E, int K, float topp, int norm_topk,
-                             float routed_scale, int32_t* __restrict__ idx_out, float* __restrict__ w_out,
+                             float routed_scale, int shared, int32_t* __restrict__ idx_out, float* __restrict__ w_out,
                              int32_t* __restrict__ nsel_out, int* err, const ExpertDesc* table) {
   const int lane = threadIdx.x & 31;
   uint32_t key[EPL];
@@ -92,13 +92,13 @@ __device__ void select_token(const float2* __restrict__ sc_row, int E, int K, fl
       wmine = ws;
     }
   }
-  select_finish(mine, wmine, K, topp, norm_topk, routed_scale, idx_out, w_out, nsel_out, table);
+  select_finish(mine, wmine, K, topp, norm_topk, routed_scale, shared, idx_out, w_out, nsel_out, table);
 }
 
 // Lane k holds the expert of slot k (mine) and its raw score (wmine): weights from the raw
 // (bias-free) score, top-p, norm and scale; every sum in slot order in binary32, no contraction.
 __device__ __forceinline__ void select_finish(int mine, float wmine, int K, float topp, int norm_topk,
-                                              float routed_scale, int32_t* __restrict__ idx_out,
+                                              float routed_scale, int shared, int32_t* __restrict__ idx_out,
                                               float* __restrict__ w_out, int32_t* __restrict__ nsel_out,
                                               const ExpertDesc* table) {
   const int lane = threadIdx.x & 31;
@@ -120,25 +120,30 @@ __device__ __forceinline__ void select_finish(int mine, float wmine, int K, floa
     denom = 0.f;
     for (int k = 0; k < m; k++) denom = __fadd_rn(denom, __shfl_sync(0xffffffffu, wmine, k));
   }
-  if (lane < K) {
+  // shared >= 0: the shared expert follows the kept slots as one more kept slot of weight 1 (no
+  // normalisation, no routed scale), and the row has K + 1 slots
+  const bool has_shared = shared >= 0;
+  if (lane < K + has_shared) {
     const bool kept = lane < m;
+    const bool is_shared = has_shared && lane == m;
     const float wv = norm_topk ? __fdiv_rn(wmine, denom) : wmine;
-    idx_out[lane] = kept ? mine : -1;
-    w_out[lane] = kept ? __fmul_rn(wv, routed_scale) : 0.f;
+    idx_out[lane] = kept ? mine : (is_shared ? shared : -1);
+    w_out[lane] = kept ? __fmul_rn(wv, routed_scale) : (is_shared ? 1.0f : 0.f);
   }
-  if (lane == 0 && nsel_out) *nsel_out = m;
+  if (lane == 0 && nsel_out) *nsel_out = m + has_shared;
   // The chosen experts' table entries go to L2: the expert kernels that follow read them first
-  // (a hint only; every id below E is inside the table).
-  if (table && lane < K)
+  // (a hint only; every id below E, and the shared id, is inside the table).
+  const int pe = lane < K ? mine : (has_shared && lane == K ? shared : -1);
+  if (table && pe >= 0)
     for (int l = 0; l < (int)(sizeof(ExpertDesc) / 128); l++)
-      prefetch_l2_line(reinterpret_cast<const char*>(table + mine) + 128 * l);
+      prefetch_l2_line(reinterpret_cast<const char*>(table + pe) + 128 * l);
 }
 
 // Selection for 1024 < E <= COLI_MAX_EXPERTS (more than 32 experts per lane): the same rules and
 // reductions as select_token, but each round re-reads the lane's (score, choice) pairs through L2
 // instead of holding them in registers, and the chosen set is a 128-bit mask per lane.
 __device__ void select_token_large(const float2* __restrict__ sc_row, int E, int K, float topp, int norm_topk,
-                                   float routed_scale, int32_t* __restrict__ idx_out, float* __restrict__ w_out,
+                                   float routed_scale, int shared, int32_t* __restrict__ idx_out, float* __restrict__ w_out,
                                    int32_t* __restrict__ nsel_out, int* err, const ExpertDesc* table) {
   const int lane = threadIdx.x & 31;
   const int epl = (E + 31) >> 5;           // <= 128
@@ -180,27 +185,28 @@ __device__ void select_token_large(const float2* __restrict__ sc_row, int E, int
       wmine = ws;
     }
   }
-  select_finish(mine, wmine, K, topp, norm_topk, routed_scale, idx_out, w_out, nsel_out, table);
+  select_finish(mine, wmine, K, topp, norm_topk, routed_scale, shared, idx_out, w_out, nsel_out, table);
 }
 
 // EPL = experts per lane (a power of two up to 32); EPL = 0: the large-E selection.
 template <int EPL>
 __device__ __forceinline__ void select_token_any(const float2* sc_row, int E, int K, float topp, int norm_topk,
-                                                 float routed_scale, int32_t* idx_out, float* w_out, int32_t* nsel_out,
-                                                 int* err, const ExpertDesc* table) {
+                                                 float routed_scale, int shared, int32_t* idx_out, float* w_out,
+                                                 int32_t* nsel_out, int* err, const ExpertDesc* table) {
   if constexpr (EPL == 0)
-    select_token_large(sc_row, E, K, topp, norm_topk, routed_scale, idx_out, w_out, nsel_out, err, table);
+    select_token_large(sc_row, E, K, topp, norm_topk, routed_scale, shared, idx_out, w_out, nsel_out, err, table);
   else
-    select_token<EPL>(sc_row, E, K, topp, norm_topk, routed_scale, idx_out, w_out, nsel_out, err, table);
+    select_token<EPL>(sc_row, E, K, topp, norm_topk, routed_scale, shared, idx_out, w_out, nsel_out, err, table);
 }
 
 template <int EPL>
 __device__ void select_all(const float2* sc, int S, int E, int K, float topp, int norm_topk, float routed_scale,
-                           int32_t* idx, float* w, int32_t* n_sel, int* err, const ExpertDesc* table) {
+                           int shared, int32_t* idx, float* w, int32_t* n_sel, int* err, const ExpertDesc* table) {
   const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int slots = K + (shared >= 0);  // output slots per token
   for (int t = warp; t < S; t += nwarps)
-    select_token_any<EPL>(sc + (size_t)t * E, E, K, topp, norm_topk, routed_scale, idx + (size_t)t * K,
-                          w + (size_t)t * K, n_sel ? n_sel + t : nullptr, err, table);
+    select_token_any<EPL>(sc + (size_t)t * E, E, K, topp, norm_topk, routed_scale, shared, idx + (size_t)t * slots,
+                          w + (size_t)t * slots, n_sel ? n_sel + t : nullptr, err, table);
 }
 
 // Logits GEMV: CTA b computes rows e = b * kRowsPerCta + r (r < kRowsPerCta) for every token;
@@ -211,7 +217,7 @@ __device__ void select_all(const float2* sc, int S, int E, int K, float topp, in
 template <bool VEC4>
 __device__ __forceinline__ void router_body(const void* __restrict__ x, int x_dtype, int S, int D,
                                             const float* __restrict__ Wr, const float* __restrict__ bias, int E,
-                                            int K, float topp, int norm_topk, float routed_scale,
+                                            int K, float topp, int norm_topk, float routed_scale, int shared,
                                             float2* __restrict__ sc_ws, int32_t* __restrict__ idx,
                                             float* __restrict__ w, int32_t* __restrict__ n_sel,
                                             int* __restrict__ status, unsigned* arrivals, int epl,
@@ -280,12 +286,12 @@ __device__ __forceinline__ void router_body(const void* __restrict__ x, int x_dt
   __syncthreads();
   if (!am_last) return;
   switch (epl) {
-    case 1: select_all<1>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
-    case 2: select_all<2>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
-    case 4: select_all<4>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
-    case 8: select_all<8>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
-    case 16: select_all<16>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
-    default: select_all<32>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel, status, table); break;
+    case 1: select_all<1>(sc_ws, S, E, K, topp, norm_topk, routed_scale, shared, idx, w, n_sel, status, table); break;
+    case 2: select_all<2>(sc_ws, S, E, K, topp, norm_topk, routed_scale, shared, idx, w, n_sel, status, table); break;
+    case 4: select_all<4>(sc_ws, S, E, K, topp, norm_topk, routed_scale, shared, idx, w, n_sel, status, table); break;
+    case 8: select_all<8>(sc_ws, S, E, K, topp, norm_topk, routed_scale, shared, idx, w, n_sel, status, table); break;
+    case 16: select_all<16>(sc_ws, S, E, K, topp, norm_topk, routed_scale, shared, idx, w, n_sel, status, table); break;
+    default: select_all<32>(sc_ws, S, E, K, topp, norm_topk, routed_scale, shared, idx, w, n_sel, status, table); break;
   }
   __syncthreads();
   if (tid == 0) atomicExch(arrivals, 0u);
@@ -294,20 +300,20 @@ __device__ __forceinline__ void router_body(const void* __restrict__ x, int x_dt
 template <bool VEC4>
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(
     const void* __restrict__ x, int x_dtype, int S, int D, const float* __restrict__ Wr,
-    const float* __restrict__ bias, int E, int K, float topp, int norm_topk, float routed_scale,
+    const float* __restrict__ bias, int E, int K, float topp, int norm_topk, float routed_scale, int shared,
     float2* __restrict__ sc_ws, int32_t* __restrict__ idx, float* __restrict__ w,
     int32_t* __restrict__ n_sel, int* __restrict__ status, int epl, const ExpertDesc* table) {
-  router_body<VEC4>(x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk, routed_scale, sc_ws, idx, w, n_sel, status,
+  router_body<VEC4>(x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk, routed_scale, shared, sc_ws, idx, w, n_sel, status,
                     reinterpret_cast<unsigned*>(status + 1), epl, table);
 }
 
 template <bool VEC4>
 __global__ void __launch_bounds__(kRouterThreads) router_fixed_kernel(
     const void* __restrict__ x, int x_dtype, int S, int D, const float* __restrict__ Wr,
-    const float* __restrict__ bias, int E, int K, float topp, int norm_topk, float routed_scale,
+    const float* __restrict__ bias, int E, int K, float topp, int norm_topk, float routed_scale, int shared,
     float2* __restrict__ sc_ws, int32_t* __restrict__ idx, float* __restrict__ w,
     int32_t* __restrict__ n_sel, int* __restrict__ status, unsigned* arrivals, int epl, const ExpertDesc* table) {
-  router_body<VEC4>(x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk, routed_scale, sc_ws, idx, w, n_sel, status,
+  router_body<VEC4>(x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk, routed_scale, shared, sc_ws, idx, w, n_sel, status,
                     arrivals, epl, table);
 }
 
@@ -393,18 +399,19 @@ __global__ void router_finish_kernel(const float* __restrict__ part, int S, int 
 
 template <int EPL>
 __global__ void router_select_kernel(const float2* sc, int S, int E, int K, float topp, int norm_topk,
-                                     float routed_scale, int32_t* idx, float* w, int32_t* n_sel, int* err,
+                                     float routed_scale, int shared, int32_t* idx, float* w, int32_t* n_sel, int* err,
                                      const ExpertDesc* table) {
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= S) return;  // uniform per warp
-  select_token_any<EPL>(sc + (size_t)t * E, E, K, topp, norm_topk, routed_scale, idx + (size_t)t * K,
-                        w + (size_t)t * K, n_sel ? n_sel + t : nullptr, err, table);
+  const int slots = K + (shared >= 0);  // output slots per token
+  select_token_any<EPL>(sc + (size_t)t * E, E, K, topp, norm_topk, routed_scale, shared, idx + (size_t)t * slots,
+                        w + (size_t)t * slots, n_sel ? n_sel + t : nullptr, err, table);
 }
 
 // sc_ws: S E (score, choice) pairs; part: kRSplit S E floats
 static int launch_router_batched(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr,
                                  const float* bias, int E, int K, float topp, int norm_topk, float routed_scale,
-                                 int32_t* idx, float* w, int32_t* n_sel, float2* sc_ws, float* part) {
+                                 int shared, int32_t* idx, float* w, int32_t* n_sel, float2* sc_ws, float* part) {
   const ExpertDesc* table = ctx->table_count > 0 ? ctx->d_table : nullptr;
   ProfScope prof(ctx, COLI_KERNEL_ROUTER);
   router_gemm_kernel<<<dim3((E + kRT - 1) / kRT, (S + kRT - 1) / kRT, kRSplit), 256, 0, ctx->stream>>>(x, x_dtype, S, D,
@@ -419,8 +426,8 @@ static int launch_router_batched(coli_ctx* ctx, const void* x, int x_dtype, int 
   switch (epl) {
 #define COLI_SELECT_CASE(N)                                                                                        \
   case N:                                                                                                          \
-    router_select_kernel<N><<<sg, 256, 0, ctx->stream>>>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w,   \
-                                                         n_sel, ctx->d_status, table);                            \
+    router_select_kernel<N><<<sg, 256, 0, ctx->stream>>>(sc_ws, S, E, K, topp, norm_topk, routed_scale, shared,   \
+                                                         idx, w, n_sel, ctx->d_status, table);                    \
     break;
     COLI_SELECT_CASE(1)
     COLI_SELECT_CASE(2)
@@ -429,8 +436,8 @@ static int launch_router_batched(coli_ctx* ctx, const void* x, int x_dtype, int 
     COLI_SELECT_CASE(16)
     COLI_SELECT_CASE(32)
     default:  // more than 1024 experts
-      router_select_kernel<0><<<sg, 256, 0, ctx->stream>>>(sc_ws, S, E, K, topp, norm_topk, routed_scale, idx, w, n_sel,
-                                                            ctx->d_status, table);
+      router_select_kernel<0><<<sg, 256, 0, ctx->stream>>>(sc_ws, S, E, K, topp, norm_topk, routed_scale, shared, idx, w,
+                                                            n_sel, ctx->d_status, table);
 #undef COLI_SELECT_CASE
   }
   cudaError_t e = cudaGetLastError();
@@ -439,13 +446,13 @@ static int launch_router_batched(coli_ctx* ctx, const void* x, int x_dtype, int 
 }
 
 int launch_router(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr, const float* bias,
-                  int E, int K, float topp, int norm_topk, float routed_scale, int32_t* idx, float* w,
+                  int E, int K, float topp, int norm_topk, float routed_scale, int shared, int32_t* idx, float* w,
                   int32_t* n_sel) {
   if (S >= kBatchedS || E > kDecodeMaxE) {
     const size_t sc_bytes = align_up((size_t)S * E * sizeof(float2), 256);
     int rc = ensure_workspace(ctx, sc_bytes + (size_t)kRSplit * S * E * sizeof(float));
     if (rc != COLI_OK) return rc;
-    return launch_router_batched(ctx, x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk, routed_scale, idx, w, n_sel,
+    return launch_router_batched(ctx, x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk, routed_scale, shared, idx, w, n_sel,
                                  reinterpret_cast<float2*>(ctx->ws.base),
                                  reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ctx->ws.base) + sc_bytes));
   }
@@ -470,9 +477,9 @@ int launch_router(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const
   cfg.numAttrs = 1;
   const void* xp = x;
   cudaError_t le = vec4 ? cudaLaunchKernelEx(&cfg, router_kernel<true>, xp, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk,
-                                             routed_scale, sc_ws, idx, w, n_sel, ctx->d_status, epl, table)
+                                             routed_scale, shared, sc_ws, idx, w, n_sel, ctx->d_status, epl, table)
                         : cudaLaunchKernelEx(&cfg, router_kernel<false>, xp, x_dtype, S, D, Wr, bias, E, K, topp,
-                                             norm_topk, routed_scale, sc_ws, idx, w, n_sel, ctx->d_status, epl, table);
+                                             norm_topk, routed_scale, shared, sc_ws, idx, w, n_sel, ctx->d_status, epl, table);
   if (le != cudaSuccess) return cuda_fail(ctx, le, "router launch");
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(ctx, e, "router launch");
@@ -507,7 +514,7 @@ static unsigned char* g_fixed_addr[kFixedMaxDevices];  // device address of g_ro
 
 int launch_router_noalloc(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr,
                           const float* bias, int E, int K, float topp, int norm_topk, float routed_scale,
-                          int32_t* idx, float* w, int32_t* n_sel) {
+                          int shared, int32_t* idx, float* w, int32_t* n_sel) {
   if ((long long)S * E > kFixedRouterCells)
     return fail(ctx, COLI_E_INVAL,
                 "router_select_noalloc: S * E = " + std::to_string((long long)S * E) + " exceeds the fixed scratch limit " +
@@ -529,7 +536,7 @@ int launch_router_noalloc(coli_ctx* ctx, const void* x, int x_dtype, int S, int 
   unsigned* arrivals = reinterpret_cast<unsigned*>(base);
   float2* sc_ws = reinterpret_cast<float2*>(base + kFixedPairsOff);
   if (S >= kBatchedS || E > kDecodeMaxE)  // the many-token path, as coli_router_select takes it (no arrival counter)
-    return launch_router_batched(ctx, x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk, routed_scale, idx, w, n_sel,
+    return launch_router_batched(ctx, x, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk, routed_scale, shared, idx, w, n_sel,
                                  sc_ws, reinterpret_cast<float*>(base + kFixedPartOff));
   cudaError_t e = cudaMemsetAsync(arrivals, 0, sizeof(unsigned), ctx->stream);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "router_select_noalloc: clear counter");
@@ -550,9 +557,9 @@ int launch_router_noalloc(coli_ctx* ctx, const void* x, int x_dtype, int S, int 
   cfg.numAttrs = 1;
   const void* xp = x;
   e = vec4 ? cudaLaunchKernelEx(&cfg, router_fixed_kernel<true>, xp, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk,
-                                routed_scale, sc_ws, idx, w, n_sel, ctx->d_status, arrivals, epl, table)
+                                routed_scale, shared, sc_ws, idx, w, n_sel, ctx->d_status, arrivals, epl, table)
            : cudaLaunchKernelEx(&cfg, router_fixed_kernel<false>, xp, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk,
-                                routed_scale, sc_ws, idx, w, n_sel, ctx->d_status, arrivals, epl, table);
+                                routed_scale, shared, sc_ws, idx, w, n_sel, ctx->d_status, arrivals, epl, table);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "router_select_noalloc launch");
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(ctx, e, "router_select_noalloc launch");

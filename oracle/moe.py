@@ -286,6 +286,25 @@ def w4_linear(x, W: Tensor, resid=None) -> np.ndarray:
     return y if resid is None else np.asarray(resid, dtype=np.float64) + y
 
 
+def append_shared(idx, w, n_sel, shared_id: int):
+    """Routes with the shared expert as one more kept slot of weight 1 right after each token's
+    kept slots: idx, w [S x (K+1)] and n_sel + 1; the slots after it hold -1 and 0 ([attn], [pipe];
+    the placement and the unscaled weight 1 are our reading, see moe_block_with_shared)."""
+    idx = np.atleast_2d(np.asarray(idx, np.int32))
+    w = np.atleast_2d(np.asarray(w, np.float32))
+    S, K = idx.shape
+    n_sel = np.full(S, K, np.int32) if n_sel is None else np.asarray(n_sel, np.int32)
+    idx2 = np.full((S, K + 1), -1, np.int32)
+    w2 = np.zeros((S, K + 1), np.float32)
+    for t in range(S):
+        m = int(n_sel[t])
+        idx2[t, :m] = idx[t, :m]
+        w2[t, :m] = w[t, :m]
+        idx2[t, m] = shared_id
+        w2[t, m] = 1.0
+    return idx2, w2, n_sel + 1
+
+
 def moe_block_with_shared(x, experts, idx, w, n_sel, shared, resid=None) -> np.ndarray:
     """y[t] = resid[t] + (routed[t] + E_shared(x[t])), float64.
 

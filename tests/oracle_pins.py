@@ -370,4 +370,14 @@ def pin_shared_expert_bruteforce(o):
         assert np.allclose(y0[t], sh, rtol=1e-12, atol=1e-12), t  # no routed slot: the shared expert alone
 
 
+def pin_append_shared_worked(o):
+    """Hand-written rows: the shared slot lands right after the kept slots with weight 1."""
+    idx = np.array([[4, 2, -1], [7, 1, 5]], np.int32)
+    w = np.array([[0.75, 0.25, 0.0], [0.5, 0.3, 0.2]], np.float32)
+    i2, w2, n2 = o.append_shared(idx, w, np.array([2, 3], np.int32), 9)
+    assert i2.tolist() == [[4, 2, 9, -1], [7, 1, 5, 9]]
+    assert w2.tolist() == [[0.75, 0.25, 1.0, 0.0], [0.5, 0.30000001192092896, 0.20000000298023224, 1.0]]
+    assert n2.tolist() == [3, 4]
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

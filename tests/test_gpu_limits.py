@@ -5,7 +5,8 @@
 - I = 32768 (COLI_MAX_DIM): 1024 threads per down row, the route-parallel down kernel.
 - S = COLI_MAX_GROUP_TOKENS (1024) tokens on the GEMV path.
 - K = E = 32 (COLI_MAX_K): every expert chosen by every token.
-- Down kernels whose block (K ceil(I/1024) 32 threads) is smaller than a 64-row segment or its row-scale cells.
+- Down kernels whose block (K ceil(I/1024) 32 threads) is smaller than a 64-row segment or its row-scale cells,
+  and blocks of 576 and 768 threads (9 and 12 slots).
 - bf16 rows that are not 16-byte aligned, and the tensor-core path at D = 8192 (checked with its tolerance).
 """
 import pytest
@@ -35,6 +36,9 @@ LIMITS = [
     # kernel's block is smaller than a segment's rows (and its row-scale cells)
     LayerConfig("K1-D6144-I128", D=6144, I=128, E=4, K=1),
     LayerConfig("K4-D6144-I1024", D=6144, I=1024, E=8, K=4, gs="mixed:64"),
+    # 9 and 12 slots of 64 threads: the 640- and 768-thread down kernels (a shared expert after 8 or 11 routed)
+    LayerConfig("K9-I2048", D=256, I=2048, E=16, K=9),
+    LayerConfig("K12-I2048", D=320, I=2048, E=16, K=12, gs="mixed:64"),
     # bf16 rows of 200 columns (400 bytes: not 16-byte aligned after row 0), one and several tokens
     LayerConfig("bf16-D200-S1", D=200, I=136, E=12, K=3, x_dtype="bf16"),
     LayerConfig("bf16-D200-S3", D=200, I=136, E=12, K=3, S=3, x_dtype="bf16"),

@@ -5,8 +5,11 @@
   per CTA and token switches inside a segment), at the 1024-thread width and at 6144 x 6144.
 - y written in place over the residual; argument errors leave the context usable.
 - The shared expert, commit "CUDA batch MLA attention, ..., W4A16 kernels": an always-chosen expert
-  of weight 1, registered outside the router's ids and issued as its own group next to the routed
-  group ([resid] issue/take), against the oracle's routed + shared block.
+  of weight 1, registered outside the router's ids. Two ways: the router appends it after each
+  token's kept slots (coli_router_select_shared, checked slot for slot against the oracle's
+  append_shared of the plain router's output) and one coli_expert_group call runs K + 1 slots; or
+  it is issued as its own group next to the routed group ([resid] issue/take). Both against the
+  oracle's routed + shared block.
 """
 import ctypes
 
@@ -113,6 +116,8 @@ def test_linear_in_place_and_errors(ctx):
 @pytest.mark.parametrize("cfg", [
     LayerConfig("shared-S1", D=512, I=256, E=16, K=4, routed_scale=2.5),
     LayerConfig("shared-S4-g64-bf16", D=512, I=320, E=16, K=4, S=4, gs=64, topp=0.9, x_dtype="bf16"),
+    # 32 tokens x 5 slots over 16 experts: the batched router and the tensor-core expert path
+    LayerConfig("shared-S32-tc", D=256, I=128, E=16, K=4, S=32, gs=64, x_dtype="bf16", zipf=True, topp=0.8),
 ], ids=lambda c: c.name)
 def test_shared_expert_layer(ctx, cfg):
     layer = DeviceLayer(ctx, cfg)
@@ -141,7 +146,22 @@ def test_shared_expert_layer(ctx, cfg):
         shared = oracle_experts(cfg, [e_sh])[e_sh]
         ref = O.moe_block_with_shared(xw, experts, idx, w, n, shared, rw)
         rtol, atol = (BF16_RTOL, bf16_atol(ref)) if cfg.x_dtype == "bf16" else (F32_RTOL, f32_atol(ref))
+        if cfg.name.endswith("-tc"):  # groups with many rows per expert may run on the tensor cores
+            from test_gpu_prefill import TC_RTOL, tc_atol
+            rtol, atol = TC_RTOL, tc_atol(ref)
         print(cfg.name, assert_close(to_np(y), ref, rtol, atol, cfg.name))
+        # the router appends the shared slot; one grouped call with K + 1 slots
+        i2 = torch.empty(cfg.S, cfg.K + 1, dtype=torch.int32, device="cuda")
+        w2 = torch.empty(cfg.S, cfg.K + 1, device="cuda")
+        n2 = torch.empty(cfg.S, dtype=torch.int32, device="cuda")
+        B.coli_router_select_shared(ctx, xt, layer.Wr, layer.bias, cfg.K, cfg.topp, cfg.norm_topk, cfg.routed_scale,
+                                    e_sh, i2, w2, n2)
+        ia, wa, na = O.append_shared(idx, w, n, e_sh)
+        assert np.array_equal(to_np(i2), ia) and np.array_equal(to_np(w2), wa) and np.array_equal(to_np(n2), na)
+        y2 = torch.empty_like(xt)
+        B.coli_expert_group(ctx, xt, i2, w2, n2, cfg.K + 1, rt, y2)
+        assert B.coli_check_error(ctx) == 0, B.coli_last_error(ctx)
+        print(cfg.name, "one call", assert_close(to_np(y2), ref, rtol, atol, cfg.name + " one call"))
     finally:
         B.coli_expert_table_set(ctx, e_sh, 0, 0, 0)
         for h in hs:

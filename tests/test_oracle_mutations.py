@@ -178,10 +178,24 @@ def shared_weighted_like_slot0(o):
     o.moe_block_with_shared = bad
 
 
+def shared_slot_at_row_end(o):
+    orig = o.append_shared
+
+    def bad(idx, w, n_sel, shared_id):
+        i2, w2, n2 = orig(idx, w, n_sel, shared_id)
+        for t in range(i2.shape[0]):
+            m = int(n2[t]) - 1
+            i2[t, m], w2[t, m] = -1, 0.0
+            i2[t, -1], w2[t, -1] = shared_id, 1.0
+        return i2, w2, n2
+    o.append_shared = bad
+
+
 MUTATIONS = [swap_nibble_order, offset_seven, tie_to_higher_index, weights_from_choice, scale_before_norm,
              topp_drops_reaching_slot, norm_over_all_slots, sigmoid_sign, silu_on_up, drop_residual,
              group_scales_column_major, group_index_by_byte, down_transposed_roles, gate_up_swapped,
-             linear_drops_residual, linear_reads_columns_reversed, shared_weighted_like_slot0]
+             linear_drops_residual, linear_reads_columns_reversed, shared_weighted_like_slot0,
+             shared_slot_at_row_end]
 
 
 @pytest.mark.parametrize("mutate", MUTATIONS, ids=[m.__name__ for m in MUTATIONS])
