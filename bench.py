@@ -38,7 +38,7 @@ def parse():
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill, shared-expert and dense-projection figures")
-    ap.add_argument("--cpu-worker", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-steps", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -271,33 +271,53 @@ def workload_desc(cfg):
 # CPU oracle leg (reference arm and cpu_baseline): runs in a child process pinned to one thread.
 # ------------------------------------------------------------------------------------------------
 
-def cpu_worker(workload: str, tokens: int):
+def cpu_step_worker(workload: str, steps: int, warmup: int):
+    """The oracle in steps of a bounded sample: step s routes token s (the whole router) and runs ONE of
+    its kept experts (slot s mod n_sel). The per-layer figure is the mean router time plus the mean
+    kept count times the mean expert time."""
     import oracle.moe as O
     from int4_grouped_expert_router_gb300.workload import CONFIGS, host_expert, router_host_inputs
 
     cfg = CONFIGS[workload]
-    t0 = time.perf_counter()
-    for tok in range(tokens):
-        x, Wr, bias, resid = router_host_inputs(cfg, tok)
+    t_router, t_expert, kept, t_step = [], [], [], []
+    for s in range(warmup + steps):
+        x, Wr, bias, resid = router_host_inputs(cfg, s)
+        t0 = time.perf_counter()
         idx, w, n, _ = O.router_select(x, Wr, bias, cfg.K, cfg.topp, cfg.norm_topk, cfg.routed_scale)
-        experts = {}
-        for e in set(int(v) for v in idx.reshape(-1) if v >= 0):
-            experts[e] = tuple(O.Tensor(p, s, r, c, gs) for (p, s, r, c, gs) in host_expert(cfg, e))
-        O.expert_group(x, experts, idx, w, n, resid)
-    dt = time.perf_counter() - t0
-    print(json.dumps({"us_per_layer": dt / tokens * 1e6, "tokens": tokens, "seconds": dt}))
+        t1 = time.perf_counter()
+        k = s % int(n[0])
+        gate, up, down = (O.Tensor(p, sc, r, c, gs) for (p, sc, r, c, gs) in host_expert(cfg, int(idx[0, k])))
+        t2 = time.perf_counter()
+        float(w[0, k]) * O.expert_ffn(x[0], gate, up, down)
+        t3 = time.perf_counter()
+        if s >= warmup:
+            t_router.append(t1 - t0)
+            t_expert.append(t3 - t2)
+            kept.append(int(n[0]))
+            t_step.append((t1 - t0) + (t3 - t2))
+    mr, me, mk = statistics.mean(t_router), statistics.mean(t_expert), statistics.mean(kept)
+    print(json.dumps({"us_per_layer": (mr + mk * me) * 1e6, "steps": steps, "warmup": warmup,
+                      "ms_per_step": statistics.mean(t_step) * 1e3, "router_ms": mr * 1e3, "expert_ms": me * 1e3,
+                      "kept": mk}))
 
 
-def run_cpu_leg(workload: str, tokens: int):
+def run_oracle_steps(workload: str, steps: int, warmup: int):
+    """cpu_step_worker in a fresh single-threaded process (no GPU visible); returns its JSON."""
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", str(tokens), "--workload", workload],
-                       capture_output=True, text=True, env=env, timeout=900)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-steps", str(steps), "--warmup", str(warmup),
+                        "--workload", workload], capture_output=True, text=True, env=env, timeout=3600)
     if r.returncode != 0:
         raise RuntimeError(f"oracle timing failed: {r.stderr[-2000:]}")
     return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def oracle_sample(res, workload):
+    return (f"{res['steps']} steps, each one token of the {workload} layer: the whole router and one of its kept "
+            f"experts in turn (router {res['router_ms']:.1f} ms, expert {res['expert_ms']:.0f} ms, {res['kept']:.1f} "
+            "kept); value = router + kept x expert")
 
 
 def reference_arm(args, rank, world):
@@ -305,18 +325,16 @@ def reference_arm(args, rank, world):
         return 0
     from int4_grouped_expert_router_gb300.workload import CONFIGS
     cfg = CONFIGS[args.workload]
-    per_step_tokens = 1
-    tokens = max(1, (args.steps + args.warmup) * per_step_tokens)
-    tokens = min(tokens, 6)  # bounded sample: a few seconds of single-threaded oracle per token
-    res = run_cpu_leg(args.workload, tokens)
+    res = run_oracle_steps(args.workload, args.steps, args.warmup)
     v = res["us_per_layer"]
     line = {
-        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": res["tokens"],
-        "warmup": 0, "ms_per_step": v / 1000.0, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": res["steps"],
+        "warmup": res["warmup"], "ms_per_step": res["ms_per_step"], "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded SplitMix64; shapes of the pages' GLM-5.2 decode layer)",
         "config": {"workload": workload_desc(cfg)},
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"{res['tokens']} tokens of the {args.workload} layer (router + 8 experts each)"},
+                         "sample": oracle_sample(res, args.workload)},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -573,11 +591,9 @@ def gpu_arm(args, rank, world, local):
     if rank == 0:
         cpu = None
         try:
-            cpu_tokens = 4
-            res = run_cpu_leg(args.workload, cpu_tokens)
+            res = run_oracle_steps(args.workload, 40, 1)  # about 10 s of single-threaded oracle
             cpu = {"value": res["us_per_layer"], "unit": UNIT, "cores": 1, "kind": "oracle",
-                   "sample": f"{res['tokens']} tokens of the {args.workload} layer (router + kept experts), "
-                             f"{res['seconds']:.1f} s single-threaded"}
+                   "sample": oracle_sample(res, args.workload)}
         except Exception as exc:  # the CPU leg must not hide the GPU number
             cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": f"failed: {exc}"[:300]}
         p50 = statistics.median(step_ms) * 1000.0
@@ -631,8 +647,8 @@ def gpu_arm(args, rank, world, local):
 
 def main():
     args = parse()
-    if args.cpu_worker:
-        cpu_worker(args.workload, args.cpu_worker)
+    if args.cpu_steps:
+        cpu_step_worker(args.workload, args.cpu_steps, args.warmup)
         return 0
     rank, world, local = dist_env()
     if args.impl == "reference":
