@@ -229,6 +229,12 @@ int coli_init(coli_ctx** out, int device, void* cuda_stream) {
   if ((e = cudaMalloc(&p, kStatusBytes)) != cudaSuccess) goto fail;
   ctx->d_status = static_cast<int*>(p);
   if ((e = cudaMemset(ctx->d_status, 0, kStatusBytes)) != cudaSuccess) goto fail;
+  {
+    const int32_t route[2] = {0, 0x3f800000};  // expert 0, then the bits of 1.0f
+    if ((e = cudaMalloc(&p, sizeof(route))) != cudaSuccess) goto fail;
+    ctx->d_solo_route = static_cast<int32_t*>(p);
+    if ((e = cudaMemcpy(ctx->d_solo_route, route, sizeof(route), cudaMemcpyHostToDevice)) != cudaSuccess) goto fail;
+  }
   ctx->coop_mode = probe_coop_mode(ctx);
   *out = ctx;
   return COLI_OK;
@@ -245,7 +251,9 @@ void coli_destroy(coli_ctx* ctx) {
   for (auto& t : ctx->tensors) {
     if (t.w) cudaFree(t.w);
     if (t.s) cudaFree(t.s);
+    if (t.d_solo) cudaFree(t.d_solo);
   }
+  if (ctx->d_solo_route) cudaFree(ctx->d_solo_route);
   if (ctx->d_table) cudaFree(ctx->d_table);
   if (ctx->d_status) cudaFree(ctx->d_status);
   if (ctx->ws.base) cudaFree(ctx->ws.base);
@@ -392,6 +400,21 @@ uint64_t coli_expert_upload(coli_ctx* ctx, const uint8_t* packed, const float* s
     cudaFree(ps);
     return 0;
   }
+  {  // a one-entry expert table whose down tensor is this one (coli_w4_linear for one token)
+    ExpertDesc solo{};
+    solo.t[T_DOWN] = t.desc;
+    solo.valid = 1;
+    void* pd = nullptr;
+    if ((e = cudaMalloc(&pd, sizeof(ExpertDesc))) != cudaSuccess ||
+        (e = cudaMemcpy(pd, &solo, sizeof(ExpertDesc), cudaMemcpyHostToDevice)) != cudaSuccess) {
+      if (pd) cudaFree(pd);
+      cudaFree(pw);
+      cudaFree(ps);
+      cuda_fail(ctx, e, "upload: device descriptor");
+      return 0;
+    }
+    t.d_solo = static_cast<ExpertDesc*>(pd);
+  }
   t.live = true;
   ctx->tensors.push_back(t);
   return (uint64_t)ctx->tensors.size();
@@ -417,6 +440,7 @@ int coli_expert_free(coli_ctx* ctx, uint64_t handle) {
   if (e != cudaSuccess) return cuda_fail(ctx, e, "free: stream sync");
   cudaFree(t.w);
   cudaFree(t.s);
+  if (t.d_solo) cudaFree(t.d_solo);
   t = HostTensor{};
   return COLI_OK;
 }
@@ -540,7 +564,8 @@ int coli_w4_linear(coli_ctx* ctx, uint64_t W, const void* x, int x_dtype, int S,
   if (!valid_handle(ctx, W)) return fail(ctx, COLI_E_INVAL, "w4_linear: unknown tensor handle");
   if (injected(ctx)) return COLI_E_INJECTED;
   cudaSetDevice(ctx->device);
-  int rc = launch_linear(ctx, ctx->tensors[W - 1].desc, x, x_dtype, S, resid, y);
+  const HostTensor& t = ctx->tensors[W - 1];
+  int rc = launch_linear(ctx, t.desc, t.d_solo, x, x_dtype, S, resid, y);
   if (rc == COLI_OK) ctx->compute_calls++;
   return rc;
 }

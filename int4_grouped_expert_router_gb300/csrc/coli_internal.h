@@ -77,6 +77,7 @@ struct HostTensor {
   int table_refs = 0;
   bool live = false;
   TensorDesc desc{};  // device view, tensor maps included
+  ExpertDesc* d_solo = nullptr;  // device entry {down = this tensor, valid}: the one-token dense projection
 };
 
 struct Workspace {
@@ -99,6 +100,7 @@ struct coli_ctx {
   std::vector<uint64_t> table_handles;       // 3 per entry
   int table_D = 0, table_I = 0, table_count = 0;
   int* d_status = nullptr;  // kStatusBytes of device status words (see kSyncBase)
+  int32_t* d_solo_route = nullptr;  // device {expert 0} and, after it, {weight 1.0f}: the one-slot route
   // decode (S == 1) expert FFN as one cooperative kernel: COLI_DECODE_FUSED=1 (default 0), and how
   // this device launches it (2: cooperative + programmatic dependent launch, 1: cooperative, 0: no)
   bool decode_fused = false;
@@ -162,7 +164,9 @@ int launch_router_noalloc(coli_ctx* ctx, const void* x, int x_dtype, int S, int 
 int launch_expert_group(coli_ctx* ctx, const void* x, int x_dtype, int S, const int32_t* idx,
                         const float* w, const int32_t* n_sel, int K, const void* resid, void* y, int y_dtype);
 // y [S x O] = resid + W x for S tokens of the uploaded tensor T [O x I] (coli_w4_linear).
-int launch_linear(coli_ctx* ctx, const TensorDesc& T, const void* x, int x_dtype, int S, const void* resid, void* y);
+// S == 1 runs the down kernel on `solo`, a one-entry table whose down tensor is T.
+int launch_linear(coli_ctx* ctx, const TensorDesc& T, const ExpertDesc* solo, const void* x, int x_dtype, int S,
+                  const void* resid, void* y);
 // y [S x D] (dtype) = resid + the n issued partial sums [S x D] f32, added in issue order.
 int launch_take(coli_ctx* ctx, int S, int D, int n, const void* resid, int dtype, void* y);
 // Which cooperative launch forms this device accepts (coli_ctx::coop_mode), found with an empty

@@ -273,6 +273,7 @@ struct GroupParams {
   const void* resid;
   void* y;
   float* h;        // [routes x I]
+  int h_dtype;     // dtype of h (f32; the dense projection passes its activations here)
   float* yr;       // [routes x D] (S > 1)
   int* plan;       // pre[0..S] (written by CTA 0 of the gate/up kernel)
   int* err;
@@ -962,7 +963,7 @@ __global__ void __launch_bounds__(MAXT, 1) down_reduce_kernel(GroupParams P, int
   griddep_wait();  // h is written by the gate/up kernel
   float hv[32];
   Limbs L;
-  load_chunk_f32(P.h, COLI_DTYPE_F32, (size_t)k * P.I, 32 * c, active ? P.I : 0, hv);
+  load_chunk_f32(P.h, P.h_dtype, (size_t)k * P.I, 32 * c, active ? P.I : 0, hv);
   if (!make_limbs(hv, L) && active) set_error(P.err, COLI_E_NONFINITE);
   if (warp_on && lane == 0)  // the rest of the ring once h has arrived (its loads go first)
     for (int s = kDPreStages; s < kDStages; s++) issue_next();
@@ -1003,7 +1004,7 @@ __global__ void __launch_bounds__(MAXT, 1) down_reduce_kernel(GroupParams P, int
 #pragma unroll 1
         for (int u = 0; u < kBoxRows; u++)
           tmp[u] = (ok && active && u < n)
-                       ? chunk_dot_slow(lds128(st + u * lt.rowB + 16 * lane), L, lt, P.h, COLI_DTYPE_F32,
+                       ? chunk_dot_slow(lds128(st + u * lt.rowB + 16 * lane), L, lt, P.h, P.h_dtype,
                                         (size_t)k * P.I, d0 + u, c)
                        : 0.f;
 #pragma unroll
@@ -1417,6 +1418,7 @@ int launch_expert_group(coli_ctx* ctx, const void* x, int x_dtype, int S, const 
   P.resid = resid;
   P.y = y;
   P.h = reinterpret_cast<float*>(ctx->ws.base);
+  P.h_dtype = COLI_DTYPE_F32;
   P.yr = reinterpret_cast<float*>(ctx->ws.base + h_bytes);
   P.plan = reinterpret_cast<int*>(ctx->ws.base + h_bytes + yr_bytes + yp_bytes);
   P.err = ctx->d_status;
@@ -1481,7 +1483,47 @@ int launch_expert_group(coli_ctx* ctx, const void* x, int x_dtype, int S, const 
   return COLI_OK;
 }
 
-int launch_linear(coli_ctx* ctx, const TensorDesc& T, const void* x, int x_dtype, int S, const void* resid, void* y) {
+int launch_linear(coli_ctx* ctx, const TensorDesc& T, const ExpertDesc* solo, const void* x, int x_dtype, int S,
+                  const void* resid, void* y) {
+  const int CI = (T.cols + 31) / 32;
+  const int TPE = (CI + 31) / 32 * 32;
+  if (S == 1 && solo && down_smem_bytes(TPE / 32) <= 220 * 1024) {
+    // one token: the down kernel's per-warp TMA rings over a one-slot route {expert 0 of `solo`, weight 1},
+    // with the activations in place of h
+    GroupParams G{};
+    G.x = x;
+    G.x_dtype = x_dtype;
+    G.y_dtype = x_dtype;
+    G.S = 1;
+    G.D = T.rows;
+    G.I = T.cols;
+    G.K = 1;
+    G.idx = ctx->d_solo_route;
+    G.w = reinterpret_cast<const float*>(ctx->d_solo_route + 1);
+    G.n_sel = nullptr;
+    G.table = solo;
+    G.resid = resid;
+    G.y = y;
+    G.h = const_cast<float*>(static_cast<const float*>(x));
+    G.h_dtype = x_dtype;
+    G.err = ctx->d_status;
+    const size_t smem = down_smem_bytes(TPE / 32);
+    auto kern = TPE <= 256 ? down_reduce_kernel<256> : (TPE <= 512 ? down_reduce_kernel<512> : down_reduce_kernel<1024>);
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+      return cuda_fail(ctx, e, "linear smem attribute");
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, TPE, smem) != cudaSuccess) {
+      (void)cudaGetLastError();
+      occ = 1;
+    }
+    int grid = ctx->num_sms * (occ > 0 ? occ : 1);
+    if (grid > T.rows) grid = T.rows;
+    ProfScope prof(ctx, COLI_KERNEL_LINEAR);
+    e = launch_k(kern, grid, TPE, smem, ctx->stream, false, false, G, TPE);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "linear launch");
+    return COLI_OK;
+  }
   LinearParams P;
   P.x = x;
   P.resid = resid;
@@ -1491,8 +1533,7 @@ int launch_linear(coli_ctx* ctx, const TensorDesc& T, const void* x, int x_dtype
   P.O = T.rows;
   P.I = T.cols;
   P.err = ctx->d_status;
-  const int CI = (T.cols + 31) / 32;
-  const int nt = (CI + 31) / 32 * 32;
+  const int nt = TPE;
   auto kern = nt <= 256 ? linear_kernel<256> : (nt <= 512 ? linear_kernel<512> : linear_kernel<1024>);
   int occ = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, nt, 0) != cudaSuccess) {

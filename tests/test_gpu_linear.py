@@ -1,8 +1,9 @@
 """The dense int4 projection (coli_w4_linear) and a layer with a shared expert, against the oracle.
 
 - coli_w4_linear over every scale layout (per row, chunk groups with a tail, generic even gs), ragged
-  widths, f32 and bf16, with and without a residual, one token and many (several finishing segments
-  per CTA and token switches inside a segment), at the 1024-thread width and at 6144 x 6144.
+  widths, f32 and bf16, with and without a residual, one token (the down kernel's TMA rings) and many
+  (several finishing segments per CTA and token switches inside a segment), at the widest blocks and
+  at 6144 x 6144.
 - y written in place over the residual; argument errors leave the context usable.
 - The shared expert, commit "CUDA batch MLA attention, ..., W4A16 kernels": an always-chosen expert
   of weight 1, registered outside the router's ids. Two ways: the router appends it after each
@@ -58,6 +59,12 @@ CASES = [
     ("segments", 4096, 256, 0, 64, "f32", True),
     ("wide-1024-threads", 96, 20000, 128, 2, "f32", True),
     ("square-6144", 6144, 6144, 0, 1, "f32", True),
+    # one token runs on the down kernel's TMA rings: every scale layout, bf16 activations, wide rows
+    ("s1-generic-gs6-bf16", 50, 96, 6, 1, "bf16", True),
+    ("s1-g64-tail-bf16", 203, 200, 64, 1, "bf16", False),
+    ("s1-g32-f32", 1000, 1000, 32, 1, "f32", True),
+    ("s1-wide-640-threads", 96, 20000, 128, 1, "f32", True),
+    ("s1-bf16-6144", 6144, 6144, 0, 1, "bf16", True),
 ]
 
 
