@@ -254,6 +254,29 @@ COLI_API int coli_expert_group_take(coli_ctx *ctx, const void *resid, void *y);
 COLI_API int coli_w4_linear(coli_ctx *ctx, uint64_t W, const void *x, int x_dtype, int S, const void *resid,
                             void *y);
 
+/*
+ * Expert parallelism over `world` GPUs, the device steps ([resid] reduces the device groups' partial
+ * sums in a fixed order; [pipe] spreads the expert groups over the cards). Expert e belongs to rank
+ * e mod world. Each rank routes every token itself (coli_router_select is deterministic), keeps its
+ * own routes with coli_routes_shard, issues them (coli_expert_group_issue) and takes the partial sum
+ * without a residual (coli_expert_group_take with resid NULL, f32 activations). The ranks' partial
+ * rows are then gathered (a collective of the caller's choice) and summed here in rank order.
+ *
+ * coli_routes_shard: idx_out, w_out [S x K], n_out [S]: token t's kept slots (k < n_sel[t]; all K if
+ * n_sel is NULL) whose expert e satisfies e mod world == rank, moved to the front in slot order; the
+ * other slots get idx -1 and w 0. A kept slot with e < 0 or e >= COLI_MAX_EXPERTS belongs to no rank
+ * and sets COLI_E_ROUTE in the device error word. 0 <= rank < world; device pointers.
+ *
+ * coli_partials_reduce: y = resid + (((p_0 + p_1) + p_2) + ... + p_{n-1}) element by element in
+ * binary32, with parts = n consecutive [S x D] f32 partials (device) and resid (NULL: none), y in
+ * dtype ([S x D], device). Against one GPU the result differs only in the grouping of the slots'
+ * terms. Profiled as COLI_KERNEL_COMBINE.
+ */
+COLI_API int coli_routes_shard(coli_ctx *ctx, const int32_t *idx, const float *w, const int32_t *n_sel, int S,
+                               int K, int rank, int world, int32_t *idx_out, float *w_out, int32_t *n_out);
+COLI_API int coli_partials_reduce(coli_ctx *ctx, const float *parts, int n, int S, int D, const void *resid,
+                                  int dtype, void *y);
+
 #ifdef __cplusplus
 }
 #endif

@@ -59,6 +59,8 @@ SIGNATURES = {
     "coli_router_select": (_I, [_P, _P, _I, _I, _I, _P, _P, _I, _I, _F, _I, _F, _P, _P, _P]),
     "coli_router_select_noalloc": (_I, [_P, _P, _I, _I, _I, _P, _P, _I, _I, _F, _I, _F, _P, _P, _P]),
     "coli_router_select_shared": (_I, [_P, _P, _I, _I, _I, _P, _P, _I, _I, _F, _I, _F, _I, _P, _P, _P]),
+    "coli_routes_shard": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
+    "coli_partials_reduce": (_I, [_P, _P, _I, _I, _I, _P, _I, _P]),
     "coli_expert_upload": (_U64, [_P, _P, _P, _I, _I, _I]),
     "coli_expert_free": (_I, [_P, _U64]),
     "coli_tensor_shape": (_I, [_P, _U64, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
@@ -297,6 +299,35 @@ def coli_expert_group_take(ctx, resid, y):
     if resid is not None and resid.shape != y.shape:
         raise ValueError("expert_group_take: inconsistent shapes")
     return _check(ctx, library().coli_expert_group_take(ctx, _ptr(resid), _ptr(y)), "coli_expert_group_take")
+
+
+def coli_routes_shard(ctx, idx, w, n_sel, rank, world, idx_out, w_out, n_out):
+    """This rank's kept routes (expert e mod world == rank) moved to the front of each row."""
+    S, K = idx.shape
+    for t, name, dt in ((idx, "idx", torch.int32), (w, "w", torch.float32), (idx_out, "idx_out", torch.int32),
+                        (w_out, "w_out", torch.float32)):
+        _dev(t, dt, name)
+        if tuple(t.shape) != (S, K):
+            raise ValueError(f"routes_shard: {name} must be [S x K]")
+    _dev(n_sel, torch.int32, "n_sel")
+    _dev(n_out, torch.int32, "n_out")
+    if n_out.numel() != S or (n_sel is not None and n_sel.numel() != S):
+        raise ValueError("routes_shard: n_sel and n_out must have S entries")
+    rc = library().coli_routes_shard(ctx, _ptr(idx), _ptr(w), _ptr(n_sel), S, K, rank, world, _ptr(idx_out),
+                                     _ptr(w_out), _ptr(n_out))
+    return _check(ctx, rc, "coli_routes_shard")
+
+
+def coli_partials_reduce(ctx, parts, resid, y):
+    """y = resid + (((p_0 + p_1) + ...) in order) for parts [n x S x D] f32; resid may be None."""
+    _dev(parts, torch.float32, "parts")
+    _dev(y, name="y")
+    _dev(resid, y.dtype, "resid")
+    n, S, D = parts.shape
+    if tuple(y.shape) != (S, D) or (resid is not None and resid.shape != y.shape):
+        raise ValueError("partials_reduce: y and resid must be [S x D]")
+    rc = library().coli_partials_reduce(ctx, _ptr(parts), n, S, D, _ptr(resid), act_dtype(y), _ptr(y))
+    return _check(ctx, rc, "coli_partials_reduce")
 
 
 def coli_profile_enable(ctx, on):

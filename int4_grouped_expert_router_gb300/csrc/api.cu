@@ -6,6 +6,7 @@
 #include <string>
 
 #include "coli_internal.h"
+#include "ep.h"
 
 namespace coli {
 
@@ -566,6 +567,33 @@ int coli_w4_linear(coli_ctx* ctx, uint64_t W, const void* x, int x_dtype, int S,
   cudaSetDevice(ctx->device);
   const HostTensor& t = ctx->tensors[W - 1];
   int rc = launch_linear(ctx, t.desc, t.d_solo, x, x_dtype, S, resid, y);
+  if (rc == COLI_OK) ctx->compute_calls++;
+  return rc;
+}
+
+int coli_routes_shard(coli_ctx* ctx, const int32_t* idx, const float* w, const int32_t* n_sel, int S, int K, int rank,
+                      int world, int32_t* idx_out, float* w_out, int32_t* n_out) {
+  if (!ctx) return COLI_E_INVAL;
+  if (!idx || !w || !idx_out || !w_out || !n_out) return fail(ctx, COLI_E_INVAL, "routes_shard: NULL pointer");
+  if (S < 1 || S > COLI_MAX_TOKENS || K < 1 || K > COLI_MAX_K || world < 1 || rank < 0 || rank >= world)
+    return fail(ctx, COLI_E_INVAL, "routes_shard: size, rank or world out of range");
+  if (injected(ctx)) return COLI_E_INJECTED;
+  cudaSetDevice(ctx->device);
+  int rc = launch_routes_shard(ctx, idx, w, n_sel, S, K, rank, world, idx_out, w_out, n_out);
+  if (rc == COLI_OK) ctx->compute_calls++;
+  return rc;
+}
+
+int coli_partials_reduce(coli_ctx* ctx, const float* parts, int n, int S, int D, const void* resid, int dtype,
+                         void* y) {
+  if (!ctx) return COLI_E_INVAL;
+  if (!parts || !y) return fail(ctx, COLI_E_INVAL, "partials_reduce: NULL pointer");
+  if (dtype != COLI_DTYPE_F32 && dtype != COLI_DTYPE_BF16) return fail(ctx, COLI_E_INVAL, "partials_reduce: dtype");
+  if (n < 1 || S < 1 || S > COLI_MAX_TOKENS || D < 1 || D > COLI_MAX_DIM)
+    return fail(ctx, COLI_E_INVAL, "partials_reduce: size out of range");
+  if (injected(ctx)) return COLI_E_INJECTED;
+  cudaSetDevice(ctx->device);
+  int rc = launch_partials_reduce(ctx, parts, n, S, D, resid, dtype, y);
   if (rc == COLI_OK) ctx->compute_calls++;
   return rc;
 }

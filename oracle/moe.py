@@ -320,3 +320,44 @@ def moe_block_with_shared(x, experts, idx, w, n_sel, shared, resid=None) -> np.n
     sh = np.stack([expert_ffn(x[t], gate, up, down) for t in range(x.shape[0])])
     y = routed + sh
     return y if resid is None else np.asarray(resid, dtype=np.float64) + y
+
+
+# ------------------------------------------------------------------------------------------
+# Expert parallelism over ranks [resid], [pipe]
+# ------------------------------------------------------------------------------------------
+
+def expert_owner(e: int, world: int) -> int:
+    """Rank that holds expert e. Reading: the pages spread expert groups over the cards without a
+    rule; we take e mod world (experts of neighbouring ids land on different ranks)."""
+    return int(e) % int(world)
+
+
+def shard_routes(idx, w, n_sel, rank: int, world: int):
+    """Rank ``rank``'s share of the routes: each token's kept slots whose expert it owns, moved to
+    the front in slot order; idx, w [S x K] (the rest -1 and 0) and the count n [S]."""
+    idx = np.atleast_2d(np.asarray(idx, np.int32))
+    w = np.atleast_2d(np.asarray(w, np.float32))
+    S, K = idx.shape
+    n_sel = np.full(S, K, np.int32) if n_sel is None else np.asarray(n_sel, np.int32)
+    idx2 = np.full((S, K), -1, np.int32)
+    w2 = np.zeros((S, K), np.float32)
+    n2 = np.zeros(S, np.int32)
+    for t in range(S):
+        j = 0
+        for k in range(int(n_sel[t])):
+            if idx[t, k] >= 0 and expert_owner(idx[t, k], world) == rank:
+                idx2[t, j], w2[t, j] = idx[t, k], w[t, k]
+                j += 1
+        n2[t] = j
+    return idx2, w2, n2
+
+
+def ep_layer(x, experts, idx, w, n_sel, world: int, resid=None) -> np.ndarray:
+    """The expert-parallel block: every rank's partial sum over its own routes (expert_group with
+    no residual), added in rank order, then the residual ([resid]: a fixed-order reduce of the
+    device groups' partial sums). Equal to expert_group up to the grouping of the terms."""
+    parts = [expert_group(x, experts, *shard_routes(idx, w, n_sel, r, world), None) for r in range(world)]
+    acc = parts[0]
+    for p in parts[1:]:
+        acc = acc + p
+    return acc if resid is None else np.asarray(resid, dtype=np.float64) + acc

@@ -380,4 +380,45 @@ def pin_append_shared_worked(o):
     assert n2.tolist() == [3, 4]
 
 
+def pin_shard_routes_worked(o):
+    """Hand-written rows over 2 and 3 ranks: owned kept slots first, in slot order; the rest -1/0."""
+    idx = np.array([[4, 7, 2, 9], [3, 6, 1, -1]], np.int32)
+    w = np.array([[0.4, 0.3, 0.2, 0.1], [0.5, 0.25, 0.25, 0.0]], np.float32)
+    n = np.array([3, 3], np.int32)
+    i0, w0, n0 = o.shard_routes(idx, w, n, 0, 2)
+    i1, w1, n1 = o.shard_routes(idx, w, n, 1, 2)
+    assert i0.tolist() == [[4, 2, -1, -1], [6, -1, -1, -1]] and n0.tolist() == [2, 1]
+    assert i1.tolist() == [[7, -1, -1, -1], [3, 1, -1, -1]] and n1.tolist() == [1, 2]
+    assert w0[0].tolist()[:2] == [np.float32(0.4), np.float32(0.2)] and w1[1].tolist()[:2] == [0.5, 0.25]
+    i2, _, n2 = o.shard_routes(idx, w, None, 2, 3)  # all four slots kept; 2 and 9 are not owned by rank 2
+    assert i2.tolist() == [[2, -1, -1, -1], [-1, -1, -1, -1]] and n2.tolist() == [1, 0]
+
+
+def pin_ep_layer_partition(o):
+    """Every kept slot lands on exactly one rank; the rank-order sum equals the one-rank block up to
+    rounding, and one rank is the one-rank block exactly."""
+    D, I, E, K, S = 8, 6, 7, 3, 4
+    experts = {}
+    for e in range(E):
+        trip = []
+        for which, (r, c) in zip("gud", ((I, D), (I, D), (D, I))):
+            p, sc = synth.expert_tensor(synth.stream_seed(90, e, which), r, c, 0)
+            trip.append(o.Tensor(p, sc, r, c, 0))
+        experts[e] = tuple(trip)
+    x = synth.normal(synth.stream_seed(91, "x"), S * D).reshape(S, D)
+    resid = synth.normal(synth.stream_seed(91, "r"), S * D).reshape(S, D)
+    idx = np.array([[6, 1, 3], [0, 5, 2], [4, 4, 1], [2, 3, -1]], np.int32)
+    w = np.array([[0.5, 0.3, 0.2], [0.6, 0.3, 0.1], [0.7, 0.2, 0.1], [0.75, 0.25, 0.0]], np.float32)
+    n = np.array([3, 2, 3, 2], np.int32)
+    ref = o.expert_group(x, experts, idx, w, n, resid)
+    assert np.array_equal(o.ep_layer(x, experts, idx, w, n, 1, resid), ref)
+    for world in (2, 3, 5):
+        shards = [o.shard_routes(idx, w, n, r, world) for r in range(world)]
+        for t in range(S):
+            owned = sorted((int(i), float(v)) for (si, sw, sn) in shards for i, v in zip(si[t, :sn[t]], sw[t, :sn[t]]))
+            assert owned == sorted((int(i), float(v)) for i, v in zip(idx[t, :n[t]], w[t, :n[t]])), (world, t)
+        got = o.ep_layer(x, experts, idx, w, n, world, resid)
+        assert np.allclose(got, ref, rtol=1e-12, atol=1e-12), world
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -191,11 +191,24 @@ def shared_slot_at_row_end(o):
     o.append_shared = bad
 
 
+def shard_by_block_not_modulo(o):
+    o.expert_owner = lambda e, world: min(int(e) * int(world) // 8, int(world) - 1)
+
+
+def ep_drops_last_rank(o):
+    def bad(x, experts, idx, w, n_sel, world, resid=None):
+        acc = 0.0
+        for r in range(max(1, world - 1)):
+            acc = acc + o.expert_group(x, experts, *o.shard_routes(idx, w, n_sel, r, world), None)
+        return acc if resid is None else np.asarray(resid, np.float64) + acc
+    o.ep_layer = bad
+
+
 MUTATIONS = [swap_nibble_order, offset_seven, tie_to_higher_index, weights_from_choice, scale_before_norm,
              topp_drops_reaching_slot, norm_over_all_slots, sigmoid_sign, silu_on_up, drop_residual,
              group_scales_column_major, group_index_by_byte, down_transposed_roles, gate_up_swapped,
              linear_drops_residual, linear_reads_columns_reversed, shared_weighted_like_slot0,
-             shared_slot_at_row_end]
+             shared_slot_at_row_end, shard_by_block_not_modulo, ep_drops_last_rank]
 
 
 @pytest.mark.parametrize("mutate", MUTATIONS, ids=[m.__name__ for m in MUTATIONS])
