@@ -37,7 +37,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--no-clocks", action="store_true")
-    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill, shared-expert and dense-projection figures")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill, shared-expert, dense-projection and compressed-tier figures")
     ap.add_argument("--cpu-steps", type=int, default=0, help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -99,6 +99,36 @@ def linear_leg(ctx, stream, flush, D, steps=20, warmup=3):
     return {"workload": f"dense int4 projection O={D} I={D} gs=0, S=1, f32, residual", "us": us, "steps": steps,
             "launch": "one C-ABI call per step", "l2": "flushed between steps", "bytes": nbytes, "hbm_gbs": gbs,
             "hbm_frac": gbs / hpeak, "peak_kind": f"{hkind} hbm_gbs"}
+
+
+def ans_leg(ctx, stream, flush, nbytes, steps=10, warmup=3):
+    """The compressed tier's decoder: one expert's gate + up packed bytes (quantised-weight-like nibbles)
+    decoded from device-resident 4 KiB blocks, event-timed with a cold L2; raw bytes out per second."""
+    import numpy as np
+    import torch
+
+    from int4_grouped_expert_router_gb300 import binding as B
+    from int4_grouped_expert_router_gb300 import synth
+
+    data = synth.gaussian_nibble_bytes(synth.stream_seed(903, "tier"), nbytes, 2.5)
+    h = B.coli_ans_upload(ctx, data.tobytes())
+    raw, stored = B.coli_ans_info(ctx, h)
+    out = torch.empty(raw, dtype=torch.uint8, device="cuda")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(warmup + steps)]
+    with torch.cuda.stream(stream):
+        for s in range(warmup + steps):
+            flush.zero_()
+            ev[s][0].record(stream)
+            B.coli_ans_decode(ctx, h, out)
+            ev[s][1].record(stream)
+    torch.cuda.synchronize()
+    assert B.coli_check_error(ctx) == 0, B.coli_last_error(ctx)
+    ok = bool(np.array_equal(out.cpu().numpy(), data))
+    B.coli_ans_free(ctx, h)
+    us = statistics.mean(ev[s][0].elapsed_time(ev[s][1]) for s in range(warmup, warmup + steps)) * 1000.0
+    return {"workload": f"{raw} bytes of packed int4 (nibbles ~ rounded N(7.5, 2.5^2)), 4 KiB rANS blocks",
+            "us": us, "stored_over_raw": stored / raw, "raw_gbs": raw / (us * 1e-6) / 1e9,
+            "stored_gbs": stored / (us * 1e-6) / 1e9, "exact": ok, "l2": "flushed between steps"}
 
 
 def shared_expert_leg(ctx, stream, flush, layer, xs, rs, steps=20, warmup=3):
@@ -641,7 +671,8 @@ def gpu_arm(args, rank, world, local):
     extra = {}
     if rank == 0 and not args.no_prefill:
         for name, leg in (("shared_expert", lambda: shared_expert_leg(ctx, stream, flush, layer, xs, rs)),
-                          ("dense_projection", lambda: linear_leg(ctx, stream, flush, cfg.D))):
+                          ("dense_projection", lambda: linear_leg(ctx, stream, flush, cfg.D)),
+                          ("compressed_tier_decode", lambda: ans_leg(ctx, stream, flush, cfg.I * cfg.D))):
             try:
                 extra[name] = leg()
             except Exception as exc:  # these figures must not hide the decode number

@@ -12,6 +12,7 @@
  *   [attn]   c/backend_cuda.cu commit history, commit "CUDA batch MLA attention, kv_b head-sharding,
  *            fused o_proj, expert-group dispatch, W4A16 kernels"
  *   [q651]   PR #651, comment "Follow-up decode experiments" (Nsight kernel shares)
+ *   [tier]   PR #651 "cuda: add experimental lossless compressed expert tier"
  *
  * Conventions shared by every call:
  *  - Return value: COLI_OK (0) or a negative COLI_E_* code. A failed call leaves no CUDA error
@@ -276,6 +277,30 @@ COLI_API int coli_routes_shard(coli_ctx *ctx, const int32_t *idx, const float *w
                                int K, int rank, int world, int32_t *idx_out, float *w_out, int32_t *n_out);
 COLI_API int coli_partials_reduce(coli_ctx *ctx, const float *parts, int n, int S, int D, const void *resid,
                                   int dtype, void *y);
+
+/*
+ * Compressed expert tier, the codec ([tier]: experts kept as independently decodable 4096-byte ANS
+ * blocks). Our own rANS over the nibbles of a packed byte stream: a per-stream table of 16 nibble
+ * frequencies (12-bit probabilities, each >= 1), 4096-byte blocks, 32 interleaved 32-bit states per
+ * block renormalised with 16-bit words (one lane of a warp per state when decoding). Lossless: the
+ * decoded bytes equal the input exactly. Incompressible input (uniform nibbles) comes out slightly
+ * larger than it went in; the caller compares the sizes (coli_ans_info) and keeps whichever it wants.
+ *
+ * coli_ans_encode_host: host only, no context. Writes the encoded stream of bytes[0..n) to out
+ *   (cap bytes) and its length to *out_len; COLI_E_INVAL (with *out_len set) when cap is too small.
+ * coli_ans_upload: encodes n host bytes and keeps the stream on the device; returns a handle (0 on
+ *   failure, reason in coli_last_error).
+ * coli_ans_info: the raw and stored sizes of an uploaded stream.
+ * coli_ans_decode: decodes the whole stream into out (device, raw bytes), one warp per block, on the
+ *   context's stream. A stream that fails its own consistency checks sets COLI_E_FORMAT in the device
+ *   error word.
+ * coli_ans_free: frees an uploaded stream (after the context's stream has drained).
+ */
+COLI_API int coli_ans_encode_host(const uint8_t *bytes, uint64_t n, uint8_t *out, uint64_t cap, uint64_t *out_len);
+COLI_API uint64_t coli_ans_upload(coli_ctx *ctx, const uint8_t *bytes, uint64_t n);
+COLI_API int coli_ans_info(coli_ctx *ctx, uint64_t handle, uint64_t *raw_bytes, uint64_t *stored_bytes);
+COLI_API int coli_ans_decode(coli_ctx *ctx, uint64_t handle, uint8_t *out);
+COLI_API int coli_ans_free(coli_ctx *ctx, uint64_t handle);
 
 #ifdef __cplusplus
 }

@@ -61,6 +61,11 @@ SIGNATURES = {
     "coli_router_select_shared": (_I, [_P, _P, _I, _I, _I, _P, _P, _I, _I, _F, _I, _F, _I, _P, _P, _P]),
     "coli_routes_shard": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
     "coli_partials_reduce": (_I, [_P, _P, _I, _I, _I, _P, _I, _P]),
+    "coli_ans_encode_host": (_I, [_P, _U64, _P, _U64, ctypes.POINTER(ctypes.c_uint64)]),
+    "coli_ans_upload": (_U64, [_P, _P, _U64]),
+    "coli_ans_info": (_I, [_P, _U64, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]),
+    "coli_ans_decode": (_I, [_P, _U64, _P]),
+    "coli_ans_free": (_I, [_P, _U64]),
     "coli_expert_upload": (_U64, [_P, _P, _P, _I, _I, _I]),
     "coli_expert_free": (_I, [_P, _U64]),
     "coli_tensor_shape": (_I, [_P, _U64, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
@@ -328,6 +333,48 @@ def coli_partials_reduce(ctx, parts, resid, y):
         raise ValueError("partials_reduce: y and resid must be [S x D]")
     rc = library().coli_partials_reduce(ctx, _ptr(parts), n, S, D, _ptr(resid), act_dtype(y), _ptr(y))
     return _check(ctx, rc, "coli_partials_reduce")
+
+
+def coli_ans_encode_host(data: bytes) -> bytes:
+    """The library's encoded stream of ``data`` (host only; no GPU needed)."""
+    lib = library()
+    n = len(data)
+    src = ctypes.create_string_buffer(bytes(data), n)
+    need = ctypes.c_uint64()
+    lib.coli_ans_encode_host(src, n, None, 0, ctypes.byref(need))
+    out = ctypes.create_string_buffer(need.value)
+    rc = lib.coli_ans_encode_host(src, n, out, need.value, ctypes.byref(need))
+    if rc != COLI_OK:
+        raise ColiError(rc, "coli_ans_encode_host failed")
+    return out.raw[:need.value]
+
+
+def coli_ans_upload(ctx, data: bytes):
+    src = ctypes.create_string_buffer(bytes(data), len(data))
+    h = library().coli_ans_upload(ctx, src, len(data))
+    if h == 0:
+        raise ColiError(library().coli_last_code(ctx), f"coli_ans_upload: {coli_last_error(ctx)}")
+    return h
+
+
+def coli_ans_info(ctx, handle):
+    """(raw bytes, stored bytes) of an uploaded stream."""
+    raw, stored = ctypes.c_uint64(), ctypes.c_uint64()
+    _check(ctx, library().coli_ans_info(ctx, handle, ctypes.byref(raw), ctypes.byref(stored)), "coli_ans_info")
+    return raw.value, stored.value
+
+
+def coli_ans_decode(ctx, handle, out):
+    """Decode an uploaded stream into ``out`` (a CUDA uint8 tensor of the raw size)."""
+    _dev(out, torch.uint8, "out")
+    raw, _ = coli_ans_info(ctx, handle)
+    if out.numel() != raw:
+        raise ValueError("ans_decode: out must hold the raw size")
+    return _check(ctx, library().coli_ans_decode(ctx, handle, _ptr(out)), "coli_ans_decode")
+
+
+def coli_ans_free(ctx, handle):
+    return _check(ctx, library().coli_ans_free(ctx, handle), "coli_ans_free")
 
 
 def coli_profile_enable(ctx, on):

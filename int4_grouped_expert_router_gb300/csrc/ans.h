@@ -1,0 +1,26 @@
+// Compressed expert tier: the block codec (ans.cu). Declared outside the expert kernels' internal header.
+#pragma once
+
+#include <vector>
+
+#include "coli_internal.h"
+
+namespace coli {
+
+constexpr uint32_t kAnsBlockBytes = 4096;  // raw bytes per independently decodable block
+
+size_t ans_bound(uint64_t n);                                        // upper bound of a stream's size
+int ans_encode(const uint8_t* in, uint64_t n, std::vector<uint8_t>& out);  // host encoder (always succeeds)
+int ans_blocks(const void* blob_host);                               // block count of an encoded stream
+int launch_ans_decode(coli_ctx* ctx, const uint8_t* blob, int blocks, uint8_t* out);
+
+// Library-owned compressed streams of a context (coli_ans_upload handles), freed with the context.
+struct AnsStream {
+  uint8_t* d_blob = nullptr;
+  uint64_t stored = 0, raw = 0;
+  int blocks = 0;
+};
+std::vector<AnsStream>& ans_streams(coli_ctx* ctx);
+void ans_release_all(coli_ctx* ctx);
+
+}  // namespace coli

@@ -6,6 +6,7 @@
 #include <string>
 
 #include "coli_internal.h"
+#include "ans.h"
 #include "ep.h"
 
 namespace coli {
@@ -255,6 +256,7 @@ void coli_destroy(coli_ctx* ctx) {
     if (t.d_solo) cudaFree(t.d_solo);
   }
   if (ctx->d_solo_route) cudaFree(ctx->d_solo_route);
+  ans_release_all(ctx);
   if (ctx->d_table) cudaFree(ctx->d_table);
   if (ctx->d_status) cudaFree(ctx->d_status);
   if (ctx->ws.base) cudaFree(ctx->ws.base);
@@ -569,6 +571,84 @@ int coli_w4_linear(coli_ctx* ctx, uint64_t W, const void* x, int x_dtype, int S,
   int rc = launch_linear(ctx, t.desc, t.d_solo, x, x_dtype, S, resid, y);
   if (rc == COLI_OK) ctx->compute_calls++;
   return rc;
+}
+
+int coli_ans_encode_host(const uint8_t* bytes, uint64_t n, uint8_t* out, uint64_t cap, uint64_t* out_len) {
+  if (!bytes || n < 1 || !out_len) return COLI_E_INVAL;
+  std::vector<uint8_t> blob;
+  ans_encode(bytes, n, blob);
+  *out_len = blob.size();
+  if (!out || cap < blob.size()) return COLI_E_INVAL;
+  memcpy(out, blob.data(), blob.size());
+  return COLI_OK;
+}
+
+uint64_t coli_ans_upload(coli_ctx* ctx, const uint8_t* bytes, uint64_t n) {
+  if (!ctx) return 0;
+  if (!bytes || n < 1) {
+    fail(ctx, COLI_E_INVAL, "ans_upload: NULL pointer or empty stream");
+    return 0;
+  }
+  std::vector<uint8_t> blob;
+  ans_encode(bytes, n, blob);
+  cudaSetDevice(ctx->device);
+  void* p = nullptr;
+  cudaError_t e;
+  if ((e = cudaMalloc(&p, blob.size())) != cudaSuccess) {
+    cuda_fail(ctx, e, "ans_upload: cudaMalloc");
+    return 0;
+  }
+  if ((e = cudaMemcpy(p, blob.data(), blob.size(), cudaMemcpyHostToDevice)) != cudaSuccess) {
+    cudaFree(p);
+    cuda_fail(ctx, e, "ans_upload: copy");
+    return 0;
+  }
+  AnsStream st;
+  st.d_blob = static_cast<uint8_t*>(p);
+  st.stored = blob.size();
+  st.raw = n;
+  st.blocks = ans_blocks(blob.data());
+  auto& v = ans_streams(ctx);
+  v.push_back(st);
+  return (uint64_t)v.size();
+}
+
+static AnsStream* ans_stream(coli_ctx* ctx, uint64_t h) {
+  auto& v = ans_streams(ctx);
+  return (h >= 1 && h <= v.size() && v[h - 1].d_blob) ? &v[h - 1] : nullptr;
+}
+
+int coli_ans_info(coli_ctx* ctx, uint64_t h, uint64_t* raw_bytes, uint64_t* stored_bytes) {
+  if (!ctx) return COLI_E_INVAL;
+  AnsStream* st = ans_stream(ctx, h);
+  if (!st) return fail(ctx, COLI_E_INVAL, "ans_info: unknown handle");
+  if (raw_bytes) *raw_bytes = st->raw;
+  if (stored_bytes) *stored_bytes = st->stored;
+  return COLI_OK;
+}
+
+int coli_ans_decode(coli_ctx* ctx, uint64_t h, uint8_t* out) {
+  if (!ctx) return COLI_E_INVAL;
+  AnsStream* st = ans_stream(ctx, h);
+  if (!st) return fail(ctx, COLI_E_INVAL, "ans_decode: unknown handle");
+  if (!out) return fail(ctx, COLI_E_INVAL, "ans_decode: NULL pointer");
+  if (injected(ctx)) return COLI_E_INJECTED;
+  cudaSetDevice(ctx->device);
+  int rc = launch_ans_decode(ctx, st->d_blob, st->blocks, out);
+  if (rc == COLI_OK) ctx->compute_calls++;
+  return rc;
+}
+
+int coli_ans_free(coli_ctx* ctx, uint64_t h) {
+  if (!ctx) return COLI_E_INVAL;
+  AnsStream* st = ans_stream(ctx, h);
+  if (!st) return fail(ctx, COLI_E_INVAL, "ans_free: unknown handle");
+  cudaSetDevice(ctx->device);
+  cudaError_t e = cudaStreamSynchronize(ctx->stream);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "ans_free: stream sync");
+  cudaFree(st->d_blob);
+  *st = AnsStream{};
+  return COLI_OK;
 }
 
 int coli_routes_shard(coli_ctx* ctx, const int32_t* idx, const float* w, const int32_t* n_sel, int S, int K, int rank,

@@ -159,6 +159,14 @@ def expert_tensor_torch(seed: int, rows: int, cols: int, gs: int, device, scale_
     return packed, scales
 
 
+def gaussian_nibble_bytes(seed: int, nbytes: int, sigma: float = 2.5) -> np.ndarray:
+    """Packed bytes whose nibbles follow a rounded normal centred between 7 and 8 (std ``sigma``, clipped
+    to 0..15): the shape of int4-quantised weights, whose values crowd the middle of the code range."""
+    z = normal(seed, 2 * nbytes, std=sigma).astype(np.float64)
+    q = np.clip(np.floor(z + 8.0), 0, 15).astype(np.uint8)
+    return (q[0::2] | (q[1::2] << 4)).astype(np.uint8)
+
+
 def expert_seed(base: int, e: int, which: str) -> int:
     return stream_seed(base, "expert", e, which)
 

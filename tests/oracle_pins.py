@@ -421,4 +421,26 @@ def pin_ep_layer_partition(o):
         assert np.allclose(got, ref, rtol=1e-12, atol=1e-12), world
 
 
+def pin_ans_codec(o):
+    """The block codec (oracle.ans): lossless round trips across block boundaries and odd lengths, a size
+    within the entropy bound plus the per-block overhead, and a constant stream that needs no words."""
+    import oracle.ans as A
+    for n, sigma in ((1, 2.5), (31, 2.5), (4096, 2.0), (4097, 3.0), (9000, 1.5)):
+        data = bytes(synth.gaussian_nibble_bytes(synth.stream_seed(95, n), n, sigma))
+        enc = A.encode(data)
+        assert A.decode(enc) == data, n
+        nib = [b & 15 for b in data] + [b >> 4 for b in data]
+        p = np.bincount(nib, minlength=16) / len(nib)
+        h_bits = -sum(q * math.log2(q) for q in p if q > 0) * len(nib)
+        blocks = (n + 4095) // 4096
+        overhead = 56 + 4 * (blocks + 1) + blocks * (192 + 4 + 32 * 2)  # header, offsets, per-block states/counts/pad
+        assert len(enc) <= h_bits / 8 * 1.01 + overhead + 16, (n, len(enc), h_bits / 8)
+    rnd = bytes(synth.random_bytes(96, 5000))
+    assert A.decode(A.encode(rnd)) == rnd
+    const = bytes([0x88]) * 8192
+    enc = A.encode(const)
+    assert A.decode(enc) == const
+    assert len(enc) == 56 + 4 * 3 + 2 * 192  # two blocks of states and counts, not one word
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
