@@ -63,12 +63,6 @@ void make_freq(const uint64_t (&count)[16], uint64_t total, uint16_t (&freq)[16]
 
 }  // namespace
 
-size_t ans_bound(uint64_t n) {
-  const uint64_t blocks = (n + kAnsBlockBytes - 1) / kAnsBlockBytes;
-  // per symbol at most one word for a frequency of 1 (12 bits); per block the states, counts and padding
-  return sizeof(Header) + 4 * (blocks + 1) + blocks * (32 * 4 + 32 * 2 + 4) + 2 * n * 2 + 64;
-}
-
 int ans_encode(const uint8_t* in, uint64_t n, std::vector<uint8_t>& out) {
   uint64_t count[16] = {0};
   for (uint64_t i = 0; i < n; i++) {

@@ -9,7 +9,6 @@ namespace coli {
 
 constexpr uint32_t kAnsBlockBytes = 4096;  // raw bytes per independently decodable block
 
-size_t ans_bound(uint64_t n);                                        // upper bound of a stream's size
 int ans_encode(const uint8_t* in, uint64_t n, std::vector<uint8_t>& out);  // host encoder (always succeeds)
 int ans_blocks(const void* blob_host);                               // block count of an encoded stream
 int launch_ans_decode(coli_ctx* ctx, const uint8_t* blob, int blocks, uint8_t* out);
