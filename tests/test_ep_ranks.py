@@ -86,3 +86,81 @@ def test_expert_parallel_reduce_over_gloo():
             si, sw, sn = O.shard_routes(idx, w, n, r, world)
             assert np.array_equal(parts0[r], O.expert_group(x, experts, si, sw, sn, None)), (world, r)
         assert np.allclose(y0, ref1, rtol=1e-12, atol=1e-12)
+
+
+class _OracleDevice:
+    """Stand-ins for the library calls ExpertParallelLayer makes, computed by the oracle on CPU tensors."""
+
+    def __init__(self, experts):
+        self.experts, self.pending = experts, None
+
+    def coli_router_select(self, ctx, x, Wr, bias, K, topp, norm_topk, routed_scale, idx, w, n_sel):
+        i, ww, n, _ = O.router_select(x.numpy(), Wr.numpy(), None if bias is None else bias.numpy(), K, topp,
+                                      norm_topk, routed_scale)
+        idx.copy_(torch.from_numpy(i))
+        w.copy_(torch.from_numpy(ww))
+        n_sel.copy_(torch.from_numpy(n))
+
+    def coli_routes_shard(self, ctx, idx, w, n_sel, rank, world, idx_out, w_out, n_out):
+        i, ww, n = O.shard_routes(idx.numpy(), w.numpy(), n_sel.numpy(), rank, world)
+        idx_out.copy_(torch.from_numpy(i))
+        w_out.copy_(torch.from_numpy(ww))
+        n_out.copy_(torch.from_numpy(n))
+
+    def coli_expert_group_issue(self, ctx, x, idx, w, n_sel, K):
+        assert self.pending is None
+        self.pending = (x.numpy(), idx.numpy(), w.numpy(), n_sel.numpy())
+        return 0
+
+    def coli_expert_group_take(self, ctx, resid, y):
+        x, idx, w, n = self.pending
+        self.pending = None
+        p = O.expert_group(x, self.experts, idx, w, n, None)
+        y.copy_(torch.from_numpy(p if resid is None else resid.numpy() + p))
+
+    def coli_partials_reduce(self, ctx, parts, resid, y):
+        acc = parts[0].numpy().astype(np.float64)
+        for r in range(1, parts.shape[0]):
+            acc = acc + parts[r].numpy()
+        y.copy_(torch.from_numpy(acc if resid is None else resid.numpy() + acc))
+
+
+def _layer_main(rank, world, port, out):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        experts, x, resid, _, _, _ = _problem()
+        Wr = synth.normal(synth.stream_seed(301, "Wr"), E * D).reshape(E, D) * 0.1
+        mine = {e: t for e, t in experts.items() if ep.owner(e, world) == rank}
+        ep.B = _OracleDevice(mine)  # this process only: the layer's library calls go to the oracle
+        layer = ep.ExpertParallelLayer(None, rank, world)
+        y = torch.empty(S, D, dtype=torch.float64)
+        idx, w, n = layer.step(torch.from_numpy(x), torch.from_numpy(Wr), None, K, 0.0, True, 2.5,
+                               torch.from_numpy(resid.astype(np.float64)), y)
+        out[rank] = (y.numpy(), idx.numpy(), w.numpy(), n.numpy())
+        try:
+            layer.step(torch.from_numpy(x).to(torch.bfloat16), torch.from_numpy(Wr), None, K, 0.0, True, 2.5, None, y)
+            out[f"bf16-{rank}"] = "accepted"
+        except ValueError:
+            out[f"bf16-{rank}"] = "rejected"
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_expert_parallel_layer_over_gloo():
+    """ExpertParallelLayer's call order (route, shard, issue, take, gather, reduce) with world size 2, the
+    library calls computed by the oracle: every rank ends with the oracle's expert-parallel block."""
+    world, port = 2, _free_port()
+    with mp.Manager() as mgr:
+        out = mgr.dict()
+        mp.spawn(_layer_main, args=(world, port, out), nprocs=world, join=True)
+        res = dict(out)
+    experts, x, resid, idx, w, n = _problem()
+    want = O.ep_layer(x, experts, idx, w, n, world, resid)
+    for r in range(world):
+        y, i, ww, nn = res[r]
+        assert np.array_equal(i, idx) and np.array_equal(nn, n)
+        assert np.allclose(y, want, rtol=1e-6, atol=1e-6)  # the exchanged partial rows are f32
+        assert res[f"bf16-{r}"] == "rejected"
