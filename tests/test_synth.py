@@ -48,3 +48,14 @@ def test_bf16_rounding():
 def test_zipf_bias_is_skewed():
     b = synth.zipf_bias(synth.BASE_SEED, 256)
     assert b.shape == (256,) and float(b.max() - b.min()) > 1.0
+
+
+def test_gaussian_nibbles_shape_of_quantised_weights():
+    b = synth.gaussian_nibble_bytes(7, 200000, 2.5)
+    assert b.dtype == np.uint8 and b.shape == (200000,)
+    assert np.array_equal(b, synth.gaussian_nibble_bytes(7, 200000, 2.5))
+    nib = np.concatenate([b & 15, b >> 4]).astype(np.int64)
+    assert abs(float(nib.mean()) - 7.5) < 0.02 and abs(float(nib.std()) - 2.55) < 0.05
+    p = np.bincount(nib, minlength=16) / nib.size
+    h = -float(np.sum(p[p > 0] * np.log2(p[p > 0])))
+    assert 3.3 < h < 3.5  # bits per nibble: well under the 4 of uniform nibbles
