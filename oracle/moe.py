@@ -24,7 +24,9 @@ Sources (web pages about the "colibri" int4 MoE engine; cited by page and sectio
   [q651]    PR #651, comment "Follow-up decode experiments" (the generic quant_matmul's kernel share)
 
 Precision: weights are dequantised exactly (float64) and every dot product, SiLU and
-the weighted reduce run in float64. The router's decisions (top-K, top-p) are taken in
+the weighted reduce run in float64. A binary32 sequential mode (matvec_f32_seq,
+expert_ffn_f32, expert_group_f32) is kept beside it for diagnosis only: it measures how far
+a plain f32 evaluation of the same sums falls from the float64 definition. The router's decisions (top-K, top-p) are taken in
 float32, the precision of the pages' f32 logits, on float32 scores derived from the
 float64 logits by one rounding each. Every reading of an ambiguous passage is marked
 "Reading:" below.
@@ -270,6 +272,49 @@ def expert_group(x, experts, idx, w, n_sel=None, resid=None) -> np.ndarray:
             gate, up, down = experts[int(idx[t, k])]
             acc = acc + float(w[t, k]) * expert_ffn(x[t], gate, up, down)
         y[t] = acc if resid is None else np.asarray(resid[t], dtype=np.float64) + acc
+    return y
+
+
+# ------------------------------------------------------------------------------------------
+# Binary32 sequential evaluation (a diagnosis mode beside the float64 definition)
+# ------------------------------------------------------------------------------------------
+
+def matvec_f32_seq(T: Tensor, v) -> np.ndarray:
+    """W v evaluated the plainest way in binary32: W[o, j] = f32(scale(o, j) * (nibble - 8)) ([g4]),
+    each product W[o, j] * v[j] rounded to f32, and each row's products added to a running f32 sum in
+    column order j = 0, 1, ..., L - 1. Not the definition (that is the exact float64 matvec): it sizes
+    how far any binary32 evaluation of the same sums may fall from it."""
+    W32 = (scale_of(T.scales, T.rows, T.cols, T.gs).astype(F32) *
+           unpack_int4(T.packed, T.rows, T.cols).astype(F32))
+    prod = W32 * np.asarray(v, dtype=F32)[None, :]
+    return np.add.accumulate(prod, axis=1, dtype=F32)[:, -1]
+
+
+def expert_ffn_f32(x_row, gate: Tensor, up: Tensor, down: Tensor) -> np.ndarray:
+    """:func:`expert_ffn` in binary32: sequential f32 matvecs, h = g / (1 + exp(-g)) * u in f32."""
+    x32 = np.asarray(x_row, dtype=F32)
+    g = matvec_f32_seq(gate, x32)
+    u = matvec_f32_seq(up, x32)
+    with np.errstate(over="ignore"):
+        h = (g / (F32(1) + np.exp(-g))).astype(F32) * u
+    return matvec_f32_seq(down, h.astype(F32))
+
+
+def expert_group_f32(x, experts, idx, w, n_sel=None, resid=None) -> np.ndarray:
+    """:func:`expert_group` in binary32: acc = f32(acc + f32(w_k y_k)) in slot order, then resid + acc."""
+    x = np.atleast_2d(np.asarray(x, dtype=F32))
+    idx = np.atleast_2d(np.asarray(idx))
+    w = np.atleast_2d(np.asarray(w, dtype=F32))
+    S, K = idx.shape
+    if n_sel is None:
+        n_sel = np.full(S, K, dtype=np.int32)
+    y = np.zeros((S, x.shape[1]), dtype=F32)
+    for t in range(S):
+        acc = np.zeros(x.shape[1], dtype=F32)
+        for k in range(int(n_sel[t])):
+            gate, up, down = experts[int(idx[t, k])]
+            acc = (acc + (w[t, k] * expert_ffn_f32(x[t], gate, up, down)).astype(F32)).astype(F32)
+        y[t] = acc if resid is None else (np.asarray(resid[t], dtype=F32) + acc).astype(F32)
     return y
 
 

@@ -278,6 +278,54 @@ def pin_ffn_exact_integers(o):
         assert got.tolist() == want
 
 
+def pin_f32_seq_worked(o):
+    """The binary32 diagnosis mode, worked by hand.
+    (1) Terms are added in column order. A row of value-1 weights times x = [2^24, 1, ..., 1] (sixteen
+    columns) gives 2^24 in f32: every +1 is lost to round-to-even at 2^24 (spacing 2). The exact sum is
+    2^24 + 15; a pairwise sum over eight partial sums gives 2^24 + 14.
+    (2) The weight is the f32 product of scale and value, then the term the f32 product of weight and
+    activation. With scale 1 + 2^-23 and value 7 the weight 7 + 7 2^-23 rounds to 7 + 2^-20 (the
+    spacing in [4, 8) is 2^-21); times x = 3 that is 21 + 1.5 2^-19, a tie in [16, 32) (spacing 2^-19)
+    that rounds to even: 21 + 2^-18. Rounding only once, (7 + 7 2^-23) 3 = 21 + 0.65625 2^-19 would
+    round to 21 + 2^-19."""
+    ones = _tensor_from_q(o, np.ones((1, 16), np.int16), [1.0])
+    x = np.array([2.0 ** 24] + [1.0] * 15, np.float32)
+    assert o.matvec_f32_seq(ones, x).tolist() == [2.0 ** 24]
+    assert o.w4_linear(x, ones)[0].tolist() == [2.0 ** 24 + 15]
+    s = np.float32(1.0 + 2.0 ** -23)
+    seven = _tensor_from_q(o, np.array([[7, 0]], np.int16), [s])
+    assert o.matvec_f32_seq(seven, np.array([1.0, 0.0], np.float32)).tolist() == [7.0 + 2.0 ** -20]
+    assert o.matvec_f32_seq(seven, np.array([3.0, 0.0], np.float32)).tolist() == [21.0 + 2.0 ** -18]
+
+
+def pin_f32_seq_exact_cases(o):
+    """Integer activations, small integer weights and power-of-two scales keep every f32 product and
+    partial sum exact: the binary32 mode then equals the float64 definition bit for bit, for the matvec,
+    the expert FFN's gate/up/down chain up to h (where SiLU rounds) and the slot-ordered reduce of exact
+    expert outputs."""
+    D, I = 24, 6
+    for trial in range(3):
+        q = ((synth.u64(synth.stream_seed(trial, "q32"), I * D) % np.uint64(16)).astype(np.int16) - 8).reshape(I, D)
+        xi = ((synth.u64(synth.stream_seed(trial, "x32"), D) % np.uint64(9)).astype(np.int64) - 4).astype(np.float32)
+        sc = np.array([2.0 ** (k - 3) for k in range(I)], np.float32)
+        T = _tensor_from_q(o, q, sc)
+        assert o.matvec_f32_seq(T, xi).astype(np.float64).tolist() == (T.dense() @ xi.astype(np.float64)).tolist()
+    # the FFN chain and the reduce: g = 32 * sum(x) = 128 makes SiLU(g) = g exactly in both precisions
+    # (exp(-128) vanishes beside 1); expert 0 has u = 2 (h = 256), expert 1 u = 128 (h = 16384), and the
+    # down rows are small integers times h / 16
+    gate = _tensor_from_q(o, np.ones((2, 4), np.int16), [32.0, 32.0])
+    up = _tensor_from_q(o, np.ones((2, 4), np.int16), [0.5, 0.5])
+    down = _tensor_from_q(o, np.array([[1, -2], [3, 0], [-8, 7], [5, 5]], np.int16), [2.0 ** -4] * 4)
+    ex = {0: (gate, up, down), 1: (gate, gate, down)}
+    x = np.ones((1, 4), np.float32)
+    r = np.array([[1.0, -2.0, 3.0, 0.5]], np.float32)
+    y32 = o.expert_group_f32(x, ex, [[0, 1]], [[0.5, 2.0]], None, r)
+    y64 = o.expert_group(x, ex, [[0, 1]], [[0.5, 2.0]], None, r)
+    assert y32.astype(np.float64).tolist() == y64.tolist()
+    # r + 0.5 * 16 * [-1, 3, -1, 10] + 2 * 1024 * [-1, 3, -1, 10]
+    assert y64.tolist() == [[-2055.0, 6166.0, -2053.0, 20560.5]]
+
+
 def pin_reduce_properties(o):
     D, I, E = 12, 4, 3
     experts = {}

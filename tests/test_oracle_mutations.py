@@ -204,11 +204,30 @@ def ep_drops_last_rank(o):
     o.ep_layer = bad
 
 
+def f32_pairwise_sum(o):
+    """The binary32 diagnosis mode summing each row pairwise (numpy's reduce) instead of in column order."""
+    def bad(T, v):
+        W32 = (o.scale_of(T.scales, T.rows, T.cols, T.gs).astype(np.float32) *
+               o.unpack_int4(T.packed, T.rows, T.cols).astype(np.float32))
+        return np.sum(W32 * np.asarray(v, np.float32)[None, :], axis=1, dtype=np.float32)
+    o.matvec_f32_seq = bad
+
+
+def f32_weights_unrounded(o):
+    """The binary32 mode with each weight kept exact (float64 scale x value) before the f32 product."""
+    def bad(T, v):
+        W = T.dense()
+        prod = (W * np.asarray(v, np.float32).astype(np.float64)[None, :]).astype(np.float32)
+        return np.add.accumulate(prod, axis=1, dtype=np.float32)[:, -1]
+    o.matvec_f32_seq = bad
+
+
 MUTATIONS = [swap_nibble_order, offset_seven, tie_to_higher_index, weights_from_choice, scale_before_norm,
              topp_drops_reaching_slot, norm_over_all_slots, sigmoid_sign, silu_on_up, drop_residual,
              group_scales_column_major, group_index_by_byte, down_transposed_roles, gate_up_swapped,
              linear_drops_residual, linear_reads_columns_reversed, shared_weighted_like_slot0,
-             shared_slot_at_row_end, shard_by_block_not_modulo, ep_drops_last_rank]
+             shared_slot_at_row_end, shard_by_block_not_modulo, ep_drops_last_rank, f32_pairwise_sum,
+             f32_weights_unrounded]
 
 
 @pytest.mark.parametrize("mutate", MUTATIONS, ids=[m.__name__ for m in MUTATIONS])
