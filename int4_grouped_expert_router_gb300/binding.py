@@ -37,6 +37,7 @@ COLI_E_INJECTED = _C["COLI_E_INJECTED"]
 COLI_E_FORMAT = _C["COLI_E_FORMAT"]
 COLI_E_NONFINITE = _C["COLI_E_NONFINITE"]
 COLI_E_ROUTE = _C["COLI_E_ROUTE"]
+COLI_E_TIMEOUT = _C["COLI_E_TIMEOUT"]
 COLI_DTYPE_F32 = _C["COLI_DTYPE_F32"]
 COLI_DTYPE_BF16 = _C["COLI_DTYPE_BF16"]
 COLI_MAX_EXPERTS = _C["COLI_MAX_EXPERTS"]

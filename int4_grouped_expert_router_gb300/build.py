@@ -21,7 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libcoli_moe.so")
-SOURCES = ["api.cu", "router.cu", "experts.cu", "prefill.cu", "ep.cu", "ans.cu"]
+SOURCES = ["api.cu", "router.cu", "experts.cu", "decode.cu", "prefill.cu", "ep.cu", "ans.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-I" + INCLUDE]

@@ -3,6 +3,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <string>
 
 #include "coli_internal.h"
@@ -222,8 +223,15 @@ int coli_init(coli_ctx** out, int device, void* cuda_stream) {
   if (fa && *fa) ctx->fail_after = atoll(fa);
   const char* fu = getenv("COLI_DECODE_FUSED");
   if (fu && *fu) ctx->decode_fused = atoi(fu) != 0;
+  const char* fs = getenv("COLI_DECODE_STREAM");
+  if (fs && *fs) ctx->stream_ffn = atoi(fs) != 0;
+  const char* tw = getenv("COLI_TEST_WAIT_NS");
+  if (tw && *tw) ctx->wait_ns = strtoull(tw, nullptr, 10);
+  const char* th = getenv("COLI_TEST_WITHHOLD");
+  if (th && *th) ctx->test_withhold = atoi(th) != 0;
   ctx->h_table.assign(COLI_MAX_EXPERTS, ExpertDesc{});
   ctx->table_handles.assign(3 * COLI_MAX_EXPERTS, 0);
+  ctx->table_stream.assign(COLI_MAX_EXPERTS, 1);
   void* p = nullptr;
   if ((e = cudaMalloc(&p, sizeof(ExpertDesc) * COLI_MAX_EXPERTS)) != cudaSuccess) goto fail;
   ctx->d_table = static_cast<ExpertDesc*>(p);
@@ -254,6 +262,8 @@ void coli_destroy(coli_ctx* ctx) {
     if (t.w) cudaFree(t.w);
     if (t.s) cudaFree(t.s);
     if (t.d_solo) cudaFree(t.d_solo);
+    if (t.panel) cudaFree(t.panel);
+    if (t.sT) cudaFree(t.sT);
   }
   if (ctx->d_solo_route) cudaFree(ctx->d_solo_route);
   ans_release_all(ctx);
@@ -345,6 +355,9 @@ int coli_reserve(coli_ctx* ctx, int max_S, int max_E, int max_K, int max_D, int 
   const size_t prefill = pf_rows * ((size_t)max_D * 2 + (size_t)max_I * 2 + (size_t)max_D * 4 + 4) + routes * 4 +
                          (size_t)max_E * 8 + (routes / 128 + max_E + 1) * 16 + 16 * 256;
   if (prefill > experts) experts = prefill;
+  // one-launch S == 1 FFN: a partial row of y per CTA
+  const size_t stream = (size_t)ctx->num_sms * max_D * sizeof(float);
+  if (stream > experts) experts = stream;
   const size_t slots = (size_t)COLI_MAX_ISSUES * max_S * max_D * sizeof(float);
   cudaSetDevice(ctx->device);
   int rc = ensure_slots(ctx, slots);
@@ -444,6 +457,8 @@ int coli_expert_free(coli_ctx* ctx, uint64_t handle) {
   cudaFree(t.w);
   cudaFree(t.s);
   if (t.d_solo) cudaFree(t.d_solo);
+  if (t.panel) cudaFree(t.panel);
+  if (t.sT) cudaFree(t.sT);
   t = HostTensor{};
   return COLI_OK;
 }
@@ -457,6 +472,8 @@ int coli_expert_table_set(coli_ctx* ctx, int e, uint64_t gate, uint64_t up, uint
   if (gate == 0 && up == 0 && down == 0) {
     if (cur[0]) {
       for (int i = 0; i < 3; i++) ctx->tensors[cur[i] - 1].table_refs--;
+      if (!ctx->table_stream[e]) ctx->table_nostream--;
+      ctx->table_stream[e] = 1;
       ctx->table_count--;
       if (ctx->table_count == 0) ctx->table_D = ctx->table_I = 0;
     }
@@ -471,10 +488,24 @@ int coli_expert_table_set(coli_ctx* ctx, int e, uint64_t gate, uint64_t up, uint
     bool replacing = cur[0] != 0;
     if (ctx->table_count - (replacing ? 1 : 0) > 0 && (ctx->table_D != D || ctx->table_I != I))
       return fail(ctx, COLI_E_FORMAT, "table_set: every expert must share D and I");
-    if (replacing)
+    // the one-launch S == 1 FFN streams down tensors panel-major: build that view once per tensor
+    HostTensor& dnt = ctx->tensors[down - 1];
+    const bool streamable = ctx->stream_ffn && stream_tensor_ok(g, false) && stream_tensor_ok(u, false) &&
+                            stream_tensor_ok(dnt, true);
+    if (streamable) {
+      int rc = build_stream_view(ctx, dnt);
+      if (rc != COLI_OK) return rc;
+      const int gG = g.gs > 0 ? g.G : 0, uG = u.gs > 0 ? u.G : 0;
+      ctx->table_gu_maxG = std::max(ctx->table_gu_maxG, std::max(gG, uG));
+    }
+    if (replacing) {
       for (int i = 0; i < 3; i++) ctx->tensors[cur[i] - 1].table_refs--;
-    else
+      if (!ctx->table_stream[e]) ctx->table_nostream--;
+    } else {
       ctx->table_count++;
+    }
+    ctx->table_stream[e] = streamable;
+    if (!streamable) ctx->table_nostream++;
     ctx->table_D = D;
     ctx->table_I = I;
     cur[0] = gate;
@@ -483,7 +514,7 @@ int coli_expert_table_set(coli_ctx* ctx, int e, uint64_t gate, uint64_t up, uint
     for (int i = 0; i < 3; i++) ctx->tensors[cur[i] - 1].table_refs++;
     d.t[T_GATE] = g.desc;
     d.t[T_UP] = u.desc;
-    d.t[T_DOWN] = dn.desc;
+    d.t[T_DOWN] = dnt.desc;
     d.valid = 1;
   }
   ctx->h_table[e] = d;

@@ -26,11 +26,15 @@ constexpr int kScaleBox = 16;
 // nibbles per row, staged with the 128-byte swizzle), four 64-column K tiles of the MMA.
 constexpr int kTcRows = 128;
 constexpr int kTcWords = 32;
+// One-launch decode FFN: a work unit is kPanelCols rows of gate/up and the same columns of down.
+constexpr int kPanelCols = 16;
 
-// Device status words of a context: [0] error code, [1] router arrivals, [2..] the fused decode
-// kernel's synchronisation words (grid barrier at [2], [3]; row-range counters from
-// [2 + kSyncRanges]). All start at zero and are returned to zero by the kernels that use them.
+// Device status words of a context: [0] error code, [1] router arrivals, [2..] the opt-in fused
+// decode kernel's synchronisation words (grid barrier at [2], [3]; row-range counters from
+// [2 + kSyncRanges]), [4], [5] the one-launch decode FFN's grid barrier. All start at zero; the
+// router's counter is returned to zero by its last CTA, and the grid barriers' counts only grow.
 constexpr int kSyncBase = 2;
+constexpr int kStreamBar = 4;     // the one-launch decode FFN's grid barrier (64-bit arrival count)
 constexpr int kSyncRanges = 64;   // offset of the range counters from kSyncBase
 constexpr int kMaxRanges = 4096;  // range counters
 constexpr size_t kStatusBytes = (size_t)(kSyncBase + kSyncRanges + kMaxRanges) * sizeof(int);
@@ -54,6 +58,11 @@ struct TensorDesc {
   uint32_t box_w;      // words of a weight box row (min(kSliceWords, pitch / 4))
   uint32_t box_s;      // floats of a scale box row (0: scales are not staged by TMA)
   uint32_t pad_;
+  // Panel-major view for the one-launch decode FFN (built for down tensors of the expert table,
+  // NULL otherwise): column block p of kPanelCols columns is [rows x kPanelCols / 2 bytes] at
+  // panel + p * rows * kPanelCols / 2; sT holds chunk-group scales transposed, [G x rows].
+  const uint8_t* panel;
+  const float* sT;
 };
 
 enum { SCALE_ROW = 0, SCALE_CHUNK = 1, SCALE_GENERIC = 2 };
@@ -78,6 +87,8 @@ struct HostTensor {
   bool live = false;
   TensorDesc desc{};  // device view, tensor maps included
   ExpertDesc* d_solo = nullptr;  // device entry {down = this tensor, valid}: the one-token dense projection
+  uint8_t* panel = nullptr;      // panel-major copy (desc.panel), built when first used as a down tensor
+  float* sT = nullptr;           // transposed chunk-group scales (desc.sT)
 };
 
 struct Workspace {
@@ -105,6 +116,17 @@ struct coli_ctx {
   // this device launches it (2: cooperative + programmatic dependent launch, 1: cooperative, 0: no)
   bool decode_fused = false;
   int coop_mode = -1;  // -1: not probed yet
+  // S == 1 one-launch streaming FFN (decode.cu): on unless COLI_DECODE_STREAM=0; table entries whose
+  // tensors it cannot stream (group sizes that are not multiples of 32, shapes off its grid)
+  bool stream_ffn = true;
+  int table_nostream = 0;
+  std::vector<char> table_stream;  // per entry: 1 if set and streamable, or unset
+  int table_gu_maxG = 0;           // most chunk groups per gate/up row of any entry set since creation
+  // test hooks read at coli_init: a shorter limit for the streaming kernel's bounded waits
+  // (COLI_TEST_WAIT_NS) and, for the next N of its launches, a CTA that withholds its grid-barrier
+  // arrival so that every wait on that barrier gives up (COLI_TEST_WITHHOLD=N)
+  unsigned long long wait_ns = 0;
+  int test_withhold = 0;
   coli::Workspace ws;
   // resident issue/take: f32 partial sums [COLI_MAX_ISSUES][S x D] of the current round's issues
   float* slots = nullptr;
@@ -169,6 +191,41 @@ int launch_linear(coli_ctx* ctx, const TensorDesc& T, const ExpertDesc* solo, co
                   const void* resid, void* y);
 // y [S x D] (dtype) = resid + the n issued partial sums [S x D] f32, added in issue order.
 int launch_take(coli_ctx* ctx, int S, int D, int n, const void* resid, int dtype, void* y);
+// One-launch S == 1 expert FFN (decode.cu): eligibility, launch, and the per-tensor panel view
+// it streams down tensors from (built by coli_expert_table_set).
+bool stream_eligible(const coli_ctx* ctx, int S);
+bool stream_tensor_ok(const HostTensor& t, bool as_down);
+int build_stream_view(coli_ctx* ctx, HostTensor& t);
+int launch_stream_ffn(coli_ctx* ctx, const void* x, int x_dtype, const int32_t* idx, const float* w,
+                      const int32_t* n_sel, int K, const void* resid, void* y, int y_dtype);
+// Launch with programmatic stream serialisation (the kernel may start while its predecessor in
+// the stream finishes; it calls griddepcontrol.wait before reading that predecessor's output) and,
+// when `coop`, as a cooperative launch (every CTA resident at once, or the launch fails).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), int grid, int block, size_t smem, cudaStream_t st, bool pdl,
+                            bool coop, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    na++;
+  }
+  if (coop) {
+    attr[na].id = cudaLaunchAttributeCooperative;
+    attr[na].val.cooperative = 1;
+    na++;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Which cooperative launch forms this device accepts (coli_ctx::coop_mode), found with an empty
 // kernel on a private stream.
 int probe_coop_mode(coli_ctx* ctx);

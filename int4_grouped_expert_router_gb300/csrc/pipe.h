@@ -79,8 +79,8 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 #define COLI_WAIT_SPIN 1
 #endif
 
-// Wait until the phase with the given parity has completed; false after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait until the phase with the given parity has completed; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
 #if COLI_WAIT_SPIN
   // poll the non-blocking test: the thread sees the phase complete within a few hundred cycles
   // (a suspended try_wait can resume well after the phase completed)
@@ -89,16 +89,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_test_wait(bar, parity)) {
     __nanosleep(32);
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
   return true;
 #else
   if (mbar_try_wait_sleep(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait_sleep(bar, parity))
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   return true;
 #endif
+}
+
+// Wait until the phase with the given parity has completed, suspended in mbarrier.try_wait (the
+// thread issues nothing while the hardware holds it) instead of polling; false after limit_ns. For
+// kernels with many waiting warps, whose polling would take issue slots from the warps with work.
+__device__ __forceinline__ bool mbar_wait_suspend(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_test_parity(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_test_parity(bar, parity))
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  return true;
 }
 
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from global to shared
@@ -199,6 +210,12 @@ __device__ __forceinline__ uint4 lds128(const void* p) {
   return v;
 }
 
+__device__ __forceinline__ uint2 lds64(const void* p) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ float lds32f(const void* p) {
   float v;
   asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(smem_u32(p)) : "memory");
@@ -231,16 +248,22 @@ __device__ __forceinline__ void st_release_gpu(int* p, int v) {
 // arrivals of this and every earlier use of the same word, G = gridDim.x per use, so this use is
 // complete when the count reaches the next multiple of G above the value this CTA saw. Nothing is
 // reset, and the last CTA to arrive leaves at once. Every thread's global writes before the call
-// are visible to every thread after it. Returns false (the wait gave up after kWaitLimitNs)
-// uniformly across the CTA.
-__device__ __forceinline__ bool grid_barrier(unsigned long long* count) {
+// are visible to every thread after it. Returns false (the wait gave up after limit_ns)
+// uniformly across the CTA. `arrive` false: this CTA waits without arriving (a test of the give-up
+// path: the others then time out).
+__device__ __forceinline__ bool grid_barrier(unsigned long long* count, uint64_t limit_ns = kWaitLimitNs,
+                                             bool arrive = true) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
     const unsigned long long G = gridDim.x;
     unsigned long long old;
-    asm volatile("atom.add.release.gpu.u64 %0, [%1], 1;" : "=l"(old) : "l"(count) : "memory");
+    if (arrive) {
+      asm volatile("atom.add.release.gpu.u64 %0, [%1], 1;" : "=l"(old) : "l"(count) : "memory");
+    } else {
+      asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(old) : "l"(count) : "memory");
+    }
     const unsigned long long target = (old / G + 1) * G;
     if (old + 1 != target) {
       const uint64_t t0 = globaltimer_ns();
@@ -248,7 +271,7 @@ __device__ __forceinline__ bool grid_barrier(unsigned long long* count) {
         unsigned long long now;
         asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(now) : "l"(count) : "memory");
         if (now >= target) break;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
           ok = 0;
           break;
         }
