@@ -31,10 +31,9 @@ constexpr int kPanelCols = 16;
 
 // Device status words of a context: [0] error code, [1] router arrivals, [2..] the opt-in fused
 // decode kernel's synchronisation words (grid barrier at [2], [3]; row-range counters from
-// [2 + kSyncRanges]), [4], [5] the one-launch decode FFN's grid barrier. All start at zero; the
-// router's counter is returned to zero by its last CTA, and the grid barriers' counts only grow.
+// [2 + kSyncRanges]). All start at zero; the router's counter is returned to zero by its last CTA,
+// and the grid barrier's count only grows.
 constexpr int kSyncBase = 2;
-constexpr int kStreamBar = 4;     // the one-launch decode FFN's grid barrier (64-bit arrival count)
 constexpr int kSyncRanges = 64;   // offset of the range counters from kSyncBase
 constexpr int kMaxRanges = 4096;  // range counters
 constexpr size_t kStatusBytes = (size_t)(kSyncBase + kSyncRanges + kMaxRanges) * sizeof(int);
@@ -116,15 +115,15 @@ struct coli_ctx {
   // this device launches it (2: cooperative + programmatic dependent launch, 1: cooperative, 0: no)
   bool decode_fused = false;
   int coop_mode = -1;  // -1: not probed yet
-  // S == 1 one-launch streaming FFN (decode.cu): on unless COLI_DECODE_STREAM=0; table entries whose
-  // tensors it cannot stream (group sizes that are not multiples of 32, shapes off its grid)
+  // S == 1 streaming FFN (decode.cu): on unless COLI_DECODE_STREAM=0; table entries whose tensors it
+  // cannot stream (group sizes that are not multiples of 32, shapes off its grid)
   bool stream_ffn = true;
   int table_nostream = 0;
   std::vector<char> table_stream;  // per entry: 1 if set and streamable, or unset
   int table_gu_maxG = 0;           // most chunk groups per gate/up row of any entry set since creation
   // test hooks read at coli_init: a shorter limit for the streaming kernel's bounded waits
-  // (COLI_TEST_WAIT_NS) and, for the next N of its launches, a CTA that withholds its grid-barrier
-  // arrival so that every wait on that barrier gives up (COLI_TEST_WITHHOLD=N)
+  // (COLI_TEST_WAIT_NS) and, for the next N of its launches, a CTA whose producer withholds the copy
+  // of its first stage so that the waits on it give up (COLI_TEST_WITHHOLD=N)
   unsigned long long wait_ns = 0;
   int test_withhold = 0;
   coli::Workspace ws;
@@ -191,8 +190,8 @@ int launch_linear(coli_ctx* ctx, const TensorDesc& T, const ExpertDesc* solo, co
                   const void* resid, void* y);
 // y [S x D] (dtype) = resid + the n issued partial sums [S x D] f32, added in issue order.
 int launch_take(coli_ctx* ctx, int S, int D, int n, const void* resid, int dtype, void* y);
-// One-launch S == 1 expert FFN (decode.cu): eligibility, launch, and the per-tensor panel view
-// it streams down tensors from (built by coli_expert_table_set).
+// Streaming S == 1 expert FFN (decode.cu): eligibility, launch, and the per-tensor panel view it
+// streams down tensors from (built by coli_expert_table_set).
 bool stream_eligible(const coli_ctx* ctx, int S);
 bool stream_tensor_ok(const HostTensor& t, bool as_down);
 int build_stream_view(coli_ctx* ctx, HostTensor& t);

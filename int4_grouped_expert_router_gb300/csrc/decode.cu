@@ -1,6 +1,6 @@
 // S = 1 decode: the whole grouped int4 expert FFN of one token -- gate + up dual GEMV, SiLU(g) * u,
-// the down GEMV, per-expert weighting and a fixed-order reduce into the residual -- in one
-// persistent launch that streams every kept expert's weights once.
+// the down GEMV, per-expert weighting and a fixed-order reduce into the residual -- as one persistent
+// streaming kernel that reads every kept expert's weights once, and a small reduce kernel.
 //
 // Sources: c/backend_cuda.cu commit history, commit "The TC_W4A16 branch ..." (the grouped decode
 // path: dual gate/up GEMV, SiLU, down GEMV), commit "grouped MoE kernels were per-row-only" (per-row
@@ -13,18 +13,22 @@
 // each of its units, the 16 gate rows, the 16 up rows and the same 16 columns of down (kept
 // panel-major by the library, one contiguous [D x 8 byte] block per unit), and adds
 // w_k * scale * (the unit's down dot product) into its own partial row of y. No CTA waits for
-// another CTA's h, so each CTA's weight stream runs from its first unit to its last without a
-// dependency bubble. At the end every CTA stores its partial row, the grid meets once (a cooperative
-// launch: every CTA is resident) and CTA c adds the partial rows of its share of y in CTA order,
-// then the residual: a fixed-order, atomics-free reduce, bit-identical from run to run.
+// another CTA, so each CTA's weight stream runs from its first unit to its last without a
+// dependency bubble. Every CTA stores its partial row; the reduce kernel, chained by programmatic
+// dependent launch, adds the partial rows in CTA order and then the residual: a fixed-order,
+// atomics-free reduce, bit-identical from run to run.
 //
-// Streaming. One producer lane per CTA copies the unit's blocks into a ring of shared-memory stages
-// with bulk asynchronous copies (cp.async.bulk, completion on an mbarrier); every stage is 2 D
-// bytes: four gate or up rows (a row is D / 2 bytes), or a quarter of the down panel (D / 4 rows of
-// 8 bytes), or scales. The consumer warps (D / 512 of them, one activation chunk of 32 columns per
-// thread, two thread rows) never leave the ring: each stage is released to the producer as soon as
-// every warp has read it, and every wait suspends the warp in mbarrier.try_wait rather than polling.
-// A separate warp turns each unit's row sums into h while the consumers stream the next unit.
+// Roles inside a CTA (D = 512 NW, NW consumer warps per role):
+//   - NW gate/up warps: one 32-column chunk of x per thread (its limbs in registers), two thread
+//     rows; per unit they dot the 16 gate and 16 up rows with x and leave each warp's row sums;
+//   - one warp that turns a unit's row sums into h = SiLU(g s_g) (u s_u) and its limbs;
+//   - NW down warps: 16 rows of y per thread; per unit they dot the unit's down panel with h and
+//     accumulate w_k s_d times that into their rows of the partial;
+//   - two producer lanes that fill a gate/up ring and a down ring of shared-memory stages with bulk
+//     asynchronous copies (cp.async.bulk, completion on mbarriers).
+// The gate/up warps run ahead of the down warps by up to kHB units (the row sums and h limbs are
+// kHB-deep rings with back-pressure), so a unit's down work overlaps the next units' gate/up work on
+// other warps. Every wait is bounded and suspends in mbarrier.try_wait.
 //
 // Arithmetic: the block-fixed-point dp4a dot product of dot.h. Gate and up use 32-column chunks of
 // x; the down projection uses the unit's 16 values of h as one 16-column block (its own power-of-two
@@ -35,10 +39,9 @@
 
 namespace coli {
 
-constexpr int kStMaxStages = 32;
-constexpr int kStMinStages = 3;   // one stage read, two in flight
-constexpr int kStMaxWarps = 16;   // consumer warps: D <= 8192
-constexpr int kLag = 2;           // a unit's down stage follows the gate/up stages of the unit kLag later
+constexpr int kStMaxStages = 4;   // per ring
+constexpr int kStMaxWarps = 12;   // warps per consumer role: D <= 6144 (two stages of each ring fit)
+constexpr int kHB = 4;            // units of row sums and h limbs in flight between the roles
 
 struct StreamSlot {
   const uint8_t* gw;  // gate rows [I x D/2]
@@ -49,82 +52,126 @@ struct StreamSlot {
   const float* ds;    // down scales: [D] (per row) or transposed chunk-group scales [Gd x D]
   float wk;           // routing weight of the slot
   int gmode, umode, dmode;
-  int Gg, Gu;         // groups per gate / up row
+  int Gg, Gu;         // scales per gate / up row (1 per row, or one per chunk group)
   int gsg, gsu, gsd;  // group sizes (0: per row)
   int ok;
 };
 
 struct StreamCtrl {
-  uint64_t full[kStMaxStages];   // stage holds data (producer's expect_tx + the copies' bytes)
-  uint64_t empty[kStMaxStages];  // every consumer warp has read the stage
-  uint64_t redf[kLag + 1];       // every consumer thread has stored its row sums of unit n (buffer n % 3)
-  uint64_t hlf[kLag + 1];        // the h warp has stored the limbs of that unit's h
+  uint64_t full_g[kStMaxStages], empty_g[kStMaxStages];  // gate/up ring
+  uint64_t full_d[kStMaxStages], empty_d[kStMaxStages];  // down ring
+  uint64_t redf[kHB], redfree[kHB];  // row sums of unit n stored (buffer n % kHB) / read by the h warp
+  uint64_t hlf[kHB], hlfree[kHB];    // h limbs of unit n stored / read by every down warp
   StreamSlot slot[COLI_MAX_K];
-  float red[kLag + 1][kStMaxWarps][16];  // per consumer warp: its 8 gate and 8 up row sums of a unit
-  Limbs16 hl[kLag + 1];                  // h of a unit as one 16-column block of limbs
-  float fold[32 * (kStMaxWarps + 2)];  // final reduce: group sums
+  float red[kHB][kStMaxWarps][16];   // per gate/up warp: its 8 gate and 8 up row sums of a unit
+  float fs[kHB][2][16];              // per-row gate and up scales of a unit's 16 rows (1 for chunk scales)
+  Limbs16 hl[kHB];                   // h of a unit as one 16-column block of limbs
   int m;
 };
 
 struct StreamParams {
   const void* x;
-  int x_dtype, y_dtype;
+  int x_dtype;
   int D, I, K;
   const int32_t* idx;
   const float* w;
   const int32_t* n_sel;
   const ExpertDesc* table;
-  const void* resid;
-  void* y;
   float* part;               // [gridDim.x x D] partial rows
-  unsigned long long* bar;   // grid barrier count (monotonic)
   int* err;
-  int nst;                   // ring stages
-  uint32_t sb;               // stage bytes: 16 gate/up rows and their chunk scales, a down panel (8 D)
+  int nsg, nsd;              // stages of the gate/up ring and of the down ring
+  uint32_t sbg, sbd;         // their stage bytes
   unsigned long long wait_ns;
-  int withhold;              // test hook: CTA 0 does not arrive at the grid barrier
+  int withhold;              // test hook: the CTA owning unit 0 withholds the copy of its first gate stage
 };
 
-// Warp roles: warps 0 .. NW-1 consume the ring (NW = D / 512), warp NW is the producer (one lane
-// issues every copy), warp NW + 1 turns each unit's row sums into h and its limbs.
-//
-// Order of a CTA's stream, for its kept units n = 0, 1, ... (unit n: slot j, rows i0 .. i0 + 15),
-// one stage each:
-//   gate rows i0 .. i0 + 15 (+ their chunk-group scales), up rows (+ scales), then for unit n - 2 its
-//   down scales when they change (a new slot, or chunk-group scales) and its down panel;
-// and finally the down scales and panels of the last two units. A unit's down stage thus follows the
-// gate/up stages of the next two units: while the consumers stream those, the h warp turns its row
-// sums into h, and no consumer waits for another. Stages are large (a whole unit's gate rows, 8 D
-// bytes) so that each wait and release is paid for by eight independent chunk dot products per
-// thread.
+// Limbs of 16 values of h held by lanes 0..15 (lanes 16..31 hold 0); every lane returns the same
+// limbs: lane 8 w + 2 b + p holds column 8 w + 2 b + p, whose digits go to byte b of word (w, p).
+__device__ __forceinline__ bool warp_limbs16(float h, int lane, Limbs16& L) {
+  float M = fabsf(h);
+  const bool bad = !(fmaf(h, 0.f, 0.f) == 0.f);  // NaN or infinite
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  const bool finite = !__any_sync(0xffffffffu, bad);
+  int e = 0;
+  if (finite && M > 0.f) frexpf(M, &e);  // M < 2^e
+  int q = 22 - e;                         // M 2^q in [2^21, 2^22)
+  q = q > 122 ? 122 : q;
+  const float scale = (finite && M > 0.f) ? __int_as_float((127 + q) << 23) : 0.f;
+  const int xi = __float2int_rn(h * scale);
+  const uint32_t z = ((uint32_t)xi + 0x808080u) ^ 0x808080u;
+#pragma unroll
+  for (int w = 0; w < 2; w++)
+#pragma unroll
+    for (int p = 0; p < 2; p++) {
+      const uint32_t z0 = __shfl_sync(0xffffffffu, z, 8 * w + p), z1 = __shfl_sync(0xffffffffu, z, 8 * w + 2 + p);
+      const uint32_t z2 = __shfl_sync(0xffffffffu, z, 8 * w + 4 + p), z3 = __shfl_sync(0xffffffffu, z, 8 * w + 6 + p);
+      const uint32_t a01 = prmt(z0, z1, 0x5140u), a23 = prmt(z2, z3, 0x5140u);
+      const uint32_t c01 = prmt(z0, z1, 0x6262u), c23 = prmt(z2, z3, 0x6262u);
+      L.r[w][p][0] = prmt(a01, a23, 0x5410u);
+      L.r[w][p][1] = prmt(a01, a23, 0x7632u);
+      L.r[w][p][2] = prmt(c01, c23, 0x5410u);
+    }
+#pragma unroll
+  for (int l = 0; l < 3; l++) {
+    int se = 0, so = 0;
+#pragma unroll
+    for (int w = 0; w < 2; w++) {
+      se = dp4a_ss(L.r[w][0][l], 0x01010101u, se);
+      so = dp4a_ss(L.r[w][1][l], 0x01010101u, so);
+    }
+    L.a0[l] = -8 * se;
+    L.b0[l] = -128 * so;
+  }
+  L.k01 = (finite && M > 0.f) ? __int_as_float((127 - q - 4) << 23) : 0.f;
+  L.k2 = (finite && M > 0.f) ? __int_as_float((127 + 12 - q) << 23) : 0.f;
+  return finite;
+}
+
+// Bounded wait that records COLI_E_TIMEOUT and sets `stop` when it gives up (a stopped role waits
+// no more and its results are discarded: the call reports the error).
+__device__ __forceinline__ void role_wait(uint64_t* bar, uint32_t parity, uint64_t lim, bool& stop, int* err) {
+  if (!stop && !mbar_wait_suspend(bar, parity, lim)) {
+    stop = true;
+    set_error(err, COLI_E_TIMEOUT);
+  }
+}
+
 template <int MAXT>
 __global__ void __launch_bounds__(MAXT, 1) stream_ffn_kernel(const StreamParams P) {
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 127) & ~uintptr_t(127));
   StreamCtrl& cs = *reinterpret_cast<StreamCtrl*>(base);
-  uint8_t* ring = base + (sizeof(StreamCtrl) + 127) / 128 * 128;
+  uint8_t* ring_g = base + (sizeof(StreamCtrl) + 127) / 128 * 128;
+  uint8_t* ring_d = ring_g + (size_t)P.nsg * P.sbg;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int D = P.D, NW = D / 512, NCT = 32 * NW;  // consumer warps and threads
+  const int D = P.D, NW = D / 512, NCT = 32 * NW;  // warps and threads of a consumer role
   const int C = D / 32;                            // activation chunks = 16 NW
-  const uint32_t SB = P.sb;                        // stage bytes
   const uint32_t pitch = (uint32_t)D / 2;          // bytes of a gate/up row
   const uint32_t rows_bytes = 16u * pitch;         // a unit's 16 gate (or up) rows = its down panel
-  const int NST = P.nst;
+  const int NSG = P.nsg, NSD = P.nsd;
   const uint64_t lim = P.wait_ns ? P.wait_ns : kWaitLimitNs;
+  const int W_PG = 2 * NW, W_PD = 2 * NW + 1, W_H = 2 * NW + 2;  // producer warps and the h warp
 
   if (tid == 0) {
-    for (int s = 0; s < NST; s++) {
-      mbar_init(&cs.full[s], 1);
-      mbar_init(&cs.empty[s], NW);
+    for (int s = 0; s < NSG; s++) {
+      mbar_init(&cs.full_g[s], 1);
+      mbar_init(&cs.empty_g[s], NW);
     }
-    for (int b = 0; b <= kLag; b++) {
+    for (int s = 0; s < NSD; s++) {
+      mbar_init(&cs.full_d[s], 1);
+      mbar_init(&cs.empty_d[s], NW);
+    }
+    for (int b = 0; b < kHB; b++) {
       mbar_init(&cs.redf[b], NCT);
+      mbar_init(&cs.redfree[b], 1);
       mbar_init(&cs.hlf[b], 1);
+      mbar_init(&cs.hlfree[b], NW);
     }
     mbar_fence_init();
   }
-  // consumer prologue, overlapping the router's tail: the limbs of this thread's chunk of x
-  const int c = tid % C, r0 = tid / C;  // consumers: r0 in {0, 1}
+  // gate/up prologue, overlapping the router's tail: the limbs of this thread's chunk of x
+  const int c = tid % C, r0 = tid / C;  // gate/up threads: r0 in {0, 1}
   Limbs X;
   if (warp < NW) {
     float xv[32];
@@ -164,8 +211,7 @@ __global__ void __launch_bounds__(MAXT, 1) stream_ffn_kernel(const StreamParams 
       sl.wk = ld_cg_f32(P.w + tid);
       // the host launches this kernel only for tables it can stream; anything else is a bad entry
       if (sl.gmode == SCALE_GENERIC || sl.umode == SCALE_GENERIC || sl.dmode == SCALE_GENERIC || !sl.dp ||
-          !sl.ds || (sl.gmode == SCALE_CHUNK && rows_bytes + 64u * sl.Gg > SB) ||
-          (sl.umode == SCALE_CHUNK && rows_bytes + 64u * sl.Gu > SB)) {
+          !sl.ds || rows_bytes + 64u * sl.Gg > P.sbg || rows_bytes + 64u * sl.Gu > P.sbg) {
         ok = false;
         set_error(P.err, COLI_E_ROUTE);
       }
@@ -173,286 +219,219 @@ __global__ void __launch_bounds__(MAXT, 1) stream_ffn_kernel(const StreamParams 
     sl.ok = ok;
   }
   __syncthreads();
-  griddep_launch_dependents();
+  griddep_launch_dependents();  // the reduce kernel may launch; it waits for this grid to finish
 
   const int UB = P.I / kPanelCols;  // units per slot
   const long long total = (long long)m * UB;
   const int ubeg = (int)((long long)blockIdx.x * total / gridDim.x);
   const int uend = (int)((long long)(blockIdx.x + 1) * total / gridDim.x);
+  bool stop = false;
 
-  if (warp == NW) {
-    // ---------------- producer: one lane issues every copy of this CTA's units ----------------
+  if (warp == W_PG || warp == W_PD) {
+    // ---------------- producers: one lane per ring issues its copies in unit order ----------------
     if (lane == 0) {
+      const bool gu = warp == W_PG;
       const uint64_t pol = l2_evict_first_policy();
+      uint64_t* full = gu ? cs.full_g : cs.full_d;
+      uint64_t* empty = gu ? cs.empty_g : cs.empty_d;
+      uint8_t* ring = gu ? ring_g : ring_d;
+      const int NS = gu ? NSG : NSD;
+      const uint32_t SB = gu ? P.sbg : P.sbd;
       uint32_t q = 0, s = 0, ph = 0;  // stage sequence number, its slot and the slot's use parity
-      bool pstop = false;
-      // one stage of up to two pieces (weights, then their chunk scales) on one barrier
+      bool withhold = gu && P.withhold && ubeg == 0 && uend > 0;  // the CTA that owns unit 0
+      // one stage of up to two pieces (weights, then their scales) on one barrier
       auto issue = [&](const void* src, uint32_t bytes, const void* src2, uint32_t bytes2, bool weights) {
-        if (pstop) return;
-        if (q >= (uint32_t)NST && !mbar_wait_suspend(&cs.empty[s], ph ^ 1u, lim)) {
-          pstop = true;
-          set_error(P.err, COLI_E_TIMEOUT);
-          return;
-        }
-        mbar_arrive_expect_tx(&cs.full[s], bytes + bytes2);
+        if (stop) return;
+        if (q >= (uint32_t)NS) role_wait(&empty[s], ph ^ 1u, lim, stop, P.err);
+        if (stop) return;
+        mbar_arrive_expect_tx(&full[s], bytes + bytes2);
         uint8_t* dst = ring + (size_t)s * SB;
-        if (weights)
-          bulk_g2s_stream(dst, src, bytes, &cs.full[s], pol);
-        else
-          bulk_g2s(dst, src, bytes, &cs.full[s]);
-        if (bytes2) bulk_g2s(dst + bytes, src2, bytes2, &cs.full[s]);
+        if (withhold) {  // test hook: the stage never fills, so its consumers' bounded waits give up
+          withhold = false;
+        } else {
+          if (weights)
+            bulk_g2s_stream(dst, src, bytes, &full[s], pol);
+          else
+            bulk_g2s(dst, src, bytes, &full[s]);
+          if (bytes2) bulk_g2s(dst + bytes, src2, bytes2, &full[s]);
+        }
         q++;
-        if (++s == (uint32_t)NST) {
+        if (++s == (uint32_t)NS) {
           s = 0;
           ph ^= 1u;
         }
       };
-      // the (at most kLag = 2) units whose down stages are still to come, oldest first: slot, block and
-      // whether their down scales change
-      int aj = 0, ab = 0, ad = 0, bj = 0, bbk = 0, bd = 0;
-      auto issue_down = [&](int j, int b, int dsc) {
-        const StreamSlot& sd = cs.slot[j];
-        if (dsc)
-          issue(sd.dmode == SCALE_CHUNK ? sd.ds + (size_t)(b * kPanelCols / sd.gsd) * D : sd.ds, 4u * D, nullptr, 0u,
-                false);
-        issue(sd.dp + (size_t)b * rows_bytes, rows_bytes, nullptr, 0u, true);
-      };
-      int prev = -1, n = 0;
-      for (int u = ubeg; u < uend && !pstop; u++) {
+      int prev = -1;
+      for (int u = ubeg; u < uend && !stop; u++) {
         const int j = u / UB, b = u - j * UB;
         const StreamSlot& sl = cs.slot[j];
         if (!sl.ok) continue;
         const int i0 = b * kPanelCols;
-        const bool gch = sl.gmode == SCALE_CHUNK, uch = sl.umode == SCALE_CHUNK;
-        issue(sl.gw + (size_t)i0 * pitch, rows_bytes, sl.gs + (size_t)i0 * sl.Gg, gch ? 64u * sl.Gg : 0u, true);
-        issue(sl.uw + (size_t)i0 * pitch, rows_bytes, sl.us + (size_t)i0 * sl.Gu, uch ? 64u * sl.Gu : 0u, true);
-        const int dsc = sl.dmode == SCALE_CHUNK || j != prev;
-        prev = j;
-        if (n >= kLag) {  // the oldest pending unit's down stages; then shift the pending pair
-          issue_down(aj, ab, ad);
-          aj = bj, ab = bbk, ad = bd;
-          bj = j, bbk = b, bd = dsc;
-        } else if (n == 1) {
-          bj = j, bbk = b, bd = dsc;
+        if (gu) {  // the rows, then their 16 row scales or 16 rows of chunk-group scales
+          issue(sl.gw + (size_t)i0 * pitch, rows_bytes, sl.gs + (size_t)i0 * sl.Gg, 64u * sl.Gg, true);
+          issue(sl.uw + (size_t)i0 * pitch, rows_bytes, sl.us + (size_t)i0 * sl.Gu, 64u * sl.Gu, true);
         } else {
-          aj = j, ab = b, ad = dsc;
+          if (sl.dmode == SCALE_CHUNK || j != prev)  // down scales when they change
+            issue(sl.dmode == SCALE_CHUNK ? sl.ds + (size_t)(i0 / sl.gsd) * D : sl.ds, 4u * D, nullptr, 0u, false);
+          issue(sl.dp + (size_t)b * rows_bytes, rows_bytes, nullptr, 0u, true);
         }
-        n++;
+        prev = j;
       }
-      if (n >= 1) issue_down(aj, ab, ad);
-      if (n >= 2) issue_down(bj, bbk, bd);
-      // never leave with copies in flight into the ring
-      for (uint32_t r = q > (uint32_t)NST ? q - NST : 0; r < q; r++)
-        (void)mbar_wait_suspend(&cs.full[r % NST], (r / NST) & 1, lim);
+      // never leave with copies in flight into the ring (a withheld stage is given up on, bounded)
+      for (uint32_t r = q > (uint32_t)NS ? q - NS : 0; r < q; r++)
+        (void)mbar_wait_suspend(&full[r % NS], (r / NS) & 1, lim);
     }
-  } else if (warp == NW + 1) {
-    // ---------------- h warp: row sums of a unit -> h = SiLU(g s_g) (u s_u) -> limbs ----------------
-    bool stop = false;
+  } else if (warp == W_H) {
+    // ---------------- h warp: row sums -> h = SiLU(g s_g) (u s_u) -> limbs ----------------
     int n = 0;
-    // row scales of the next kept unit's row i0 + lane (1 for chunk scales, applied per chunk), loaded
-    // one unit ahead so that their latency hides behind the current unit
-    int u = ubeg;
-    auto next_scales = [&](float& fg, float& fu) {
-      fg = fu = 1.f;
-      for (; u < uend; u++) {
-        const int j = u / UB;
-        const StreamSlot& sl = cs.slot[j];
-        if (!sl.ok) continue;
-        const int i0 = (u - j * UB) * kPanelCols;
-        if (lane < 16) {
-          if (sl.gmode == SCALE_ROW) fg = __ldg(sl.gs + i0 + lane);
-          if (sl.umode == SCALE_ROW) fu = __ldg(sl.us + i0 + lane);
-        }
-        u++;
-        return true;
-      }
-      return false;
-    };
-    float fg, fu;
-    bool have = next_scales(fg, fu);
-    while (have) {
-      float fg_next, fu_next;
-      const bool have_next = next_scales(fg_next, fu_next);
-      const int bb = n % (kLag + 1);
-      const bool ok = stop || mbar_wait_suspend(&cs.redf[bb], (n / (kLag + 1)) & 1, lim);
-      if (__any_sync(0xffffffffu, !ok) && !stop) {
-        stop = true;
-        if (lane == 0) set_error(P.err, COLI_E_TIMEOUT);
-      }
+    for (int u = ubeg; u < uend; u++) {
+      if (!cs.slot[u / UB].ok) continue;
+      const int b = n % kHB;
+      const uint32_t use = (uint32_t)(n / kHB);
+      role_wait(&cs.redf[b], use & 1, lim, stop, P.err);
       float h = 0.f;
-      if (lane < 16 && !stop) {
+      if (lane < 16) {
         // row `lane` = r0 + 2 i of the unit is value i (gate) and 8 + i (up) of the warps with that r0
         const int rg = lane & 1, v = lane >> 1;
         float g = 0.f, uu = 0.f;
         for (int w = rg * (NW / 2); w < (rg + 1) * (NW / 2); w++) {
-          g += cs.red[bb][w][v];
-          uu += cs.red[bb][w][8 + v];
+          g += cs.red[b][w][v];
+          uu += cs.red[b][w][8 + v];
         }
-        h = silu_mul(g * fg, uu * fu);
+        h = silu_mul(g * cs.fs[b][0][lane], uu * cs.fs[b][1][lane]);
       }
-      float hv[16];
-#pragma unroll
-      for (int i = 0; i < 16; i++) hv[i] = __shfl_sync(0xffffffffu, h, i);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&cs.redfree[b]);  // the gate/up warps may refill buffer b
       Limbs16 L;
-      const bool fin = make_limbs(hv, L);
+      const bool fin = warp_limbs16(h, lane, L);
+      if (use >= 1) role_wait(&cs.hlfree[b], (use - 1) & 1, lim, stop, P.err);
       if (lane == 0) {
         if (!fin && !stop) set_error(P.err, COLI_E_NONFINITE);
-        cs.hl[bb] = L;
-        mbar_arrive(&cs.hlf[bb]);
+        cs.hl[b] = L;
+        mbar_arrive(&cs.hlf[b]);
       }
       n++;
-      fg = fg_next;
-      fu = fu_next;
-      have = have_next;
     }
-  } else {
-    // ---------------- consumers ----------------
+  } else if (warp < NW) {
+    // ---------------- gate/up warps ----------------
+    uint32_t s = 0, ph = 0;  // ring slot of the next stage and its use parity
+    int n = 0;
+    for (int u = ubeg; u < uend; u++) {
+      const StreamSlot& sl = cs.slot[u / UB];
+      if (!sl.ok) continue;
+      const int b = n % kHB;
+      const uint32_t use = (uint32_t)(n / kHB);
+      // gate, then up: rows r0 + 2 i (i < 8) of the unit, this thread's chunk; the stage's 16 rows are
+      // followed by their scales (one per row, or one per chunk group and row). Each stage's eight values
+      // are summed over the warp at once: lanes 4 i .. 4 i + 3 end with value i, gate (or up) row r0 + 2 i.
+#pragma unroll
+      for (int t = 0; t < 2; t++) {
+        role_wait(&cs.full_g[s], ph, lim, stop, P.err);
+        const uint8_t* st = ring_g + (size_t)s * P.sbg;
+        const float* sc = reinterpret_cast<const float*>(st + rows_bytes);
+        const int mode = t ? sl.umode : sl.gmode, G = t ? sl.Gu : sl.Gg;
+        const int grp = mode == SCALE_CHUNK ? (32 * c) / (t ? sl.gsu : sl.gsg) : 0;
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+          float d = chunk_dot(lds128(st + (r0 + 2 * i) * pitch + 16 * c), X);
+          if (mode == SCALE_CHUNK) d *= sc[(r0 + 2 * i) * G + grp];
+          v[i] = d;
+        }
+        if (t == 0 && use >= 1) role_wait(&cs.redfree[b], (use - 1) & 1, lim, stop, P.err);  // buffer b is free
+        if (warp == 0 && lane < 16) cs.fs[b][t][lane] = mode == SCALE_ROW ? sc[lane] : 1.f;
+        __syncwarp();
+        if (lane == 0 && !stop) mbar_arrive(&cs.empty_g[s]);
+        if (++s == (uint32_t)NSG) {
+          s = 0;
+          ph ^= 1u;
+        }
+        warp_transpose_reduce<8>(v, lane);
+        if (!(lane & 3)) cs.red[b][warp][8 * t + (lane >> 2)] = v[0];
+      }
+      mbar_arrive(&cs.redf[b]);
+      n++;
+    }
+  } else if (warp < 2 * NW) {
+    // ---------------- down warps ----------------
+    const int td = tid - NCT;  // rows td + jj NCT of y
     float acc[16], ws[16];
 #pragma unroll
     for (int i = 0; i < 16; i++) {
       acc[i] = 0.f;
       ws[i] = 0.f;
     }
-    uint32_t s = 0, ph = 0;  // ring slot of the next stage and its use parity
-    bool stop = false;
-    auto wait_stage = [&]() -> const uint8_t* {
-      if (!stop && !mbar_wait_suspend(&cs.full[s], ph, lim)) {
-        stop = true;
-        set_error(P.err, COLI_E_TIMEOUT);
-      }
-      return ring + (size_t)s * SB;
-    };
-    auto release_stage = [&]() {
-      __syncwarp();
-      if (lane == 0 && !stop) mbar_arrive(&cs.empty[s]);
-      if (++s == (uint32_t)NST) {
+    uint32_t s = 0, ph = 0;
+    auto next_stage = [&]() {
+      if (++s == (uint32_t)NSD) {
         s = 0;
         ph ^= 1u;
       }
     };
-    // the (at most kLag = 2) units whose down stages are still to come, oldest first: slot and whether
-    // their down scales change
-    int aj = 0, ad = 0, bj = 0, bd = 0;
-    // the down part of this CTA's kept unit nn (slot j): w_k times the down scales of this thread's 16
-    // rows when they change, then rows tid + jj NCT of the unit's panel, columns i0 .. i0 + 15
-    auto do_down = [&](int nn, int j, int dsc) {
-      const int bb = nn % (kLag + 1);
-      if (dsc) {
-        const float wk = cs.slot[j].wk;
-        const float* sd = reinterpret_cast<const float*>(wait_stage());
-#pragma unroll
-        for (int jj = 0; jj < 16; jj++) ws[jj] = wk * sd[tid + jj * NCT];
-        release_stage();
-      }
-      if (!stop && !mbar_wait_suspend(&cs.hlf[bb], (nn / (kLag + 1)) & 1, lim)) {
-        stop = true;
-        set_error(P.err, COLI_E_TIMEOUT);
-      }
-      const Limbs16 HL = cs.hl[bb];
-      const uint8_t* st = wait_stage();
-#pragma unroll
-      for (int jj = 0; jj < 16; jj++) {
-        const uint2 wv = lds64(st + (size_t)(tid + jj * NCT) * 8);
-        acc[jj] = fmaf(ws[jj], chunk_dot16(wv, HL), acc[jj]);
-      }
-      release_stage();
-    };
-    int prev = -1, n = 0;
+    int n = 0, prev = -1;
     for (int u = ubeg; u < uend; u++) {
       const int j = u / UB;
       const StreamSlot& sl = cs.slot[j];
       if (!sl.ok) continue;
-      const int bb = n % (kLag + 1);
-      const int dsc = sl.dmode == SCALE_CHUNK || j != prev;
+      const int b = n % kHB;
+      const uint32_t use = (uint32_t)(n / kHB);
+      if (sl.dmode == SCALE_CHUNK || j != prev) {  // w_k times the down scales of this thread's rows
+        role_wait(&cs.full_d[s], ph, lim, stop, P.err);
+        const float* sd = reinterpret_cast<const float*>(ring_d + (size_t)s * P.sbd);
+#pragma unroll
+        for (int jj = 0; jj < 16; jj++) ws[jj] = sl.wk * sd[td + jj * NCT];
+        __syncwarp();
+        if (lane == 0 && !stop) mbar_arrive(&cs.empty_d[s]);
+        next_stage();
+      }
       prev = j;
-      // gate, then up: rows r0 + 2 i (i < 8) of the unit, this thread's chunk; chunk-group scales
-      // follow the 16 rows in the stage
-      float v[16];
-      {
-        const uint8_t* st = wait_stage();
-        const float* sc = reinterpret_cast<const float*>(st + rows_bytes);
-        const int gg = sl.gmode == SCALE_CHUNK ? (32 * c) / sl.gsg : 0;
+      role_wait(&cs.hlf[b], use & 1, lim, stop, P.err);
+      const Limbs16 HL = cs.hl[b];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&cs.hlfree[b]);
+      role_wait(&cs.full_d[s], ph, lim, stop, P.err);
+      const uint8_t* st = ring_d + (size_t)s * P.sbd;
 #pragma unroll
-        for (int i = 0; i < 8; i++) {
-          v[i] = chunk_dot(lds128(st + (r0 + 2 * i) * pitch + 16 * c), X);
-          if (sl.gmode == SCALE_CHUNK) v[i] *= sc[(r0 + 2 * i) * sl.Gg + gg];
-        }
-        release_stage();
+      for (int jj = 0; jj < 16; jj++) {
+        const uint2 wv = lds64(st + (size_t)(td + jj * NCT) * 8);
+        acc[jj] = fmaf(ws[jj], chunk_dot16(wv, HL), acc[jj]);
       }
-      {
-        const uint8_t* st = wait_stage();
-        const float* sc = reinterpret_cast<const float*>(st + rows_bytes);
-        const int gu = sl.umode == SCALE_CHUNK ? (32 * c) / sl.gsu : 0;
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-          v[8 + i] = chunk_dot(lds128(st + (r0 + 2 * i) * pitch + 16 * c), X);
-          if (sl.umode == SCALE_CHUNK) v[8 + i] *= sc[(r0 + 2 * i) * sl.Gu + gu];
-        }
-        release_stage();
-      }
-      // lanes 2 i, 2 i + 1 end with the warp total of value i: gate row r0 + 2 i (i < 8) or up row
-      // r0 + 2 (i - 8); the h warp takes it from here
-      warp_transpose_reduce<16>(v, lane);
-      if (!(lane & 1)) cs.red[bb][warp][lane >> 1] = v[0];
-      mbar_arrive(&cs.redf[bb]);
-      if (n >= kLag) {  // the oldest pending unit's down part; then shift the pending pair
-        do_down(n - kLag, aj, ad);
-        aj = bj, ad = bd;
-        bj = j, bd = dsc;
-      } else if (n == 1) {
-        bj = j, bd = dsc;
-      } else {
-        aj = j, ad = dsc;
-      }
+      __syncwarp();
+      if (lane == 0 && !stop) mbar_arrive(&cs.empty_d[s]);
+      next_stage();
       n++;
-    }
-    if (n >= 2) {
-      do_down(n - 2, aj, ad);
-      do_down(n - 1, bj, bd);
-    } else if (n == 1) {
-      do_down(0, aj, ad);
     }
     float* prow = P.part + (size_t)blockIdx.x * D;
 #pragma unroll
-    for (int jj = 0; jj < 16; jj++) prow[tid + jj * NCT] = acc[jj];
+    for (int jj = 0; jj < 16; jj++) prow[td + jj * NCT] = acc[jj];
   }
+}
 
-  // ---------------- every CTA's partial row is stored: fixed-order reduce ----------------
-  const bool arrive = !(P.withhold && blockIdx.x == 0);
-  if (!grid_barrier(P.bar, lim, arrive)) {
-    if (tid == 0) set_error(P.err, COLI_E_TIMEOUT);
-    return;
-  }
-  if (!arrive) return;
-  const int G = gridDim.x, nthr = blockDim.x;
-  const int d0 = (int)((long long)blockIdx.x * D / G), d1 = (int)((long long)(blockIdx.x + 1) * D / G);
-  const int nd = d1 - d0;
-  if (nd <= 0) return;
-  const int groups = max(1, min(G, nthr / nd));  // partial rows split into `groups` runs of CTAs
-  const int wd = nthr / groups;                  // values of y per pass
-  for (int pb = d0; pb < d1; pb += wd) {
-    const int dl = tid % wd, grp = tid / wd, d = pb + dl;
-    if (grp < groups) {
-      float s = 0.f;
-      if (d < d1) {
-        const int c0 = (int)((long long)grp * G / groups), c1 = (int)((long long)(grp + 1) * G / groups);
+// y[d] = resid[d] + (sum over the G partial rows of column d, in CTA order). A CTA takes 32 columns;
+// its eight warps add eight consecutive runs of the partial rows, then the runs are added in order.
+__global__ void __launch_bounds__(256) stream_reduce_kernel(const float* __restrict__ part, int G, int D,
+                                                            const void* resid, int x_dtype, void* y, int y_dtype) {
+  __shared__ float fold[8][32];
+  griddep_wait();  // every partial row is stored
+  const int dl = threadIdx.x & 31, grp = threadIdx.x >> 5;
+  const int d = blockIdx.x * 32 + dl;
+  float s = 0.f;
+  if (d < D) {
+    const int c0 = grp * G / 8, c1 = (grp + 1) * G / 8;
 #pragma unroll 8
-        for (int cc = c0; cc < c1; cc++) s += __ldcg(P.part + (size_t)cc * D + d);
-      }
-      cs.fold[grp * wd + dl] = s;
-    }
-    __syncthreads();
-    if (tid < wd && pb + tid < d1) {
-      const int dd = pb + tid;
-      float tot = 0.f;
-      for (int g2 = 0; g2 < groups; g2++) tot += cs.fold[g2 * wd + tid];
-      if (P.resid) tot = load_act(P.resid, P.x_dtype, dd) + tot;
-      if (P.y_dtype == COLI_DTYPE_F32)
-        static_cast<float*>(P.y)[dd] = tot;
-      else
-        static_cast<uint16_t*>(P.y)[dd] = f32_to_bf16_rn(tot);
-    }
-    __syncthreads();
+    for (int cc = c0; cc < c1; cc++) s += __ldcg(part + (size_t)cc * D + d);
+  }
+  fold[grp][dl] = s;
+  __syncthreads();
+  if (grp == 0 && d < D) {
+    float tot = fold[0][dl];
+#pragma unroll
+    for (int g2 = 1; g2 < 8; g2++) tot += fold[g2][dl];
+    if (resid) tot = load_act(resid, x_dtype, d) + tot;
+    if (y_dtype == COLI_DTYPE_F32)
+      static_cast<float*>(y)[d] = tot;
+    else
+      static_cast<uint16_t*>(y)[d] = f32_to_bf16_rn(tot);
   }
 }
 
@@ -520,39 +499,51 @@ int build_stream_view(coli_ctx* ctx, HostTensor& t) {
   return COLI_OK;
 }
 
+// Ring sizes: a gate/up stage holds a unit's 16 rows and their scales, a down stage a unit's panel
+// (or its down scales); both rings get the same number of stages, as many as fit.
+static bool stream_rings(const coli_ctx* ctx, int D, uint32_t& sbg, uint32_t& sbd, int& ns, size_t& smem) {
+  int maxsm = 0;
+  if (cudaDeviceGetAttribute(&maxsm, cudaDevAttrMaxSharedMemoryPerBlockOptin, ctx->device) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  const int gmax = ctx->table_gu_maxG > 1 ? ctx->table_gu_maxG : 1;
+  sbg = (uint32_t)align_up(8u * (uint32_t)D + 64u * (uint32_t)gmax, 128);
+  sbd = 8u * (uint32_t)D;
+  const long long room = (long long)maxsm - 128 - (long long)stream_ctrl_bytes();
+  ns = (int)(room / ((long long)sbg + sbd));
+  if (ns > kStMaxStages) ns = kStMaxStages;
+  smem = 128 + stream_ctrl_bytes() + (size_t)ns * (sbg + sbd);
+  return ns >= 2;
+}
+
 bool stream_eligible(const coli_ctx* ctx, int S) {
   const int D = ctx->table_D, I = ctx->table_I;
-  return S == 1 && ctx->stream_ffn && !ctx->decode_fused && ctx->coop_mode > 0 && ctx->table_count > 0 &&
-         ctx->table_nostream == 0 && D % 1024 == 0 && D <= 512 * kStMaxWarps && I % kPanelCols == 0;
+  uint32_t sbg, sbd;
+  int ns;
+  size_t smem;
+  return S == 1 && ctx->stream_ffn && !ctx->decode_fused && ctx->table_count > 0 && ctx->table_nostream == 0 &&
+         D % 1024 == 0 && D <= 512 * kStMaxWarps && I % kPanelCols == 0 && stream_rings(ctx, D, sbg, sbd, ns, smem);
 }
 
 int launch_stream_ffn(coli_ctx* ctx, const void* x, int x_dtype, const int32_t* idx, const float* w,
                       const int32_t* n_sel, int K, const void* resid, void* y, int y_dtype) {
   const int D = ctx->table_D, I = ctx->table_I;
-  const int NW = D / 512, threads = 32 * (NW + 2);
-  // a unit's 16 gate (or up) rows and their chunk-group scales; the down panel and down scales are smaller
-  const uint32_t SB = (uint32_t)align_up(8u * (uint32_t)D + 64u * (uint32_t)ctx->table_gu_maxG, 128);
-  int maxsm = 0;
-  cudaError_t e = cudaDeviceGetAttribute(&maxsm, cudaDevAttrMaxSharedMemoryPerBlockOptin, ctx->device);
-  if (e != cudaSuccess) return cuda_fail(ctx, e, "stream FFN: shared memory limit");
-  const long long room = (long long)maxsm - 128 - (long long)stream_ctrl_bytes();
-  int nst = (int)(room / SB);
-  if (nst > kStMaxStages) nst = kStMaxStages;
-  if (nst < kStMinStages) return fail(ctx, COLI_E_INVAL, "stream FFN: not enough shared memory for the ring");
-  const size_t smem = 128 + stream_ctrl_bytes() + (size_t)nst * SB;
-  auto kern = threads <= 320 ? stream_ffn_kernel<320> : (threads <= 448 ? stream_ffn_kernel<448> : stream_ffn_kernel<576>);
+  const int NW = D / 512, threads = 32 * (2 * NW + 3);
+  uint32_t sbg, sbd;
+  int ns;
+  size_t smem;
+  if (!stream_rings(ctx, D, sbg, sbd, ns, smem)) return fail(ctx, COLI_E_INVAL, "stream FFN: rings do not fit");
+  auto kern = threads <= 480 ? stream_ffn_kernel<480> : stream_ffn_kernel<864>;
+  cudaError_t e;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
     return cuda_fail(ctx, e, "stream FFN: shared memory attribute");
-  int occ = 0;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem)) != cudaSuccess || occ < 1)
-    return e != cudaSuccess ? cuda_fail(ctx, e, "stream FFN: occupancy") : fail(ctx, COLI_E_CUDA, "stream FFN: no residency");
   const int G = ctx->num_sms;
   int rc = ensure_workspace(ctx, (size_t)G * D * sizeof(float));
   if (rc != COLI_OK) return rc;
   StreamParams P;
   P.x = x;
   P.x_dtype = x_dtype;
-  P.y_dtype = y_dtype;
   P.D = D;
   P.I = I;
   P.K = K;
@@ -560,19 +551,25 @@ int launch_stream_ffn(coli_ctx* ctx, const void* x, int x_dtype, const int32_t* 
   P.w = w;
   P.n_sel = n_sel;
   P.table = ctx->d_table;
-  P.resid = resid;
-  P.y = y;
   P.part = reinterpret_cast<float*>(ctx->ws.base);
-  P.bar = reinterpret_cast<unsigned long long*>(ctx->d_status + kStreamBar);
   P.err = ctx->d_status;
-  P.nst = nst;
-  P.sb = SB;
+  P.nsg = P.nsd = ns;
+  P.sbg = sbg;
+  P.sbd = sbd;
   P.wait_ns = ctx->wait_ns;
   P.withhold = ctx->test_withhold > 0;  // one-shot: only the next launch withholds
   if (ctx->test_withhold > 0) ctx->test_withhold--;
-  ProfScope prof(ctx, COLI_KERNEL_GATEUP);
-  e = launch_k(kern, G, threads, smem, ctx->stream, ctx->coop_mode == 2, true, P);
+  {
+    ProfScope prof(ctx, COLI_KERNEL_GATEUP);
+    e = launch_k(kern, G, threads, smem, ctx->stream, true, false, P);
+  }
   if (e != cudaSuccess) return cuda_fail(ctx, e, "stream FFN launch");
+  {
+    ProfScope prof(ctx, COLI_KERNEL_COMBINE);
+    e = launch_k(stream_reduce_kernel, (D + 31) / 32, 256, 0, ctx->stream, true, false,
+                 static_cast<const float*>(P.part), G, D, resid, x_dtype, y, y_dtype);
+  }
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "stream FFN reduce launch");
   return COLI_OK;
 }
 

@@ -1,10 +1,9 @@
-"""S = 1 decode through the one-launch streaming FFN (split of the down projection by 16-row units,
-fixed-order reduce of per-CTA partial rows) against the oracle, against the two-kernel form, and
-its bounded waits.
+"""S = 1 decode through the streaming FFN (the down projection split by 16-row units, a fixed-order
+reduce of per-CTA partial rows) against the oracle, against the two-kernel form, and its bounded waits.
 
-The streaming kernel runs when D is a multiple of 1024 (up to 8192), I a multiple of 16 and every
+The streaming kernel runs when D is a multiple of 1024 (up to 6144), I a multiple of 16 and every
 table entry has per-row or 32-multiple group scales; the profile then records one gate/up-kind
-launch and no down launch per call.
+launch (the streaming kernel), one combine-kind launch (its reduce) and no down launch per call.
 """
 import os
 
@@ -54,8 +53,8 @@ CASES = [
     LayerConfig("D1024-K16", D=1024, I=64, E=64, K=16),
     LayerConfig("D2048-bf16", D=2048, I=256, E=16, K=4, x_dtype="bf16"),
     LayerConfig("D1024-no-norm", D=1024, I=96, E=32, K=6, norm_topk=False, routed_scale=1.0),
-    # 16 consumer warps (the widest CTA), fewer units than CTAs
-    LayerConfig("D8192-I64", D=8192, I=64, E=8, K=2),
+    # fewer units than CTAs; D = 7168 (two stages of each ring no longer fit) takes the two-kernel form
+    LayerConfig("D5120-I64", D=5120, I=64, E=8, K=2),
     # more units than CTAs on one slot, CTAs spanning slots, g96 groups (D % gs != 0 for the gate rows)
     LayerConfig("D6144-I1024-g96", D=6144, I=1024, E=8, K=3, gs=96),
 ]
@@ -75,7 +74,7 @@ def test_stream_matches_oracle_and_two_kernel_form(ctxs, cfg):
         l2.step(l2.act_tensor(x), l2.act_tensor(resid), o2)
         assert B.coli_check_error(cs) == 0, B.coli_last_error(cs)
         assert B.coli_check_error(c2) == 0, B.coli_last_error(c2)
-        assert launches(cs) == (1, 0)  # the whole FFN in one launch
+        assert launches(cs) == (1, 0)  # the whole FFN in one streaming launch (plus its reduce)
         B.coli_profile_enable(cs, 0)
         for k in ("idx", "w", "n_sel"):
             assert torch.equal(os_[k], o2[k]), k
@@ -152,9 +151,10 @@ def test_stream_bad_route_then_healthy(ctxs):
 
 
 def test_stream_bounded_wait_gives_up_then_healthy():
-    """A CTA withholds its grid-barrier arrival (test hook, one launch): every other CTA's bounded wait
-    gives up after the shortened limit and the call reports COLI_E_TIMEOUT; the next call is healthy and
-    matches the oracle. No wait is unbounded and nothing traps."""
+    """One CTA's producer withholds the copy of its first stage (test hook, one launch): the waits on that
+    stage give up after the shortened limit, the waits behind them too, and the call reports
+    COLI_E_TIMEOUT; the next call is healthy and matches the oracle. No wait is unbounded and nothing
+    traps."""
     c = make_ctx(COLI_DECODE_STREAM=1, COLI_TEST_WAIT_NS=20_000_000, COLI_TEST_WITHHOLD=1)
     cfg = LayerConfig("timeout", D=1024, I=64, E=8, K=2)
     layer = DeviceLayer(c.ctx, cfg)
