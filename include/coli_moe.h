@@ -155,12 +155,13 @@ COLI_API int coli_router_select_shared(coli_ctx *ctx, const void *x, int x_dtype
  *   - Scratch: a fixed device array of the library, one per device (2.5 MiB), holding the
  *     (score, choice) pairs and, for S >= 16, the partial logits of at most 65536 (token, expert)
  *     cells; S * E above that returns COLI_E_INVAL.
- *   - The first call on a device looks up that array's address (a CUDA symbol query with the
- *     context's device current); make that first call before any stream capture.
+ *   - The first call on a device, and again the first call in a new CUDA context there (after a
+ *     device reset, say), looks up that array's address (a CUDA symbol query with the context's
+ *     device current); make that first call before any stream capture.
  *   - The array's arrival counter is cleared on the context's stream before each launch.
  *   - All contexts on a device share the array: calls whose kernels may run at the same time
  *     (different streams, contexts or unordered host threads) race on it and give wrong results.
- *   - Not covered by coli_profile_enable's per-kernel timing.
+ *   - Timed by coli_profile_enable as COLI_KERNEL_ROUTER, like coli_router_select.
  */
 COLI_API int coli_router_select_noalloc(coli_ctx *ctx, const void *x, int x_dtype, int S, int D,
                        const float *Wr, const float *bias, int E, int K, float topp,

@@ -496,8 +496,9 @@ int launch_router(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const
 // array instead of the context's workspace: the arrival counter in the first 256 bytes, then the
 // (score, choice) pairs of at most kFixedRouterCells (token, expert) cells, then the partial
 // logits of the many-token path. Its address is looked
-// up once per device (the first call on that device); the counter is cleared on the stream before
-// every launch. All contexts on a device share the array, so calls whose kernels could overlap
+// up once per device and CUDA context (the first call there), since a device reset or another
+// context loads the module at a new address; the counter is cleared on the stream before every
+// launch. All contexts on a device share the array, so calls whose kernels could overlap
 // (different streams, contexts or host threads without ordering) race on it.
 // ------------------------------------------------------------------------------------------
 
@@ -510,7 +511,27 @@ static __device__ __align__(256) unsigned char
     g_router_fixed[kFixedPartOff + (size_t)kRSplit * kFixedRouterCells * sizeof(float)];
 
 static std::mutex g_fixed_mu;
-static unsigned char* g_fixed_addr[kFixedMaxDevices];  // device address of g_router_fixed, once set up
+static unsigned char* g_fixed_addr[kFixedMaxDevices];  // device address of g_router_fixed, once set up ...
+static void* g_fixed_ctx[kFixedMaxDevices];            // ... in this CUDA context
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// The calling thread's current CUDA context (the primary context of the current device for runtime
+// users), through the runtime's driver entry point; NULL if unavailable.
+static void* current_context() {
+  static CtxGetCurrentFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    (void)cudaGetLastError();
+  }
+  CUcontext c = nullptr;
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
 
 int launch_router_noalloc(coli_ctx* ctx, const void* x, int x_dtype, int S, int D, const float* Wr,
                           const float* bias, int E, int K, float topp, int norm_topk, float routed_scale,
@@ -524,13 +545,15 @@ int launch_router_noalloc(coli_ctx* ctx, const void* x, int x_dtype, int S, int 
   unsigned char* base;
   {
     std::lock_guard<std::mutex> lock(g_fixed_mu);
+    void* cur = current_context();  // the caller has made ctx->device current
     base = g_fixed_addr[ctx->device];
-    if (!base) {  // the caller has made ctx->device current
+    if (!base || g_fixed_ctx[ctx->device] != cur) {
       void* p = nullptr;
       cudaError_t e = cudaGetSymbolAddress(&p, g_router_fixed);
       if (e != cudaSuccess || !p) return cuda_fail(ctx, e != cudaSuccess ? e : cudaErrorInvalidSymbol, "router_select_noalloc: scratch address");
       base = static_cast<unsigned char*>(p);
       g_fixed_addr[ctx->device] = base;
+      g_fixed_ctx[ctx->device] = cur;
     }
   }
   unsigned* arrivals = reinterpret_cast<unsigned*>(base);
@@ -556,6 +579,7 @@ int launch_router_noalloc(coli_ctx* ctx, const void* x, int x_dtype, int S, int 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const void* xp = x;
+  ProfScope prof(ctx, COLI_KERNEL_ROUTER);
   e = vec4 ? cudaLaunchKernelEx(&cfg, router_fixed_kernel<true>, xp, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk,
                                 routed_scale, shared, sc_ws, idx, w, n_sel, ctx->d_status, arrivals, epl, table)
            : cudaLaunchKernelEx(&cfg, router_fixed_kernel<false>, xp, x_dtype, S, D, Wr, bias, E, K, topp, norm_topk,

@@ -1,4 +1,5 @@
-"""coli_router_select_noalloc: the router entry with fixed device scratch, against coli_router_select.
+"""coli_router_select_noalloc: the router entry with fixed device scratch, against coli_router_select
+and against the oracle.
 
 Collected last (file name) so that it runs both alone and after every other GPU test; it creates
 its own contexts and depends on no state left by other tests.
@@ -9,7 +10,7 @@ import torch
 
 from int4_grouped_expert_router_gb300 import binding as B
 from int4_grouped_expert_router_gb300 import synth
-from gpu_util import Ctx
+from gpu_util import Ctx, check_router
 
 pytestmark = pytest.mark.gpu
 
@@ -54,13 +55,21 @@ def test_matches_router_select_on_two_calls_in_a_row(case):
             assert torch.equal(na, nb), call
             assert np.array_equal(wa.cpu().numpy().view(np.uint32), wb.cpu().numpy().view(np.uint32)), call
             assert (ia >= 0).any()
+            # and against the oracle directly (exact indices except near-ties, weights rel 1e-4 / abs 1e-5)
+            xh = x.float().cpu().numpy().astype(np.float64)
+            near, _ = check_router(ia.cpu().numpy(), wa.cpu().numpy(), na.cpu().numpy(), xh, Wr.cpu().numpy(),
+                                   bias.cpu().numpy(), K, topp, norm, rs)
+            assert near <= max(1, S // 64), near
     finally:
         c.close()
 
 
-def test_device_memory_unchanged_by_calls():
-    """After the first call (which looks up the scratch address), calls leave free memory as it was."""
-    S, D, E, K = 16, 2048, 256, 8
+@pytest.mark.parametrize("S", [1, 16], ids=["decode-path", "many-token-path"])
+def test_device_memory_unchanged_by_calls(S):
+    """After a warm-up call (which looks up the scratch address), calls leave free memory as it was:
+    S = 1 takes the decode router (counter cleared on the stream, one kernel), S = 16 the many-token
+    router (three kernels)."""
+    D, E, K = 2048, 256, 8
     c = Ctx()
     try:
         x, Wr, bias = _inputs(3, S, D, E)
