@@ -39,6 +39,7 @@ def parse():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill, shared-expert, dense-projection and compressed-tier figures")
     ap.add_argument("--cpu-steps", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--check", default="", help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -271,6 +272,121 @@ def prefill_leg(ctx, stream, flush, steps=10, warmup=3):
     }
 
 
+def decode_variant_leg(ctx, stream, flush, name, steps=20, warmup=3):
+    """A decode-layer workload other than the headline one (the grouped-scale layer, or the S=4 bf16 Zipf
+    layer): graph-replayed steps with a cold L2, per-kernel event means from a second pass, the distinct
+    experts each step touched and the HBM fraction over their bytes."""
+    import numpy as np
+    import torch
+
+    from int4_grouped_expert_router_gb300 import binding as B
+    from int4_grouped_expert_router_gb300.workload import CONFIGS, DeviceLayer, router_host_inputs
+
+    cfg = CONFIGS[name]
+    layer = DeviceLayer(ctx, cfg)
+    B.coli_reserve(ctx, cfg.S, cfg.E, cfg.K, cfg.D, cfg.I)
+    n = warmup + steps
+    xs, rs, outs = [], [], []
+    for s in range(n):
+        x, _, _, resid = router_host_inputs(cfg, 700000 + s)
+        xs.append(layer.act_tensor(x))
+        rs.append(layer.act_tensor(resid))
+        outs.append(layer.outputs())
+    xin, rin, gout = torch.empty_like(xs[0]), torch.empty_like(rs[0]), layer.outputs()
+    with torch.cuda.stream(stream):
+        xin.copy_(xs[0])
+        rin.copy_(rs[0])
+        layer.step(xin, rin, gout)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        layer.step(xin, rin, gout)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for s in range(n):
+            xin.copy_(xs[s])
+            rin.copy_(rs[s])
+            flush.zero_()
+            ev[s][0].record(stream)
+            g.replay()
+            ev[s][1].record(stream)
+            for k in ("idx", "w", "n_sel", "y"):
+                outs[s][k].copy_(gout[k])
+    torch.cuda.synchronize()
+    assert B.coli_check_error(ctx) == 0, B.coli_last_error(ctx)
+    del g
+    us = [ev[s][0].elapsed_time(ev[s][1]) * 1000.0 for s in range(warmup, n)]
+    B.coli_profile_enable(ctx, True)
+    for k in (B.COLI_KERNEL_ROUTER, B.COLI_KERNEL_GATEUP, B.COLI_KERNEL_DOWN, B.COLI_KERNEL_COMBINE):
+        B.coli_profile_read(ctx, k)
+    with torch.cuda.stream(stream):
+        for s in range(warmup, n):
+            flush.zero_()
+            layer.step(xs[s], rs[s], outs[s])
+    kern = {}
+    for kname, k in (("router", B.COLI_KERNEL_ROUTER), ("gateup_or_stream", B.COLI_KERNEL_GATEUP),
+                     ("down", B.COLI_KERNEL_DOWN), ("combine_or_reduce", B.COLI_KERNEL_COMBINE)):
+        t, c = B.coli_profile_read(ctx, k)
+        if c:
+            kern[kname] = t * 1000.0 / c
+    B.coli_profile_enable(ctx, False)
+    distinct, nbytes = [], []
+    for s in range(warmup, n):
+        idx = outs[s]["idx"].cpu().numpy()
+        ids = np.unique(idx[idx >= 0])
+        distinct.append(int(ids.size))
+        nbytes.append(sum(cfg.expert_bytes(int(e)) for e in ids))
+    layer.free()
+    hpeak, hkind = peaks()
+    mean_us = statistics.mean(us)
+    gbs = statistics.mean(nbytes) / (mean_us * 1e-6) / 1e9
+    return {"workload": workload_desc(cfg) + (", Zipf-skewed routing" if cfg.zipf else ""),
+            "us_per_layer": mean_us, "p50_us": statistics.median(us), "steps": steps,
+            "launch": "one CUDA graph (router + grouped call) per step", "l2": "flushed between steps",
+            "kernels_us": kern, "distinct_experts": statistics.mean(distinct), "expert_bytes": statistics.mean(nbytes),
+            "hbm_gbs": gbs, "hbm_frac": gbs / hpeak, "peak_kind": f"{hkind} hbm_gbs"}
+
+
+def accuracy_sample(cfg, Wr, bias, xs_host, outs, rs_host, n_ffn=2):
+    """Against the oracle, for the timed tokens: router near-ties (index disagreements allowed only where the
+    oracle's choice scores are within 1e-6) over every timed token, and the largest |y - oracle| over the first
+    n_ffn tokens (the oracle FFN evaluated with the GPU's routes), with the tolerance's absolute term."""
+    import numpy as np
+
+    import oracle.moe as O
+    from int4_grouped_expert_router_gb300.workload import host_expert
+
+    near, mismatch = 0, 0
+    x_all = np.concatenate(xs_host, axis=0)
+    idx_o, w_o, n_o, (_, _, c) = O.router_select(x_all, Wr, bias, cfg.K, cfg.topp, cfg.norm_topk, cfg.routed_scale)
+    for t, out in enumerate(outs):
+        ig = np.asarray(out["idx"])[0]
+        if np.array_equal(ig, idx_o[t]):
+            continue
+        # a disagreement is a near-tie when every differing pair of experts has choice scores within 1e-6
+        pairs = [(int(a), int(b)) for a, b in zip(ig, idx_o[t]) if a != b and a >= 0 and b >= 0]
+        if pairs and all(abs(float(c[t, a]) - float(c[t, b])) < 1e-6 for a, b in pairs):
+            near += 1
+        else:
+            mismatch += 1
+    max_err, atol = 0.0, None
+    for t in range(min(n_ffn, len(outs))):
+        ig, wg, ng, yg = (np.asarray(outs[t][k], dtype=np.float64) for k in ("idx", "w", "n_sel", "y"))
+        ig = ig.astype(np.int32)
+        wg = wg.astype(np.float32)
+        ex = {}
+        for e in sorted(set(int(v) for v in ig.reshape(-1) if v >= 0)):
+            ex[e] = tuple(O.Tensor(p, s, r, cc, gs) for (p, s, r, cc, gs) in host_expert(cfg, e))
+        ref = O.expert_group(xs_host[t], ex, ig, wg, ng.astype(np.int32), rs_host[t])
+        max_err = max(max_err, float(np.abs(yg - ref).max()))
+        rms = float(np.sqrt(np.mean(ref * ref)))
+        atol = 1e-5 * max(1.0, rms)
+    return {"tokens_routed": len(outs), "router_near_ties": near, "router_mismatches": mismatch,
+            "ffn_tokens": min(n_ffn, len(outs)),
+            "max_abs_err": max_err, "abs_term": atol,
+            "tolerance": "rel 1e-4 + abs 1e-5 x max(1, rms(y)) per element"}
+
+
 def token_seed(rank: int, step: int) -> int:
     """Seed of the token a rank processes at a step: every rank (replica) gets its own tokens."""
     return rank * 100000 + step
@@ -301,7 +417,7 @@ def workload_desc(cfg):
 # CPU oracle leg (reference arm and cpu_baseline): runs in a child process pinned to one thread.
 # ------------------------------------------------------------------------------------------------
 
-def cpu_step_worker(workload: str, steps: int, warmup: int):
+def cpu_step_worker(workload: str, steps: int, warmup: int, check: str = ""):
     """The oracle in steps of a bounded sample: step s routes token s (the whole router) and runs ONE of
     its kept experts (slot s mod n_sel). The per-layer figure is the mean router time plus the mean
     kept count times the mean expert time."""
@@ -326,19 +442,29 @@ def cpu_step_worker(workload: str, steps: int, warmup: int):
             kept.append(int(n[0]))
             t_step.append((t1 - t0) + (t3 - t2))
     mr, me, mk = statistics.mean(t_router), statistics.mean(t_expert), statistics.mean(kept)
-    print(json.dumps({"us_per_layer": (mr + mk * me) * 1e6, "steps": steps, "warmup": warmup,
-                      "ms_per_step": statistics.mean(t_step) * 1e3, "router_ms": mr * 1e3, "expert_ms": me * 1e3,
-                      "kept": mk}))
+    res = {"us_per_layer": (mr + mk * me) * 1e6, "steps": steps, "warmup": warmup,
+           "ms_per_step": statistics.mean(t_step) * 1e3, "router_ms": mr * 1e3, "expert_ms": me * 1e3, "kept": mk}
+    if check:  # the GPU arm's timed tokens, checked against the same oracle
+        import numpy as np
+        z = np.load(check)
+        outs = [{"idx": z["idx"][t], "w": z["w"][t], "n_sel": z["n_sel"][t], "y": z["y"][t] if t < len(z["y"]) else None}
+                for t in range(z["idx"].shape[0])]
+        res["accuracy"] = accuracy_sample(cfg, z["Wr"], z["bias"], list(z["x"]), outs, list(z["resid"]),
+                                          n_ffn=len(z["y"]))
+    print(json.dumps(res))
 
 
-def run_oracle_steps(workload: str, steps: int, warmup: int):
+def run_oracle_steps(workload: str, steps: int, warmup: int, check: str = ""):
     """cpu_step_worker in a fresh single-threaded process (no GPU visible); returns its JSON."""
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-steps", str(steps), "--warmup", str(warmup),
-                        "--workload", workload], capture_output=True, text=True, env=env, timeout=3600)
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-steps", str(steps), "--warmup", str(warmup),
+           "--workload", workload]
+    if check:
+        cmd += ["--check", check]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=3600)
     if r.returncode != 0:
         raise RuntimeError(f"oracle timing failed: {r.stderr[-2000:]}")
     return json.loads(r.stdout.strip().splitlines()[-1])
@@ -440,7 +566,7 @@ def load_traffic(kernel: str, src_hash: str):
 def source_hash():
     import hashlib
     h = hashlib.sha256()
-    for name in ("experts.cu", "coli_internal.h", "pipe.h"):
+    for name in ("experts.cu", "decode.cu", "dot.h", "coli_internal.h", "pipe.h"):
         with open(os.path.join(ROOT, "int4_grouped_expert_router_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -469,11 +595,13 @@ def gpu_arm(args, rank, world, local):
     B.coli_reserve(ctx, cfg.S, cfg.E, cfg.K, cfg.D, cfg.I)
 
     # per-step inputs, resident on the device before timing (each rank its own tokens)
-    xs, rs = [], []
+    xs, rs, xs_host, rs_host = [], [], [], []
     for s in range(n_tok):
-        x, _, _, resid = router_host_inputs(cfg, token_seed(rank, s))
+        x, Wr_h, bias_h, resid = router_host_inputs(cfg, token_seed(rank, s))
         xs.append(layer.act_tensor(x))
         rs.append(layer.act_tensor(resid))
+        xs_host.append(x)
+        rs_host.append(resid)
     outs = [layer.outputs() for _ in range(n_tok)]
     flush_buf = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
     flush_sink = torch.empty(1, dtype=torch.float32, device="cuda")
@@ -596,10 +724,11 @@ def gpu_arm(args, rank, world, local):
         if n:
             kern[name] = {"launches": n, "mean_us": ms * 1000.0 / n}
     B.coli_profile_enable(ctx, False)
-    # S == 1 runs the whole expert FFN as one kernel (recorded as gate/up, no down launch): its
-    # algorithmic bytes are every kept expert's gate, up and down bytes; else the gate/up kernel's
+    # S == 1 streams the whole expert FFN in one kernel (recorded as gate/up, no down launch; its reduce
+    # is recorded as combine): its algorithmic bytes are every kept expert's gate, up and down bytes;
+    # else the gate/up kernel's
     fused = "down" not in kern
-    top_kernel = "decode_ffn_kernel" if fused else "gateup_kernel"
+    top_kernel = "stream_ffn_kernel" if fused else "gateup_kernel"
     top_bytes = float(np.mean(expert_bytes if fused else gateup_bytes))
     achieved = top_bytes / (kern["gateup"]["mean_us"] * 1e-6) / 1e9
     traffic = load_traffic(top_kernel, source_hash())
@@ -634,12 +763,25 @@ def gpu_arm(args, rank, world, local):
     h2d = xs[0].numel() * xs[0].element_size() + rs[0].numel() * rs[0].element_size()
     d2h = outs[0]["y"].numel() * outs[0]["y"].element_size()
 
-    launches_per_step = 2 if fused else (3 if cfg.S == 1 else 4)
+    # router + streaming FFN + its reduce, or router + gate/up + down (+ combine for S > 1)
+    launches_per_step = 3 if fused else (3 if cfg.S == 1 else 4)
     result = None
     if rank == 0:
         cpu = None
+        accuracy = None
         try:
-            res = run_oracle_steps(args.workload, 40, 1)  # about 10 s of single-threaded oracle
+            import tempfile
+            timed = list(range(args.warmup, n_tok))
+            n_ffn = min(2, len(timed))
+            check = os.path.join(tempfile.mkdtemp(prefix="coli_bench_"), "timed.npz")
+            np.savez(check, x=np.stack([xs_host[s] for s in timed]), resid=np.stack([rs_host[s] for s in timed]),
+                     Wr=Wr_h, bias=bias_h, idx=np.stack([outs[s]["idx"].cpu().numpy() for s in timed]),
+                     w=np.stack([outs[s]["w"].cpu().numpy() for s in timed]),
+                     n_sel=np.stack([outs[s]["n_sel"].cpu().numpy() for s in timed]),
+                     y=np.stack([outs[s]["y"].float().cpu().numpy() for s in timed[:n_ffn]]))
+            # about 10 s of single-threaded oracle, and the check of the timed tokens against it
+            res = run_oracle_steps(args.workload, 40, 1, check)
+            accuracy = res.get("accuracy")
             cpu = {"value": res["us_per_layer"], "unit": UNIT, "cores": 1, "kind": "oracle",
                    "sample": oracle_sample(res, args.workload)}
         except Exception as exc:  # the CPU leg must not hide the GPU number
@@ -664,6 +806,7 @@ def gpu_arm(args, rank, world, local):
                          "frac": achieved / hbm_peak, "traffic": traffic, "kernel": top_kernel,
                          "peak_kind": f"{peak_kind} hbm_gbs", "algorithmic_bytes_per_launch": top_bytes},
             "cpu_baseline": cpu,
+            "accuracy": accuracy,
             "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clock_info,
@@ -678,6 +821,14 @@ def gpu_arm(args, rank, world, local):
             except Exception as exc:  # these figures must not hide the decode number
                 extra[name] = {"error": f"{exc}"[:300]}
     layer.free()
+    # the other decode layers take the expert table over, so they run after the headline layer is freed
+    if rank == 0 and not args.no_prefill:
+        for name, leg in (("decode_grouped_scales", lambda: decode_variant_leg(ctx, stream, flush, "decode_g64")),
+                          ("decode_s4_bf16_zipf", lambda: decode_variant_leg(ctx, stream, flush, "decode_s4_bf16"))):
+            try:
+                extra[name] = leg()
+            except Exception as exc:  # these figures must not hide the decode number
+                extra[name] = {"error": f"{exc}"[:300]}
     prefill = None
     if rank == 0 and not args.no_prefill:
         try:
@@ -698,7 +849,7 @@ def gpu_arm(args, rank, world, local):
 def main():
     args = parse()
     if args.cpu_steps:
-        cpu_step_worker(args.workload, args.cpu_steps, args.warmup)
+        cpu_step_worker(args.workload, args.cpu_steps, args.warmup, args.check)
         return 0
     rank, world, local = dist_env()
     if args.impl == "reference":

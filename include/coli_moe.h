@@ -125,6 +125,11 @@ COLI_API int coli_profile_read(coli_ctx *ctx, int kind, double *total_ms, long l
  * Outputs (device, caller-owned): idx [S x K] int32, w [S x K] f32, n_sel [S] int32 (kept slots
  * per token) or NULL. Limits: 1 <= K <= min(E, COLI_MAX_K), E <= COLI_MAX_EXPERTS.
  * A non-finite score sets COLI_E_NONFINITE in the device error word.
+ * S < 16 with E <= 1024 runs as one kernel whose CTAs publish partial logits to the context's
+ * router scratch and whose first CTA selects once every partial of a token has arrived; that
+ * wait is bounded (2 s), after which the call sets COLI_E_TIMEOUT and writes an empty route
+ * (n_sel 0, idx -1, w 0) for the token. The logits' summation order depends on the CTA grid
+ * (COLI_ROUTER_ROWS / COLI_ROUTER_PARTS at coli_init), so near-tied experts may swap across grids.
  */
 COLI_API int coli_router_select(coli_ctx *ctx, const void *x, int x_dtype, int S, int D,
                        const float *Wr, const float *bias, int E, int K, float topp,
@@ -152,13 +157,15 @@ COLI_API int coli_router_select_shared(coli_ctx *ctx, const void *x, int x_dtype
  * allocate: a server that has given all free device memory to its own caching pool, or a decode
  * loop that cannot take the stall of cudaMalloc (which may synchronise the device) or of a
  * workspace that grows (which first waits for the context's stream).
- *   - Scratch: a fixed device array of the library, one per device (2.5 MiB), holding the
- *     (score, choice) pairs and, for S >= 16, the partial logits of at most 65536 (token, expert)
- *     cells; S * E above that returns COLI_E_INVAL.
+ *   - Scratch: a fixed device array of the library, one per device (2.6 MiB), holding the
+ *     one-kernel router's launch counter and partial logits (S < 16) and, for S >= 16, the
+ *     (score, choice) pairs and partial logits of at most 65536 (token, expert) cells; S * E
+ *     above that returns COLI_E_INVAL.
  *   - The first call on a device, and again the first call in a new CUDA context there (after a
  *     device reset, say), looks up that array's address (a CUDA symbol query with the context's
  *     device current); make that first call before any stream capture.
- *   - The array's arrival counter is cleared on the context's stream before each launch.
+ *   - The array's launch counter only grows, so nothing is cleared between calls and each call
+ *     is one kernel launch for S < 16 (three for S >= 16).
  *   - All contexts on a device share the array: calls whose kernels may run at the same time
  *     (different streams, contexts or unordered host threads) race on it and give wrong results.
  *   - Timed by coli_profile_enable as COLI_KERNEL_ROUTER, like coli_router_select.

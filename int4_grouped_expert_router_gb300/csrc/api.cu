@@ -229,6 +229,14 @@ int coli_init(coli_ctx** out, int device, void* cuda_stream) {
   if (tw && *tw) ctx->wait_ns = strtoull(tw, nullptr, 10);
   const char* th = getenv("COLI_TEST_WITHHOLD");
   if (th && *th) ctx->test_withhold = atoi(th) != 0;
+  const char* thr = getenv("COLI_TEST_WITHHOLD_ROUTER");
+  if (thr && *thr) ctx->test_withhold_router = atoi(thr);
+  const char* rr = getenv("COLI_ROUTER_ROWS");
+  if (rr && *rr) ctx->router_rows = atoi(rr);
+  if (ctx->router_rows != 1 && ctx->router_rows != 2 && ctx->router_rows != 4 && ctx->router_rows != 8)
+    ctx->router_rows = 0;
+  const char* rp = getenv("COLI_ROUTER_PARTS");
+  if (rp && *rp) ctx->router_parts = std::max(0, std::min(4, atoi(rp)));
   ctx->h_table.assign(COLI_MAX_EXPERTS, ExpertDesc{});
   ctx->table_handles.assign(3 * COLI_MAX_EXPERTS, 0);
   ctx->table_stream.assign(COLI_MAX_EXPERTS, 1);
@@ -239,6 +247,8 @@ int coli_init(coli_ctx** out, int device, void* cuda_stream) {
   if ((e = cudaMalloc(&p, kStatusBytes)) != cudaSuccess) goto fail;
   ctx->d_status = static_cast<int*>(p);
   if ((e = cudaMemset(ctx->d_status, 0, kStatusBytes)) != cudaSuccess) goto fail;
+  if ((e = cudaMalloc(&ctx->d_router, kRouterScratchBytes)) != cudaSuccess) goto fail;
+  if ((e = cudaMemset(ctx->d_router, 0, kRouterScratchBytes)) != cudaSuccess) goto fail;
   {
     const int32_t route[2] = {0, 0x3f800000};  // expert 0, then the bits of 1.0f
     if ((e = cudaMalloc(&p, sizeof(route))) != cudaSuccess) goto fail;
@@ -269,6 +279,7 @@ void coli_destroy(coli_ctx* ctx) {
   ans_release_all(ctx);
   if (ctx->d_table) cudaFree(ctx->d_table);
   if (ctx->d_status) cudaFree(ctx->d_status);
+  if (ctx->d_router) cudaFree(ctx->d_router);
   if (ctx->ws.base) cudaFree(ctx->ws.base);
   if (ctx->slots) cudaFree(ctx->slots);
   for (auto& r : ctx->prof_pending) {

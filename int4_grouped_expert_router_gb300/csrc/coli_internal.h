@@ -28,11 +28,13 @@ constexpr int kTcRows = 128;
 constexpr int kTcWords = 32;
 // One-launch decode FFN: a work unit is kPanelCols rows of gate/up and the same columns of down.
 constexpr int kPanelCols = 16;
+// One-launch router scratch (router.cu): a launch counter (256 bytes), then 64-bit tagged partial
+// logits of at most 15 tokens x 1024 (column part, expert) pairs.
+constexpr size_t kRouterScratchBytes = 256 + (size_t)15 * 1024 * 8;
 
-// Device status words of a context: [0] error code, [1] router arrivals, [2..] the opt-in fused
-// decode kernel's synchronisation words (grid barrier at [2], [3]; row-range counters from
-// [2 + kSyncRanges]). All start at zero; the router's counter is returned to zero by its last CTA,
-// and the grid barrier's count only grows.
+// Device status words of a context: [0] error code, [1] unused, [2..] the opt-in fused decode
+// kernel's synchronisation words (grid barrier at [2], [3]; row-range counters from
+// [2 + kSyncRanges]). All start at zero, and the grid barrier's count only grows.
 constexpr int kSyncBase = 2;
 constexpr int kSyncRanges = 64;   // offset of the range counters from kSyncBase
 constexpr int kMaxRanges = 4096;  // range counters
@@ -126,6 +128,13 @@ struct coli_ctx {
   // of its first stage so that the waits on it give up (COLI_TEST_WITHHOLD=N)
   unsigned long long wait_ns = 0;
   int test_withhold = 0;
+  // the one-launch router: its scratch (kRouterScratchBytes, zeroed at creation), the rows and
+  // column parts of its CTAs when set (COLI_ROUTER_ROWS, COLI_ROUTER_PARTS; 0: chosen per call),
+  // and a test hook: for the next N launches its last CTA withholds token 0's partial logits, so
+  // that the selection's bounded wait gives up (COLI_TEST_WITHHOLD_ROUTER=N)
+  void* d_router = nullptr;
+  int router_rows = 0, router_parts = 0;
+  int test_withhold_router = 0;
   coli::Workspace ws;
   // resident issue/take: f32 partial sums [COLI_MAX_ISSUES][S x D] of the current round's issues
   float* slots = nullptr;
@@ -154,7 +163,7 @@ bool injected(coli_ctx* ctx);  // COLI_FAIL_AFTER: true if this compute call mus
 int ensure_workspace(coli_ctx* ctx, size_t bytes);
 int ensure_slots(coli_ctx* ctx, size_t bytes);
 
-inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Brackets one kernel launch with profiling events when profiling is on.
 struct ProfScope {

@@ -95,6 +95,21 @@ class Ctx:
     def __init__(self, device=0):
         self.ctx = B.coli_init(device)
 
+    @staticmethod
+    def with_env(**env) -> "Ctx":
+        """A context created while the given COLI_* variables are set (coli_init reads them)."""
+        import os
+        old = {k: os.environ.get(k) for k in env}
+        os.environ.update({k: str(v) for k, v in env.items()})
+        try:
+            return Ctx()
+        finally:
+            for k, v in old.items():
+                if v is None:
+                    del os.environ[k]
+                else:
+                    os.environ[k] = v
+
     def close(self):
         if self.ctx is not None:
             B.coli_destroy(self.ctx)

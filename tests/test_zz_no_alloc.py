@@ -67,7 +67,7 @@ def test_matches_router_select_on_two_calls_in_a_row(case):
 @pytest.mark.parametrize("S", [1, 16], ids=["decode-path", "many-token-path"])
 def test_device_memory_unchanged_by_calls(S):
     """After a warm-up call (which looks up the scratch address), calls leave free memory as it was:
-    S = 1 takes the decode router (counter cleared on the stream, one kernel), S = 16 the many-token
+    S = 1 takes the one-kernel router (its launch counter only grows), S = 16 the many-token
     router (three kernels)."""
     D, E, K = 2048, 256, 8
     c = Ctx()
