@@ -66,6 +66,7 @@ struct StreamCtrl {
   float red[kHB][kStMaxWarps][16];   // per gate/up warp: its 8 gate and 8 up row sums of a unit
   float fs[kHB][2][16];              // per-row gate and up scales of a unit's 16 rows (1 for chunk scales)
   Limbs16 hl[kHB];                   // h of a unit as one 16-column block of limbs
+  uint64_t xfull, xfree;             // x copied into gate/up stage 0 / every gate/up warp has read it
   int m;
 };
 
@@ -83,6 +84,7 @@ struct StreamParams {
   uint32_t sbg, sbd;         // their stage bytes
   unsigned long long wait_ns;
   int withhold;              // test hook: the CTA owning unit 0 withholds the copy of its first gate stage
+  int x_bulk;                // x is 16-byte aligned: each CTA copies it whole into shared memory
 };
 
 // Limbs of 16 values of h held by lanes 0..15 (lanes 16..31 hold 0); every lane returns the same
@@ -168,58 +170,114 @@ __global__ void __launch_bounds__(MAXT, 1) stream_ffn_kernel(const StreamParams 
       mbar_init(&cs.hlf[b], 1);
       mbar_init(&cs.hlfree[b], NW);
     }
+    mbar_init(&cs.xfull, 1);
+    mbar_init(&cs.xfree, NW);
     mbar_fence_init();
+    // x (the router's input, complete before this grid started) into gate/up stage 0 with one bulk
+    // copy: every CTA needs all of it, and 152 CTAs of per-thread loads of the same 24 KiB queue for
+    // microseconds behind each other in L2, where one bulk request per CTA does not
+    if (P.x_bulk) {
+      const uint32_t xbytes = (uint32_t)D * (P.x_dtype == COLI_DTYPE_F32 ? 4u : 2u);
+      mbar_arrive_expect_tx(&cs.xfull, xbytes);
+      bulk_g2s(ring_g, P.x, xbytes, &cs.xfull);
+    }
   }
+  __syncthreads();  // the barriers are initialised before any thread waits on or arrives at one
   // gate/up prologue, overlapping the router's tail: the limbs of this thread's chunk of x
   const int c = tid % C, r0 = tid / C;  // gate/up threads: r0 in {0, 1}
   Limbs X;
   if (warp < NW) {
     float xv[32];
-    load_chunk_f32(P.x, P.x_dtype, 0, 32 * c, D, xv);
+    if (P.x_bulk) {
+      __syncwarp();
+      bool late = false;
+      role_wait(&cs.xfull, 0, lim, late, P.err);
+      if (P.x_dtype == COLI_DTYPE_F32) {  // chunk c: 32 floats at byte 128 c
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+          const uint4 u = lds128(ring_g + 128 * c + 16 * i);
+          xv[4 * i] = __uint_as_float(u.x);
+          xv[4 * i + 1] = __uint_as_float(u.y);
+          xv[4 * i + 2] = __uint_as_float(u.z);
+          xv[4 * i + 3] = __uint_as_float(u.w);
+        }
+      } else {  // 32 bf16 at byte 64 c
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+          const uint4 u = lds128(ring_g + 64 * c + 16 * i);
+          const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int h = 0; h < 4; h++) {
+            xv[8 * i + 2 * h] = __uint_as_float(w4[h] << 16);
+            xv[8 * i + 2 * h + 1] = __uint_as_float(w4[h] & 0xffff0000u);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&cs.xfree);  // stage 0 may be refilled
+    } else {
+      load_chunk_f32(P.x, P.x_dtype, 0, 32 * c, D, xv);
+    }
     if (!make_limbs(xv, X)) set_error(P.err, COLI_E_NONFINITE);
   }
   griddep_wait();  // idx, w and n_sel come from the router
-  if (tid == 0) {
-    int m = P.n_sel ? ld_cg_i32(P.n_sel) : P.K;
-    cs.m = m < 0 ? 0 : (m > P.K ? P.K : m);
-  }
-  __syncthreads();
-  const int m = cs.m;
-  if (tid < m) {
-    StreamSlot& sl = cs.slot[tid];
+  // Slots from the routes in two rounds of loads: the kept count, the expert ids and the weights
+  // together, then every table field a slot needs, read whether or not the entry turns out valid
+  // (the id is clamped into the table), so that no load waits for another's answer.
+  if (tid < P.K) {
+    const int m_raw = P.n_sel ? ld_cg_i32(P.n_sel) : P.K;
     const int e = ld_cg_i32(P.idx + tid);
-    bool ok = e >= 0 && e < COLI_MAX_EXPERTS && P.table[e].valid;
-    if (!ok) set_error(P.err, COLI_E_ROUTE);
-    if (ok) {
-      const TensorDesc& g = P.table[e].t[T_GATE];
-      const TensorDesc& u = P.table[e].t[T_UP];
-      const TensorDesc& d = P.table[e].t[T_DOWN];
-      sl.gw = g.w;
-      sl.uw = u.w;
-      sl.dp = d.panel;
-      sl.gs = g.s;
-      sl.us = u.s;
-      sl.gmode = g.mode;
-      sl.umode = u.mode;
-      sl.dmode = d.mode;
-      sl.ds = d.mode == SCALE_ROW ? d.s : d.sT;
-      sl.Gg = g.G;
-      sl.Gu = u.G;
-      sl.gsg = g.gs;
-      sl.gsu = u.gs;
-      sl.gsd = d.gs;
-      sl.wk = ld_cg_f32(P.w + tid);
+    const float wk = ld_cg_f32(P.w + tid);
+    const int m = m_raw < 0 ? 0 : (m_raw > P.K ? P.K : m_raw);
+    if (tid == 0) cs.m = m;
+    if (tid < m) {
+      const bool in_table = e >= 0 && e < COLI_MAX_EXPERTS;
+      const ExpertDesc* ed = P.table + (in_table ? e : 0);
+      const TensorDesc* g = &ed->t[T_GATE];
+      const TensorDesc* u = &ed->t[T_UP];
+      const TensorDesc* d = &ed->t[T_DOWN];
+      // every field into registers first (read-only loads, none ordered after a shared-memory store)
+      const int valid = __ldg(&ed->valid);
+      const uint8_t* gw = reinterpret_cast<const uint8_t*>(__ldg(reinterpret_cast<const unsigned long long*>(&g->w)));
+      const uint8_t* uw = reinterpret_cast<const uint8_t*>(__ldg(reinterpret_cast<const unsigned long long*>(&u->w)));
+      const uint8_t* dp = reinterpret_cast<const uint8_t*>(__ldg(reinterpret_cast<const unsigned long long*>(&d->panel)));
+      const float* gsc = reinterpret_cast<const float*>(__ldg(reinterpret_cast<const unsigned long long*>(&g->s)));
+      const float* usc = reinterpret_cast<const float*>(__ldg(reinterpret_cast<const unsigned long long*>(&u->s)));
+      const float* dsr = reinterpret_cast<const float*>(__ldg(reinterpret_cast<const unsigned long long*>(&d->s)));
+      const float* dst = reinterpret_cast<const float*>(__ldg(reinterpret_cast<const unsigned long long*>(&d->sT)));
+      const int gmode = __ldg(&g->mode), umode = __ldg(&u->mode), dmode = __ldg(&d->mode);
+      const int Gg = __ldg(&g->G), Gu = __ldg(&u->G);
+      const int gsg = __ldg(&g->gs), gsu = __ldg(&u->gs), gsd = __ldg(&d->gs);
+      StreamSlot& sl = cs.slot[tid];
+      sl.gw = gw;
+      sl.uw = uw;
+      sl.dp = dp;
+      sl.gs = gsc;
+      sl.us = usc;
+      sl.gmode = gmode;
+      sl.umode = umode;
+      sl.dmode = dmode;
+      sl.ds = dmode == SCALE_ROW ? dsr : dst;
+      sl.Gg = Gg;
+      sl.Gu = Gu;
+      sl.gsg = gsg;
+      sl.gsu = gsu;
+      sl.gsd = gsd;
+      sl.wk = wk;
+      bool ok = in_table && valid;
+      if (!ok) set_error(P.err, COLI_E_ROUTE);
       // the host launches this kernel only for tables it can stream; anything else is a bad entry
-      if (sl.gmode == SCALE_GENERIC || sl.umode == SCALE_GENERIC || sl.dmode == SCALE_GENERIC || !sl.dp ||
-          !sl.ds || rows_bytes + 64u * sl.Gg > P.sbg || rows_bytes + 64u * sl.Gu > P.sbg) {
+      if (ok && (gmode == SCALE_GENERIC || umode == SCALE_GENERIC || dmode == SCALE_GENERIC || !dp ||
+                 !(dmode == SCALE_ROW ? dsr : dst) || rows_bytes + 64u * Gg > P.sbg || rows_bytes + 64u * Gu > P.sbg)) {
         ok = false;
         set_error(P.err, COLI_E_ROUTE);
       }
+      sl.ok = ok;
     }
-    sl.ok = ok;
   }
   __syncthreads();
   griddep_launch_dependents();  // the reduce kernel may launch; it waits for this grid to finish
+  const int m = cs.m;
 
   const int UB = P.I / kPanelCols;  // units per slot
   const long long total = (long long)m * UB;
@@ -239,6 +297,7 @@ __global__ void __launch_bounds__(MAXT, 1) stream_ffn_kernel(const StreamParams 
       const uint32_t SB = gu ? P.sbg : P.sbd;
       uint32_t q = 0, s = 0, ph = 0;  // stage sequence number, its slot and the slot's use parity
       bool withhold = gu && P.withhold && ubeg == 0 && uend > 0;  // the CTA that owns unit 0
+      if (gu && P.x_bulk) role_wait(&cs.xfree, 0, lim, stop, P.err);  // x has left stage 0
       // one stage of up to two pieces (weights, then their scales) on one barrier
       auto issue = [&](const void* src, uint32_t bytes, const void* src2, uint32_t bytes2, bool weights) {
         if (stop) return;
@@ -558,6 +617,7 @@ int launch_stream_ffn(coli_ctx* ctx, const void* x, int x_dtype, const int32_t* 
   P.sbd = sbd;
   P.wait_ns = ctx->wait_ns;
   P.withhold = ctx->test_withhold > 0;  // one-shot: only the next launch withholds
+  P.x_bulk = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
   if (ctx->test_withhold > 0) ctx->test_withhold--;
   {
     ProfScope prof(ctx, COLI_KERNEL_GATEUP);

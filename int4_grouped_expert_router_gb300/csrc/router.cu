@@ -390,11 +390,16 @@ __device__ __forceinline__ void finish_rolled(int mine, float wmine, int K, floa
 // winner's key is zeroed (every finite choice maps to a nonzero key). A token with a word that
 // never arrived gets COLI_E_TIMEOUT and an empty route.
 __device__ __forceinline__ void select_tokens(const RouterArgs& a, unsigned tag) {
-  __shared__ uint32_t skey[kSelBatch][kDecodeMaxE];
-  __shared__ float ssc[kSelBatch][kDecodeMaxE];
+  // keys [nbmax][E] then raw scores [nbmax][E] in dynamic shared memory, nbmax = min(S, kSelBatch):
+  // every CTA of the grid gets the allocation, so it is kept to what CTA 0 needs (2 KiB for one token
+  // of 256 experts) and does not stop the expert kernel's CTAs from sharing the SMs
+  extern __shared__ uint32_t router_dyn[];
   __shared__ int s_late[kSelBatch];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = a.E, P = a.parts;
+  const int nbmax = min(a.S, kSelBatch);
+  uint32_t* skey = router_dyn;
+  float* ssc = reinterpret_cast<float*>(router_dyn + (size_t)nbmax * E);
   const uint64_t limit = a.wait_ns ? a.wait_ns : kWaitLimitNs;
   const int slots = a.K + (a.shared >= 0);
   for (int t0 = 0; t0 < a.S; t0 += kSelBatch) {
@@ -432,8 +437,8 @@ __device__ __forceinline__ void select_tokens(const RouterArgs& a, unsigned tag)
       const float sc = 1.0f / (1.0f + expf(-zs));
       const float ch = a.bias ? __fadd_rn(sc, __ldg(a.bias + e)) : sc;
       if (!late && (!isfinite(sc) || !isfinite(ch))) bad = true;
-      skey[tb][e] = order_key(ch);
-      ssc[tb][e] = sc;
+      skey[tb * E + e] = order_key(ch);
+      ssc[tb * E + e] = sc;
     }
     if (bad) set_error(a.err, COLI_E_NONFINITE);
     __syncthreads();
@@ -450,7 +455,7 @@ __device__ __forceinline__ void select_tokens(const RouterArgs& a, unsigned tag)
         }
         if (lane == 0 && no) *no = 0;
       } else {
-        uint32_t* kw = skey[warp];
+        uint32_t* kw = skey + warp * E;
         int mine = -1;
         float wmine = 0.f;
         for (int k = 0; k < a.K; k++) {
@@ -469,7 +474,7 @@ __device__ __forceinline__ void select_tokens(const RouterArgs& a, unsigned tag)
           __syncwarp();
           if (lane == k) {
             mine = (int)win;
-            wmine = ssc[warp][win];
+            wmine = ssc[warp * E + win];
           }
         }
         finish_rolled(mine, wmine, a.K, a.topp, a.norm_topk, a.routed_scale, a.shared, io, wo, no, a.table);
@@ -731,13 +736,18 @@ static RouterShape router_shape(const coli_ctx* ctx, int E, int D, bool vec) {
   return s;
 }
 
+template <int XT, int R>
+static cudaError_t launch_decode(const cudaLaunchConfig_t* cfg, const RouterArgs& a) {
+  return cudaLaunchKernelEx(cfg, router_decode_kernel<XT, R>, a);
+}
+
 template <int XT>
 static cudaError_t launch_decode_rows(const cudaLaunchConfig_t* cfg, int rows, const RouterArgs& a) {
   switch (rows) {
-    case 1: return cudaLaunchKernelEx(cfg, router_decode_kernel<XT, 1>, a);
-    case 2: return cudaLaunchKernelEx(cfg, router_decode_kernel<XT, 2>, a);
-    case 8: return cudaLaunchKernelEx(cfg, router_decode_kernel<XT, 8>, a);
-    default: return cudaLaunchKernelEx(cfg, router_decode_kernel<XT, 4>, a);
+    case 1: return launch_decode<XT, 1>(cfg, a);
+    case 2: return launch_decode<XT, 2>(cfg, a);
+    case 8: return launch_decode<XT, 8>(cfg, a);
+    default: return launch_decode<XT, 4>(cfg, a);
   }
 }
 
@@ -781,6 +791,7 @@ static int launch_router_decode(coli_ctx* ctx, const void* x, int x_dtype, int S
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sh.grid);
   cfg.blockDim = dim3(kRouterThreads);
+  cfg.dynamicSmemBytes = (size_t)std::min(S, kSelBatch) * E * 2 * sizeof(uint32_t);  // <= 32 KiB
   cfg.stream = ctx->stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
