@@ -38,6 +38,8 @@ def parse():
     ap.add_argument("--workload", default="decode")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill, shared-expert, dense-projection and compressed-tier figures")
+    ap.add_argument("--parallel", default="ep", choices=["ep", "replicas"],
+                    help="N > 1: split each layer's experts over the ranks (expert e on rank e mod N), or run N replicas")
     ap.add_argument("--cpu-steps", type=int, default=0, help=argparse.SUPPRESS)
     ap.add_argument("--check", default="", help=argparse.SUPPRESS)
     return ap.parse_args()
@@ -387,6 +389,22 @@ def accuracy_sample(cfg, Wr, bias, xs_host, outs, rs_host, n_ffn=2):
             "tolerance": "rel 1e-4 + abs 1e-5 x max(1, rms(y)) per element"}
 
 
+def ep_owned(e: int, rank: int, world: int) -> bool:
+    """Expert parallelism: rank `rank` holds expert e when e mod world == rank."""
+    return int(e) % int(world) == int(rank)
+
+
+def ep_token_seed(step: int) -> int:
+    """Under expert parallelism every rank works on the same token (each on its own experts)."""
+    return token_seed(0, step)
+
+
+def ep_job_us_per_layer(total_ms: float, steps: int) -> float:
+    """Whole-job time per layer under expert parallelism: the ranks run the same `steps` layers together, so
+    the job's time (the slowest rank's) is divided by the layers alone."""
+    return total_ms * 1000.0 / steps
+
+
 def token_seed(rank: int, step: int) -> int:
     """Seed of the token a rank processes at a step: every rank (replica) gets its own tokens."""
     return rank * 100000 + step
@@ -622,22 +640,28 @@ def gpu_arm(args, rank, world, local):
             dist.barrier()
         torch.cuda.synchronize()
 
-    # ---- eager pass (the same steps launched from Python), reported beside the graph number ----
+    # ---- timed region: each step launches the two C-ABI calls (coli_router_select, coli_expert_group) as a
+    # caller does, on inputs resident in HBM; before each step, outside its events, L2 is flushed ----
     for s in range(args.warmup):
         flush.zero_()
         layer.step(xs[s], rs[s], outs[s])
     barrier()
-    eager_ms = []
+    clocks = ClockSampler(local, enabled=not args.no_clocks and rank == 0)
+    time.sleep(0.3)
+    t_wall = time.perf_counter()
     for s in range(args.warmup, n_tok):
         flush.zero_()
         ev[s][0].record(stream)
         layer.step(xs[s], rs[s], outs[s])
         ev[s][1].record(stream)
     barrier()
-    eager_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.warmup, n_tok)]
+    wall = time.perf_counter() - t_wall
+    clock_info = clocks.stop()
+    assert B.coli_check_error(ctx) == 0, B.coli_last_error(ctx)
+    step_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.warmup, n_tok)]
 
-    # ---- timed region: one CUDA graph of the two C-ABI calls over fixed device buffers; before each
-    # step (outside its events) that step's resident inputs are copied in and L2 is flushed ----
+    # ---- the same steps replayed from one CUDA graph of the two calls over fixed device buffers, reported
+    # beside (each step's inputs are copied in and L2 is flushed before its events) ----
     xin, rin, gout = torch.empty_like(xs[0]), torch.empty_like(rs[0]), layer.outputs()
     xin.copy_(xs[0])
     rin.copy_(rs[0])
@@ -646,30 +670,21 @@ def gpu_arm(args, rank, world, local):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         layer.step(xin, rin, gout)
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_tok)]
 
     def graph_step(s):
         xin.copy_(xs[s])
         rin.copy_(rs[s])
         flush.zero_()
-        ev[s][0].record(stream)
+        gev[s][0].record(stream)
         graph.replay()
-        ev[s][1].record(stream)
-        for k in ("idx", "w", "n_sel", "y"):
-            outs[s][k].copy_(gout[k])
+        gev[s][1].record(stream)
 
-    for s in range(args.warmup):
+    for s in range(n_tok):
         graph_step(s)
     barrier()
-    clocks = ClockSampler(local, enabled=not args.no_clocks and rank == 0)
-    time.sleep(0.3)
-    t_wall = time.perf_counter()
-    for s in range(args.warmup, n_tok):
-        graph_step(s)
-    barrier()
-    wall = time.perf_counter() - t_wall
-    clock_info = clocks.stop()
     assert B.coli_check_error(ctx) == 0, B.coli_last_error(ctx)
-    step_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.warmup, n_tok)]
+    graph_ms = [gev[s][0].elapsed_time(gev[s][1]) for s in range(args.warmup, n_tok)]
     # back to back, reported beside the cold-L2 number: successive tokens' layers with no flush in between
     # (Wr and whatever else survives stays in L2); 8 graphs over 8 tokens' own buffers, replayed round robin
     # under one event pair
@@ -796,8 +811,9 @@ def gpu_arm(args, rank, world, local):
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "expert_bytes_per_layer": mean_expert_bytes,
                        "layer_hbm_gbs": layer_gbs, "layer_hbm_frac": layer_gbs / hbm_peak,
-                       "launch": "one CUDA graph (coli_router_select + coli_expert_group captured) replayed per step; the step's inputs are copied into its fixed buffers before the step's events",
-                       "eager_us": statistics.mean(eager_ms) * 1000.0,
+                       "launch": "coli_router_select + coli_expert_group launched per step (no graph), inputs resident in HBM",
+                       "graph_us": statistics.mean(graph_ms) * 1000.0,
+                       "graph": "the same two calls captured in one CUDA graph, replayed per step over fixed buffers into which each step's inputs are copied before its events",
                        "back_to_back_us": b2b_us, "back_to_back": "8 tokens' layer graphs replayed round robin, no L2 flush",
                        "p50_us": p50, "p10_us": float(np.percentile(step_ms, 10)) * 1000.0,
                        "p90_us": float(np.percentile(step_ms, 90)) * 1000.0,
@@ -846,6 +862,91 @@ def gpu_arm(args, rank, world, local):
     return 0
 
 
+def ep_arm(args, rank, world, local):
+    """N > 1, expert parallel: every rank routes the same tokens, runs its own experts' routes (issue + take),
+    all-gathers the partial rows (NCCL) and adds them in rank order with the residual last. The job time per
+    layer is the slowest rank's (strong scaling: the layer's work is fixed and split over the ranks)."""
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from int4_grouped_expert_router_gb300 import binding as B
+    from int4_grouped_expert_router_gb300.build import build
+    from int4_grouped_expert_router_gb300.ep import ExpertParallelLayer
+    from int4_grouped_expert_router_gb300.workload import CONFIGS, DeviceLayer, router_host_inputs
+
+    build()
+    torch.cuda.set_device(local)
+    dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    cfg = CONFIGS[args.workload]
+    if cfg.x_dtype != "f32" or cfg.S != 1:
+        raise SystemExit("the expert-parallel bench runs one f32 token per layer")
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    ctx = B.coli_init(local, stream)
+    layer = DeviceLayer(ctx, cfg, owned=lambda e: ep_owned(e, rank, world))
+    ep = ExpertParallelLayer(ctx, rank, world)
+    n_tok = args.warmup + args.steps
+    xs, rs = [], []
+    for s in range(n_tok):
+        x, _, _, resid = router_host_inputs(cfg, ep_token_seed(s))
+        xs.append(layer.act_tensor(x))
+        rs.append(layer.act_tensor(resid))
+    y = torch.empty(1, cfg.D, device="cuda")
+    flush_buf = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    flush_sink = torch.empty(1, dtype=torch.float32, device="cuda")
+
+    def flush():
+        flush_buf.zero_()
+        torch.sum(flush_buf, dim=0, out=flush_sink[0])
+
+    def step(s):
+        return ep.step(xs[s], layer.Wr, layer.bias, cfg.K, cfg.topp, cfg.norm_topk, cfg.routed_scale, rs[s], y)
+
+    for s in range(args.warmup):
+        flush()
+        step(s)
+    dist.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_tok)]
+    routes = []
+    for s in range(args.warmup, n_tok):
+        flush()
+        ev[s][0].record(stream)
+        idx, _, _ = step(s)
+        ev[s][1].record(stream)
+        routes.append(idx)
+    dist.barrier()
+    torch.cuda.synchronize()
+    assert B.coli_check_error(ctx) == 0, B.coli_last_error(ctx)
+    local_ms = sum(ev[s][0].elapsed_time(ev[s][1]) for s in range(args.warmup, n_tok))
+    total_ms = max_over_ranks(local_ms, dist, "cuda")
+    us = ep_job_us_per_layer(total_ms, args.steps)
+    layer_bytes, my_bytes = [], []
+    for idx in routes:
+        ids = sorted(set(int(e) for e in idx.cpu().numpy().reshape(-1) if e >= 0))
+        layer_bytes.append(sum(cfg.expert_bytes(e) for e in ids))
+        my_bytes.append(sum(cfg.expert_bytes(e) for e in ids if ep_owned(e, rank, world)))
+    hpeak, hkind = peaks()
+    if rank == 0:
+        gbs = float(np.mean(layer_bytes)) / (us * 1e-6) / 1e9
+        print(json.dumps({
+            "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": us / 1000.0, "higher_is_better": False, "scaling": "strong", "vs_baseline": None,
+            "dtype": "int4xf32", "data": "synthetic (seeded SplitMix64; shapes of the pages' GLM-5.2 decode layer)",
+            "config": {"workload": workload_desc(cfg), "parallelism": f"ep{world} (expert e on rank e mod {world})",
+                       "l2": "flushed between steps (256 MiB write then read, outside the events)",
+                       "launch": "router + routes shard + issue/take + NCCL all-gather + partials reduce per step",
+                       "expert_bytes_per_layer": float(np.mean(layer_bytes)),
+                       "rank0_expert_bytes_per_layer": float(np.mean(my_bytes)),
+                       "layer_hbm_gbs": gbs, "layer_hbm_frac_of_one_gpu": gbs / hpeak},
+        }))
+    layer.free()
+    B.coli_destroy(ctx)
+    dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse()
     if args.cpu_steps:
@@ -854,6 +955,8 @@ def main():
     rank, world, local = dist_env()
     if args.impl == "reference":
         return reference_arm(args, rank, world)
+    if world > 1 and args.parallel == "ep":
+        return ep_arm(args, rank, world, local)
     return gpu_arm(args, rank, world, local)
 
 

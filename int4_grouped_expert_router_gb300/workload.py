@@ -87,14 +87,18 @@ def router_host_inputs(cfg: LayerConfig, token0: int = 0):
 
 
 class DeviceLayer:
-    """All E experts of one layer uploaded to the library, plus device router weights."""
+    """The E experts of one layer uploaded to the library (or only those `owned(e)` accepts: one rank's
+    share under expert parallelism), plus device router weights."""
 
-    def __init__(self, ctx, cfg: LayerConfig, device="cuda", generate_on_device=None):
+    def __init__(self, ctx, cfg: LayerConfig, device="cuda", generate_on_device=None, owned=None):
         self.ctx, self.cfg, self.device = ctx, cfg, device
         if generate_on_device is None:
             generate_on_device = cfg.D * cfg.I * cfg.E > 64 * 1024 * 1024
         self.handles = []
         for e in range(cfg.E):
+            if owned is not None and not owned(e):
+                self.handles.append(None)
+                continue
             gs = cfg.gs_of(e)
             hs = []
             for which, (rows, cols) in (("gate", (cfg.I, cfg.D)), ("up", (cfg.I, cfg.D)), ("down", (cfg.D, cfg.I))):
@@ -131,9 +135,10 @@ class DeviceLayer:
         B.coli_expert_group(self.ctx, x, out["idx"], out["w"], out["n_sel"], c.K, resid, out["y"])
 
     def free(self):
-        for e in range(self.cfg.E):
-            B.coli_expert_table_set(self.ctx, e, 0, 0, 0)
+        for e, hs in enumerate(self.handles):
+            if hs is not None:
+                B.coli_expert_table_set(self.ctx, e, 0, 0, 0)
         for hs in self.handles:
-            for h in hs:
+            for h in hs or ():
                 B.coli_expert_free(self.ctx, h)
         self.handles = []

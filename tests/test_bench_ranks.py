@@ -66,3 +66,37 @@ def test_reference_arm_prints_on_rank0_only():
     with contextlib.redirect_stdout(buf):
         assert bench.reference_arm(A(), 1, 2) == 0
     assert buf.getvalue() == ""
+
+
+def _ep_rank_main(rank, world, port, local_ms, out):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        owned = [e for e in range(256) if bench.ep_owned(e, rank, world)]
+        seeds = [bench.ep_token_seed(s) for s in range(20)]
+        m = bench.max_over_ranks(local_ms[rank], dist, "cpu")
+        out[rank] = (owned, seeds, m, bench.ep_job_us_per_layer(m, 10))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_expert_parallel_ranks_split_experts_and_share_tokens(world):
+    """--gpus N with expert parallelism: the ranks own disjoint experts that cover the layer, route the same
+    tokens, and the job's per-layer time is the slowest rank's time divided by the layers (not by N: the ranks
+    run each layer together)."""
+    port = _free_port()
+    local_ms = [1.0 + r for r in range(world)]
+    with mp.Manager() as mgr:
+        out = mgr.dict()
+        mp.spawn(_ep_rank_main, args=(world, port, local_ms, out), nprocs=world, join=True)
+        res = dict(out)
+    owned = [set(res[r][0]) for r in range(world)]
+    assert set().union(*owned) == set(range(256))
+    assert sum(len(o) for o in owned) == 256
+    assert all(res[r][1] == res[0][1] for r in range(world))
+    for r in range(world):
+        assert res[r][2] == max(local_ms)
+        assert res[r][3] == pytest.approx(max(local_ms) * 1000.0 / 10)

@@ -92,3 +92,48 @@ def test_unowned_kept_slot_is_reported(ctx):
     B.coli_routes_shard(ctx, idx, w, torch.tensor([1], dtype=torch.int32, device="cuda"), 1, 2, si, sw, sn)
     assert B.coli_check_error(ctx) == 0  # the bad slot is beyond n_sel: ignored
     assert si.tolist() == [[3, -1, -1]] and sn.tolist() == [1]
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_each_rank_holds_only_its_experts(world):
+    """The deployment shape of the expert-parallel bench: one context per simulated rank whose table holds only
+    the experts e with e mod world == rank (DeviceLayer owned=...), every rank routing the same token itself;
+    the rank-order reduce of their partials matches the oracle's expert-parallel block."""
+    import bench
+    cfg = LayerConfig("ep-owned", D=1024, I=256, E=16, K=8, routed_scale=2.5)
+    ctxs = [Ctx() for _ in range(world)]
+    layers = [DeviceLayer(c.ctx, cfg, owned=lambda e, r=r: bench.ep_owned(e, r, world)) for r, c in enumerate(ctxs)]
+    try:
+        x, _, _, resid = router_host_inputs(cfg)
+        parts = torch.empty(world, 1, cfg.D, device="cuda")
+        routes = None
+        for r, (c, layer) in enumerate(zip(ctxs, layers)):
+            xt, rt = layer.act_tensor(x), layer.act_tensor(resid)
+            ep = ExpertParallelLayer(c.ctx, r, world)
+            idx = torch.empty(1, cfg.K, dtype=torch.int32, device="cuda")
+            w = torch.empty(1, cfg.K, device="cuda")
+            n = torch.empty(1, dtype=torch.int32, device="cuda")
+            B.coli_router_select(c.ctx, xt, layer.Wr, layer.bias, cfg.K, cfg.topp, cfg.norm_topk, cfg.routed_scale,
+                                 idx, w, n)
+            si, sw, sn = torch.empty_like(idx), torch.empty_like(w), torch.empty_like(n)
+            B.coli_routes_shard(c.ctx, idx, w, n, r, world, si, sw, sn)
+            B.coli_expert_group_issue(c.ctx, xt, si, sw, sn, cfg.K)
+            B.coli_expert_group_take(c.ctx, None, parts[r])
+            assert B.coli_check_error(c.ctx) == 0, B.coli_last_error(c.ctx)
+            got = tuple(to_np(t) for t in (idx, w, n))
+            if routes is None:
+                routes = got
+            else:  # every rank routes alike
+                assert all(np.array_equal(a, b) for a, b in zip(got, routes))
+            assert ep.world == world
+        y = torch.empty(1, cfg.D, device="cuda")
+        B.coli_partials_reduce(ctxs[0].ctx, parts, layers[0].act_tensor(resid), y)
+        assert B.coli_check_error(ctxs[0].ctx) == 0
+        idx, w, n = routes
+        ref = O.ep_layer(x, oracle_experts(cfg, idx), idx, w, n, world, resid)
+        assert_close(to_np(y), ref, F32_RTOL, f32_atol(ref), f"owned experts, world {world}")
+    finally:
+        for layer in layers:
+            layer.free()
+        for c in ctxs:
+            c.close()
