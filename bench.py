@@ -134,6 +134,49 @@ def ans_leg(ctx, stream, flush, nbytes, steps=10, warmup=3):
             "stored_gbs": stored / (us * 1e-6) / 1e9, "exact": ok, "l2": "flushed between steps"}
 
 
+def ans_gemv_leg(ctx, stream, flush, rows=2048, cols=6144, steps=10, warmup=3):
+    """The compressed tier's fused block decode + GEMV on a gate-shaped tensor [2048 x 6144] (per-row scales,
+    quantised-weight-like nibbles), beside decoding the same stream to a raw buffer and the raw int4 GEMV
+    of the same tensor (uploaded uncompressed): event-timed, cold L2."""
+    import numpy as np
+    import torch
+
+    from int4_grouped_expert_router_gb300 import binding as B
+    from int4_grouped_expert_router_gb300 import synth
+
+    packed = synth.gaussian_nibble_bytes(synth.stream_seed(904, "tier-gemv"), rows * cols // 2, 2.5)
+    scales = synth.uniform(synth.stream_seed(904, "tier-gemv-s"), rows, 0.005, 0.02).astype(np.float32)
+    h = B.coli_ans_upload(ctx, packed.tobytes())
+    raw, stored = B.coli_ans_info(ctx, h)
+    W = B.coli_expert_upload(ctx, torch.from_numpy(packed), torch.from_numpy(scales), rows, cols, 0)
+    st = torch.from_numpy(scales).cuda()
+    x = torch.from_numpy(synth.normal(synth.stream_seed(904, "tier-gemv-x"), cols).astype(np.float32)).cuda()
+    y_f, y_r = torch.empty(rows, device="cuda"), torch.empty(1, rows, device="cuda")
+    out = torch.empty(raw, dtype=torch.uint8, device="cuda")
+    calls = {"fused": lambda: B.coli_ans_w4_linear(ctx, h, st, rows, cols, 0, x, None, y_f),
+             "decode_only": lambda: B.coli_ans_decode(ctx, h, out),
+             "raw_gemv": lambda: B.coli_w4_linear(ctx, W, x.view(1, cols), None, y_r)}
+    res = {}
+    for name, call in calls.items():
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(warmup + steps)]
+        with torch.cuda.stream(stream):
+            for s in range(warmup + steps):
+                flush.zero_()
+                ev[s][0].record(stream)
+                call()
+                ev[s][1].record(stream)
+        torch.cuda.synchronize()
+        res[name] = statistics.mean(ev[s][0].elapsed_time(ev[s][1]) for s in range(warmup, warmup + steps)) * 1000.0
+    assert B.coli_check_error(ctx) == 0, B.coli_last_error(ctx)
+    max_diff = float((y_f - y_r.view(-1)).abs().max().item())
+    B.coli_ans_free(ctx, h)
+    B.coli_expert_free(ctx, W)
+    return {"workload": f"int4 [{rows} x {cols}], per-row scales, one token; stream of 4 KiB rANS blocks",
+            "fused_us": res["fused"], "decode_only_us": res["decode_only"], "raw_gemv_us": res["raw_gemv"],
+            "stored_over_raw": stored / raw, "fused_raw_gbs": raw / (res["fused"] * 1e-6) / 1e9,
+            "max_abs_diff_fused_vs_raw_gemv": max_diff, "l2": "flushed between steps"}
+
+
 def shared_expert_leg(ctx, stream, flush, layer, xs, rs, steps=20, warmup=3):
     """The decode layer with an always-chosen shared expert (weight 1, the routed experts' shape): the
     router appends it after the kept slots and one grouped call runs all K + 1 experts, as one CUDA
@@ -831,7 +874,8 @@ def gpu_arm(args, rank, world, local):
     if rank == 0 and not args.no_prefill:
         for name, leg in (("shared_expert", lambda: shared_expert_leg(ctx, stream, flush, layer, xs, rs)),
                           ("dense_projection", lambda: linear_leg(ctx, stream, flush, cfg.D)),
-                          ("compressed_tier_decode", lambda: ans_leg(ctx, stream, flush, cfg.I * cfg.D))):
+                          ("compressed_tier_decode", lambda: ans_leg(ctx, stream, flush, cfg.I * cfg.D)),
+                          ("compressed_tier_gemv", lambda: ans_gemv_leg(ctx, stream, flush))):
             try:
                 extra[name] = leg()
             except Exception as exc:  # these figures must not hide the decode number

@@ -310,6 +310,25 @@ COLI_API int coli_ans_info(coli_ctx *ctx, uint64_t handle, uint64_t *raw_bytes, 
 COLI_API int coli_ans_decode(coli_ctx *ctx, uint64_t handle, uint8_t *out);
 COLI_API int coli_ans_free(coli_ctx *ctx, uint64_t handle);
 
+/*
+ * Compressed tier, fused block decode + GEMV ([tier], comment "Fused decode/matvec feasibility
+ * result": each block is decoded on chip and its row partials computed at once, writing only small
+ * partial sums instead of the raw tensor). The uploaded stream (coli_ans_upload) must hold an int4
+ * tensor W [O x I] in the packed format of coli_expert_upload: O rows of I/2 bytes, so raw bytes =
+ * O * I / 2. For one token,
+ *   y[o] = resid[o] + sum_i W[o, i] x[i],   W[o, i] = scale(o, i) (n(o, i) - 8)
+ * with scales as for coli_expert_upload (gs == 0: [O] per row; gs > 0 and even: [O x ceil(I/gs)]),
+ * a device pointer the caller keeps. Arithmetic in binary32: each decoded nibble's term
+ * (n - 8) x[i] (times its group's scale when gs > 0) is summed per lane, the lanes' sums in lane
+ * order per (block, row), a row's blocks in block order, then times the row scale (gs == 0) and
+ * plus the residual; deterministic, bit-identical from run to run. x [I], resid [O] or NULL, y [O]:
+ * x_dtype (f32 or bf16, y rounded to bf16 once), device pointers. Limits: I even, 256 <= I <= 16384.
+ * COLI_E_INVAL for a bad handle, shape, pointer or dtype; a stream that fails its own consistency
+ * checks sets COLI_E_FORMAT in the device error word. Profiled as COLI_KERNEL_LINEAR.
+ */
+COLI_API int coli_ans_w4_linear(coli_ctx *ctx, uint64_t handle, const float *scales, int O, int I, int gs,
+                                const void *x, int x_dtype, const void *resid, void *y);
+
 #ifdef __cplusplus
 }
 #endif

@@ -67,6 +67,7 @@ SIGNATURES = {
     "coli_ans_info": (_I, [_P, _U64, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]),
     "coli_ans_decode": (_I, [_P, _U64, _P]),
     "coli_ans_free": (_I, [_P, _U64]),
+    "coli_ans_w4_linear": (_I, [_P, _U64, _P, _I, _I, _I, _P, _I, _P, _P]),
     "coli_expert_upload": (_U64, [_P, _P, _P, _I, _I, _I]),
     "coli_expert_free": (_I, [_P, _U64]),
     "coli_tensor_shape": (_I, [_P, _U64, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
@@ -363,6 +364,20 @@ def coli_ans_info(ctx, handle):
     raw, stored = ctypes.c_uint64(), ctypes.c_uint64()
     _check(ctx, library().coli_ans_info(ctx, handle, ctypes.byref(raw), ctypes.byref(stored)), "coli_ans_info")
     return raw.value, stored.value
+
+
+def coli_ans_w4_linear(ctx, handle, scales, O, I, gs, x, resid, y):
+    """y = resid + W x for an int4 tensor W [O x I] kept as a compressed stream (fused decode + GEMV);
+    scales is the f32 scale tensor of W on the device, x [I] (or [1 x I]), y and resid [O]."""
+    _dev(scales, torch.float32, "scales")
+    _dev(x, name="x")
+    _dev(resid, x.dtype, "resid")
+    _dev(y, x.dtype, "y")
+    if x.numel() != I or y.numel() != O or (resid is not None and resid.numel() != O):
+        raise ValueError("ans_w4_linear: x must hold I values and y, resid O")
+    rc = library().coli_ans_w4_linear(ctx, handle, _ptr(scales), O, I, gs, _ptr(x), act_dtype(x), _ptr(resid),
+                                      _ptr(y))
+    return _check(ctx, rc, "coli_ans_w4_linear")
 
 
 def coli_ans_decode(ctx, handle, out):

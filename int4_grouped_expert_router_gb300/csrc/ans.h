@@ -20,6 +20,9 @@ struct AnsStream {
   int blocks = 0;
 };
 std::vector<AnsStream>& ans_streams(coli_ctx* ctx);
+// y = resid + W x for an int4 tensor W [O x I] kept as a compressed stream (fused block decode + GEMV)
+int launch_ans_gemv(coli_ctx* ctx, const AnsStream& st, const float* scales, int O, int I, int gs, const void* x,
+                    int x_dtype, const void* resid, void* y);
 void ans_release_all(coli_ctx* ctx);
 
 }  // namespace coli

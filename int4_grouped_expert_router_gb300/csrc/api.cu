@@ -681,6 +681,22 @@ int coli_ans_decode(coli_ctx* ctx, uint64_t h, uint8_t* out) {
   return rc;
 }
 
+int coli_ans_w4_linear(coli_ctx* ctx, uint64_t h, const float* scales, int O, int I, int gs, const void* x,
+                       int x_dtype, const void* resid, void* y) {
+  if (!ctx) return COLI_E_INVAL;
+  AnsStream* st = ans_stream(ctx, h);
+  if (!st) return fail(ctx, COLI_E_INVAL, "ans_w4_linear: unknown handle");
+  if (!scales || !x || !y) return fail(ctx, COLI_E_INVAL, "ans_w4_linear: NULL pointer");
+  if (x_dtype != COLI_DTYPE_F32 && x_dtype != COLI_DTYPE_BF16) return fail(ctx, COLI_E_INVAL, "ans_w4_linear: dtype");
+  if (O < 1 || I < 256 || I > 16384 || I % 2 || gs < 0 || gs % 2 || (uint64_t)O * (uint64_t)(I / 2) != st->raw)
+    return fail(ctx, COLI_E_INVAL, "ans_w4_linear: shape does not match the stream (O rows of I/2 bytes, I even, 256 <= I <= 16384)");
+  if (injected(ctx)) return COLI_E_INJECTED;
+  cudaSetDevice(ctx->device);
+  int rc = launch_ans_gemv(ctx, *st, scales, O, I, gs, x, x_dtype, resid, y);
+  if (rc == COLI_OK) ctx->compute_calls++;
+  return rc;
+}
+
 int coli_ans_free(coli_ctx* ctx, uint64_t h) {
   if (!ctx) return COLI_E_INVAL;
   AnsStream* st = ans_stream(ctx, h);
