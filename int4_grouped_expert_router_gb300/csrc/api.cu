@@ -610,7 +610,9 @@ int coli_w4_linear(coli_ctx* ctx, uint64_t W, const void* x, int x_dtype, int S,
   if (injected(ctx)) return COLI_E_INJECTED;
   cudaSetDevice(ctx->device);
   const HostTensor& t = ctx->tensors[W - 1];
-  int rc = launch_linear(ctx, t.desc, t.d_solo, x, x_dtype, S, resid, y);
+  // one token through a tensor whose rows and scales can be streamed in 16-row units: the streaming kernel
+  int rc = S == 1 && ctx->stream_ffn && stream_linear_ok(t) ? launch_stream_linear(ctx, t, x, x_dtype, resid, y)
+                                                           : launch_linear(ctx, t.desc, t.d_solo, x, x_dtype, S, resid, y);
   if (rc == COLI_OK) ctx->compute_calls++;
   return rc;
 }

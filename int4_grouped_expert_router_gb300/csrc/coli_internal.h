@@ -203,6 +203,8 @@ int launch_take(coli_ctx* ctx, int S, int D, int n, const void* resid, int dtype
 // streams down tensors from (built by coli_expert_table_set).
 bool stream_eligible(const coli_ctx* ctx, int S);
 bool stream_tensor_ok(const HostTensor& t, bool as_down);
+bool stream_linear_ok(const HostTensor& t);
+int launch_stream_linear(coli_ctx* ctx, const HostTensor& t, const void* x, int x_dtype, const void* resid, void* y);
 int build_stream_view(coli_ctx* ctx, HostTensor& t);
 int launch_stream_ffn(coli_ctx* ctx, const void* x, int x_dtype, const int32_t* idx, const float* w,
                       const int32_t* n_sel, int K, const void* resid, void* y, int y_dtype);

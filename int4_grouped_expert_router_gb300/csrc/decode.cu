@@ -495,6 +495,217 @@ __global__ void __launch_bounds__(256) stream_reduce_kernel(const float* __restr
 }
 
 // ------------------------------------------------------------------------------------------
+// One token through a dense int4 tensor, y = resid + W x (coli_w4_linear with S = 1): the gate/up role
+// of the streaming FFN on its own. Units of 16 rows; CTA c streams the rows of its contiguous range of
+// units through a ring of bulk-copied stages (16 rows and their scales each); NW row warps dot them with
+// x's limbs (one 32-column chunk per thread, rows r0 + 2i, i < 8) and leave each warp's row sums; a
+// finishing warp adds a row's warp sums in warp order, applies the row scale and the residual and writes
+// y. A unit's rows belong to one CTA, so no CTA waits for another and no reduce follows.
+// ------------------------------------------------------------------------------------------
+
+constexpr int kLinStages = 3;
+
+struct LinCtrl {
+  uint64_t full[kLinStages], empty[kLinStages];
+  uint64_t redf[kHB], redfree[kHB];
+  uint64_t xfull;
+  float red[kHB][kStMaxWarps][8];  // per row warp: its 8 row sums of a unit
+  float fs[kHB][16];
+};
+
+struct LinParams {
+  const uint8_t* w;  // rows of I/2 bytes
+  const float* s;    // per-row scales, or G per row
+  const void* x;
+  const void* resid;
+  void* y;
+  int* err;
+  int O, I, G, gs, mode, x_dtype, x_bulk;
+  uint32_t sb;       // stage bytes
+  unsigned long long wait_ns;
+};
+
+__global__ void __launch_bounds__(448, 1) stream_linear_kernel(const LinParams P) {
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 127) & ~uintptr_t(127));
+  LinCtrl& cs = *reinterpret_cast<LinCtrl*>(base);
+  uint8_t* xbuf = base + (sizeof(LinCtrl) + 127) / 128 * 128;
+  uint8_t* ring = xbuf + (size_t)P.I * 4;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int I = P.I, NW = I / 512, NCT = 32 * NW, C = I / 32;
+  const uint32_t pitch = (uint32_t)I / 2, rows_bytes = 16u * pitch;
+  const uint64_t lim = P.wait_ns ? P.wait_ns : kWaitLimitNs;
+  const int W_P = NW, W_F = NW + 1;  // producer warp, finishing warp
+  if (tid == 0) {
+    for (int s = 0; s < kLinStages; s++) {
+      mbar_init(&cs.full[s], 1);
+      mbar_init(&cs.empty[s], NW);
+    }
+    for (int b = 0; b < kHB; b++) {
+      mbar_init(&cs.redf[b], NCT);
+      mbar_init(&cs.redfree[b], 1);
+    }
+    mbar_init(&cs.xfull, 1);
+    mbar_fence_init();
+    if (P.x_bulk) {
+      const uint32_t xbytes = (uint32_t)I * (P.x_dtype == COLI_DTYPE_F32 ? 4u : 2u);
+      mbar_arrive_expect_tx(&cs.xfull, xbytes);
+      bulk_g2s(xbuf, P.x, xbytes, &cs.xfull);
+    }
+  }
+  __syncthreads();
+  const int U = P.O / 16;
+  const int ubeg = (int)((long long)blockIdx.x * U / gridDim.x), uend = (int)((long long)(blockIdx.x + 1) * U / gridDim.x);
+  bool stop = false;
+  if (warp < NW) {
+    // ---------------- row warps ----------------
+    const int c = tid % C, r0 = tid / C;
+    Limbs X;
+    {
+      float xv[32];
+      if (P.x_bulk) {
+        bool late = false;
+        role_wait(&cs.xfull, 0, lim, late, P.err);
+        if (P.x_dtype == COLI_DTYPE_F32) {
+#pragma unroll
+          for (int i = 0; i < 8; i++) {
+            const uint4 u = lds128(xbuf + 128 * c + 16 * i);
+            xv[4 * i] = __uint_as_float(u.x);
+            xv[4 * i + 1] = __uint_as_float(u.y);
+            xv[4 * i + 2] = __uint_as_float(u.z);
+            xv[4 * i + 3] = __uint_as_float(u.w);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; i++) {
+            const uint4 u = lds128(xbuf + 64 * c + 16 * i);
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int h = 0; h < 4; h++) {
+              xv[8 * i + 2 * h] = __uint_as_float(w4[h] << 16);
+              xv[8 * i + 2 * h + 1] = __uint_as_float(w4[h] & 0xffff0000u);
+            }
+          }
+        }
+      } else {
+        load_chunk_f32(P.x, P.x_dtype, 0, 32 * c, I, xv);
+      }
+      if (!make_limbs(xv, X)) set_error(P.err, COLI_E_NONFINITE);
+    }
+    const int grp = P.mode == SCALE_CHUNK ? (32 * c) / P.gs : 0;
+    uint32_t s = 0, ph = 0;
+    int n = 0;
+    for (int u = ubeg; u < uend && !stop; u++) {
+      const int b = n % kHB;
+      const uint32_t use = (uint32_t)(n / kHB);
+      role_wait(&cs.full[s], ph, lim, stop, P.err);
+      const uint8_t* st = ring + (size_t)s * P.sb;
+      const float* sc = reinterpret_cast<const float*>(st + rows_bytes);
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 8; i++) {
+        float d = chunk_dot(lds128(st + (r0 + 2 * i) * pitch + 16 * c), X);
+        if (P.mode == SCALE_CHUNK) d *= sc[(r0 + 2 * i) * P.G + grp];
+        v[i] = d;
+      }
+      if (use >= 1) role_wait(&cs.redfree[b], (use - 1) & 1, lim, stop, P.err);
+      if (warp == 0 && lane < 16) cs.fs[b][lane] = P.mode == SCALE_ROW ? sc[lane] : 1.f;
+      __syncwarp();
+      if (lane == 0 && !stop) mbar_arrive(&cs.empty[s]);
+      if (++s == (uint32_t)kLinStages) {
+        s = 0;
+        ph ^= 1u;
+      }
+      warp_transpose_reduce<8>(v, lane);
+      if (!(lane & 3)) cs.red[b][warp][lane >> 2] = v[0];
+      mbar_arrive(&cs.redf[b]);
+      n++;
+    }
+  } else if (warp == W_P) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      const uint32_t sbytes = P.mode == SCALE_ROW ? 64u : 64u * (uint32_t)P.G;
+      uint32_t q = 0, s = 0, ph = 0;
+      for (int u = ubeg; u < uend && !stop; u++) {
+        if (q >= (uint32_t)kLinStages) role_wait(&cs.empty[s], ph ^ 1u, lim, stop, P.err);
+        if (stop) break;
+        mbar_arrive_expect_tx(&cs.full[s], rows_bytes + sbytes);
+        uint8_t* dst = ring + (size_t)s * P.sb;
+        bulk_g2s_stream(dst, P.w + (size_t)u * rows_bytes, rows_bytes, &cs.full[s], pol);
+        bulk_g2s(dst + rows_bytes, P.s + (size_t)u * 16 * (P.mode == SCALE_ROW ? 1 : P.G), sbytes, &cs.full[s]);
+        q++;
+        if (++s == (uint32_t)kLinStages) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      for (uint32_t r = q > (uint32_t)kLinStages ? q - kLinStages : 0; r < q; r++)
+        (void)mbar_wait_suspend(&cs.full[r % kLinStages], (r / kLinStages) & 1, lim);
+    }
+  } else if (warp == W_F) {
+    // ---------------- finishing warp: row sums -> y ----------------
+    int n = 0;
+    for (int u = ubeg; u < uend && !stop; u++) {
+      const int b = n % kHB;
+      role_wait(&cs.redf[b], (uint32_t)(n / kHB) & 1, lim, stop, P.err);
+      if (lane < 16 && !stop) {
+        // row `lane` = r0 + 2 i of the unit is value i of the warps with that r0
+        const int rg = lane & 1, v = lane >> 1;
+        float t = 0.f;
+        for (int w = rg * (NW / 2); w < (rg + 1) * (NW / 2); w++) t += cs.red[b][w][v];
+        t *= cs.fs[b][lane];
+        const int row = 16 * u + lane;
+        if (P.resid) t = load_act(P.resid, P.x_dtype, row) + t;
+        if (P.x_dtype == COLI_DTYPE_F32)
+          static_cast<float*>(P.y)[row] = t;
+        else
+          static_cast<uint16_t*>(P.y)[row] = f32_to_bf16_rn(t);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&cs.redfree[b]);
+      n++;
+    }
+  }
+  // never leave with the x copy in flight (it completes before any row warp starts; bounded)
+  if (tid == 0 && P.x_bulk) (void)mbar_wait_suspend(&cs.xfull, 0, lim);
+}
+
+bool stream_linear_ok(const HostTensor& t) {
+  return t.I % 1024 == 0 && t.I <= 512 * kStMaxWarps && t.O % 16 == 0 && (t.gs == 0 || t.gs % 32 == 0) &&
+         t.pitch == (uint32_t)t.I / 2;
+}
+
+int launch_stream_linear(coli_ctx* ctx, const HostTensor& t, const void* x, int x_dtype, const void* resid, void* y) {
+  LinParams P;
+  P.w = t.w;
+  P.s = t.s;
+  P.x = x;
+  P.resid = resid;
+  P.y = y;
+  P.err = ctx->d_status;
+  P.O = t.O;
+  P.I = t.I;
+  P.G = t.G;
+  P.gs = t.gs;
+  P.mode = t.desc.mode;
+  P.x_dtype = x_dtype;
+  P.x_bulk = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+  P.sb = (uint32_t)align_up(16u * (uint32_t)t.I / 2 + 64u * (uint32_t)t.G, 128);
+  P.wait_ns = ctx->wait_ns;
+  const int NW = t.I / 512;
+  const size_t smem = 128 + align_up(sizeof(LinCtrl), 128) + (size_t)t.I * 4 + (size_t)kLinStages * P.sb;
+  cudaError_t e = cudaFuncSetAttribute(stream_linear_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "stream linear: shared memory attribute");
+  int grid = ctx->num_sms;
+  if (grid > t.O / 16) grid = t.O / 16;
+  ProfScope prof(ctx, COLI_KERNEL_LINEAR);
+  e = launch_k(stream_linear_kernel, grid, 32 * (NW + 2), smem, ctx->stream, false, false, P);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "stream linear launch");
+  return COLI_OK;
+}
+
+// ------------------------------------------------------------------------------------------
 // Panel-major view of a down tensor: column block p (kPanelCols columns) of every row, contiguous.
 // ------------------------------------------------------------------------------------------
 

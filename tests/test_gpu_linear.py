@@ -65,6 +65,11 @@ CASES = [
     ("s1-g32-f32", 1000, 1000, 32, 1, "f32", True),
     ("s1-wide-640-threads", 96, 20000, 128, 1, "f32", True),
     ("s1-bf16-6144", 6144, 6144, 0, 1, "bf16", True),
+    # one token through tensors the streaming kernel takes (I a multiple of 1024 up to 6144, O of 16, gs 0 or 32 k)
+    ("s1-stream-g64", 2048, 6144, 64, 1, "f32", True),
+    ("s1-stream-g32-bf16", 4096, 2048, 32, 1, "bf16", False),
+    ("s1-stream-3-units", 48, 1024, 0, 1, "f32", True),
+    ("s1-stream-I5120", 1040, 5120, 0, 1, "f32", False),
 ]
 
 
@@ -174,3 +179,29 @@ def test_shared_expert_layer(ctx, cfg):
         for h in hs:
             B.coli_expert_free(ctx, h)
         layer.free()
+
+
+@pytest.mark.parametrize("O_,I_,gs", [(6144, 6144, 0), (2048, 6144, 64)])
+def test_one_token_streaming_matches_the_ring_form(O_, I_, gs):
+    """One token: the streaming kernel (default) against the down-kernel ring form (COLI_DECODE_STREAM=0)."""
+    from gpu_util import Ctx
+    T, x, r = make_case(O_ + gs, O_, I_, gs, 1, "f32")
+    cs, c2 = Ctx(), Ctx.with_env(COLI_DECODE_STREAM=0)
+    hs = [B.coli_expert_upload(c.ctx, torch.from_numpy(T.packed.reshape(-1).copy()), torch.from_numpy(T.scales.copy()),
+                               O_, I_, gs) for c in (cs, c2)]
+    try:
+        xt, rt = dev(x, "f32"), dev(r, "f32")
+        ys = [torch.empty(1, O_, device="cuda") for _ in range(2)]
+        for c, h, y in zip((cs, c2), hs, ys):
+            B.coli_profile_enable(c.ctx, 1)
+            B.coli_profile_read(c.ctx, B.COLI_KERNEL_LINEAR)
+            B.coli_w4_linear(c.ctx, h, xt, rt, y)
+            assert B.coli_check_error(c.ctx) == 0, B.coli_last_error(c.ctx)
+            assert B.coli_profile_read(c.ctx, B.COLI_KERNEL_LINEAR)[1] == 1
+        ref = O.w4_linear(x, T, r)
+        assert_close(to_np(ys[0]), ref, F32_RTOL, f32_atol(ref), "streaming")
+        assert_close(to_np(ys[1]), to_np(ys[0]), 2 * F32_RTOL, 2 * f32_atol(ref), "streaming vs rings")
+    finally:
+        for c, h in zip((cs, c2), hs):
+            B.coli_expert_free(c.ctx, h)
+            c.close()
