@@ -41,7 +41,10 @@ def parse():
     ap.add_argument("--parallel", default="ep", choices=["ep", "replicas"],
                     help="N > 1: split each layer's experts over the ranks (expert e on rank e mod N), or run N replicas")
     ap.add_argument("--cpu-steps", type=int, default=0, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-offset", type=int, default=0, help=argparse.SUPPRESS)
     ap.add_argument("--check", default="", help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-procs", type=int, default=0,
+                    help="oracle processes of the CPU baseline (default: one per core this process may run on, at most 32)")
     return ap.parse_args()
 
 
@@ -475,12 +478,13 @@ def workload_desc(cfg):
 
 
 # ------------------------------------------------------------------------------------------------
-# CPU oracle leg (reference arm and cpu_baseline): runs in a child process pinned to one thread.
+# CPU oracle leg (reference arm and cpu_baseline): runs in child processes, one per core, each pinned to one
+# thread.
 # ------------------------------------------------------------------------------------------------
 
-def cpu_step_worker(workload: str, steps: int, warmup: int, check: str = ""):
-    """The oracle in steps of a bounded sample: step s routes token s (the whole router) and runs ONE of
-    its kept experts (slot s mod n_sel). The per-layer figure is the mean router time plus the mean
+def cpu_step_worker(workload: str, steps: int, warmup: int, check: str = "", offset: int = 0):
+    """The oracle in steps of a bounded sample: step s routes token offset + s (the whole router) and runs
+    ONE of its kept experts (slot s mod n_sel). The per-layer figure is the mean router time plus the mean
     kept count times the mean expert time."""
     import oracle.moe as O
     from int4_grouped_expert_router_gb300.workload import CONFIGS, host_expert, router_host_inputs
@@ -488,7 +492,7 @@ def cpu_step_worker(workload: str, steps: int, warmup: int, check: str = ""):
     cfg = CONFIGS[workload]
     t_router, t_expert, kept, t_step = [], [], [], []
     for s in range(warmup + steps):
-        x, Wr, bias, resid = router_host_inputs(cfg, s)
+        x, Wr, bias, resid = router_host_inputs(cfg, offset + s)
         t0 = time.perf_counter()
         idx, w, n, _ = O.router_select(x, Wr, bias, cfg.K, cfg.topp, cfg.norm_topk, cfg.routed_scale)
         t1 = time.perf_counter()
@@ -515,26 +519,73 @@ def cpu_step_worker(workload: str, steps: int, warmup: int, check: str = ""):
     print(json.dumps(res))
 
 
-def run_oracle_steps(workload: str, steps: int, warmup: int, check: str = ""):
-    """cpu_step_worker in a fresh single-threaded process (no GPU visible); returns its JSON."""
+def host_cores() -> int:
+    """Cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def combine_oracle_results(results):
+    """Oracle processes run side by side on separate cores, each timing its own tokens: the box finishes
+    layers at the sum of their rates, so its time per layer is 1 / sum(1 / t_i). Process 0's fields (and
+    its accuracy check) are kept; `single_core_us` is the median single-process figure."""
+    rate = sum(1.0 / r["us_per_layer"] for r in results)
+    out = dict(results[0])
+    out["us_per_layer"] = 1.0 / rate
+    out["single_core_us"] = statistics.median(r["us_per_layer"] for r in results)
+    out["procs"] = len(results)
+    out["steps"] = sum(r["steps"] for r in results)
+    out["router_ms"] = statistics.mean(r["router_ms"] for r in results)
+    out["expert_ms"] = statistics.mean(r["expert_ms"] for r in results)
+    out["kept"] = statistics.mean(r["kept"] for r in results)
+    out["ms_per_step"] = statistics.mean(r["ms_per_step"] for r in results)
+    return out
+
+
+def run_oracle_steps(workload: str, steps: int, warmup: int, check: str = "", procs: int = 1):
+    """cpu_step_worker in `procs` fresh single-threaded processes run at the same time (no GPU visible),
+    each on its own tokens (process i starts at token 1000 i); only process 0 checks the GPU's tokens.
+    Returns the combined JSON (combine_oracle_results)."""
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
-    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-steps", str(steps), "--warmup", str(warmup),
-           "--workload", workload]
-    if check:
-        cmd += ["--check", check]
-    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=3600)
-    if r.returncode != 0:
-        raise RuntimeError(f"oracle timing failed: {r.stderr[-2000:]}")
-    return json.loads(r.stdout.strip().splitlines()[-1])
+    children = []
+    for i in range(max(1, procs)):
+        cmd = [sys.executable, os.path.abspath(__file__), "--cpu-steps", str(steps), "--warmup", str(warmup),
+               "--workload", workload, "--cpu-offset", str(1000 * i)]
+        if check and i == 0:
+            cmd += ["--check", check]
+        children.append(subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True, env=env))
+    results, errors = [], []
+    for ch in children:
+        try:
+            out, err = ch.communicate(timeout=3600)
+        except subprocess.TimeoutExpired:
+            ch.kill()
+            out, err = ch.communicate()
+        if ch.returncode != 0:
+            errors.append(err[-2000:])
+        else:
+            results.append(json.loads(out.strip().splitlines()[-1]))
+    if errors or not results:
+        raise RuntimeError(f"oracle timing failed: {(errors or ['no result'])[0]}")
+    return combine_oracle_results(results)
+
+
+def oracle_procs(args) -> int:
+    return args.cpu_procs if args.cpu_procs > 0 else min(host_cores(), 32)
 
 
 def oracle_sample(res, workload):
-    return (f"{res['steps']} steps, each one token of the {workload} layer: the whole router and one of its kept "
-            f"experts in turn (router {res['router_ms']:.1f} ms, expert {res['expert_ms']:.0f} ms, {res['kept']:.1f} "
-            "kept); value = router + kept x expert")
+    procs = res.get("procs", 1)
+    return (f"{procs} single-threaded oracle processes side by side, {res['steps']} steps in all, each one token of "
+            f"the {workload} layer: the whole router and one of its kept experts in turn (router "
+            f"{res['router_ms']:.1f} ms, expert {res['expert_ms']:.0f} ms, {res['kept']:.1f} kept); per process "
+            f"router + kept x expert ({res.get('single_core_us', res['us_per_layer']) / 1000:.0f} ms per layer on one "
+            "core); value = 1 / (sum of the processes' layer rates)")
 
 
 def reference_arm(args, rank, world):
@@ -542,16 +593,19 @@ def reference_arm(args, rank, world):
         return 0
     from int4_grouped_expert_router_gb300.workload import CONFIGS
     cfg = CONFIGS[args.workload]
-    res = run_oracle_steps(args.workload, args.steps, args.warmup)
+    try:
+        res = run_oracle_steps(args.workload, args.steps, args.warmup, procs=oracle_procs(args))
+    except RuntimeError:  # e.g. too little host memory for one process per core: one process
+        res = run_oracle_steps(args.workload, args.steps, args.warmup, procs=1)
     v = res["us_per_layer"]
     line = {
-        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": res["steps"],
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": res["warmup"], "ms_per_step": res["ms_per_step"], "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded SplitMix64; shapes of the pages' GLM-5.2 decode layer)",
         "config": {"workload": workload_desc(cfg)},
-        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": oracle_sample(res, args.workload)},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": res["procs"], "kind": "oracle",
+                         "single_core_value": res["single_core_us"], "sample": oracle_sample(res, args.workload)},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -837,11 +891,11 @@ def gpu_arm(args, rank, world, local):
                      w=np.stack([outs[s]["w"].cpu().numpy() for s in timed]),
                      n_sel=np.stack([outs[s]["n_sel"].cpu().numpy() for s in timed]),
                      y=np.stack([outs[s]["y"].float().cpu().numpy() for s in timed[:n_ffn]]))
-            # about 10 s of single-threaded oracle, and the check of the timed tokens against it
-            res = run_oracle_steps(args.workload, 40, 1, check)
+            # about 10 s of oracle on every core, and the check of the timed tokens against it
+            res = run_oracle_steps(args.workload, 40, 1, check, procs=oracle_procs(args))
             accuracy = res.get("accuracy")
-            cpu = {"value": res["us_per_layer"], "unit": UNIT, "cores": 1, "kind": "oracle",
-                   "sample": oracle_sample(res, args.workload)}
+            cpu = {"value": res["us_per_layer"], "unit": UNIT, "cores": res["procs"], "kind": "oracle",
+                   "single_core_value": res["single_core_us"], "sample": oracle_sample(res, args.workload)}
         except Exception as exc:  # the CPU leg must not hide the GPU number
             cpu = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": f"failed: {exc}"[:300]}
         p50 = statistics.median(step_ms) * 1000.0
@@ -994,7 +1048,7 @@ def ep_arm(args, rank, world, local):
 def main():
     args = parse()
     if args.cpu_steps:
-        cpu_step_worker(args.workload, args.cpu_steps, args.warmup, args.check)
+        cpu_step_worker(args.workload, args.cpu_steps, args.warmup, args.check, args.cpu_offset)
         return 0
     rank, world, local = dist_env()
     if args.impl == "reference":
