@@ -213,11 +213,19 @@ COLI_API int coli_expert_table_set(coli_ctx *ctx, int e, uint64_t gate, uint64_t
  * and y is rounded to bf16 once at the end). idx, w, n_sel: as produced by coli_router_select,
  * device pointers. Slots with idx < 0 beyond n_sel are ignored. D and I come from the table.
  * Every weight byte of an expert is read once per call however many of the S tokens chose it.
- * Kernel forms: with S == 1, a gate/up kernel and a down kernel chained by programmatic dependent
- * launch; with COLI_DECODE_FUSED=1 in the environment at coli_init, one cooperative kernel for the
- * whole call (profiled as COLI_KERNEL_GATEUP) where the device supports cooperative launch and
- * I <= 4096. The two forms give bit-identical y. bf16 batches with enough routed rows per expert
- * run on the tensor cores instead ([tcgate]).
+ * Kernel forms, chosen on the host:
+ *   - S == 1, every expert of the table streamable (D a multiple of 1024 and at most 6144, I a
+ *     multiple of 16, every group size 0 or a multiple of 32): one persistent streaming kernel that
+ *     runs each kept expert's gate, up and down rows as 16-row units, then a reduce kernel chained
+ *     by programmatic dependent launch (profiled as COLI_KERNEL_GATEUP and COLI_KERNEL_COMBINE).
+ *     The library keeps a panel-major copy of each such down tensor for it (made at table_set).
+ *     COLI_DECODE_STREAM=0 in the environment at coli_init turns this form off.
+ *   - Otherwise, S == 1: a gate/up kernel and a down kernel chained by programmatic dependent
+ *     launch; with COLI_DECODE_FUSED=1 in the environment at coli_init, one cooperative kernel for
+ *     the whole call (profiled as COLI_KERNEL_GATEUP) where the device supports cooperative launch
+ *     and I <= 4096. These two forms give bit-identical y.
+ *   - S > 1: the gate/up and down kernels over every token's routes, then a slot-ordered combine;
+ *     bf16 batches with enough routed rows per expert run on the tensor cores instead ([tcgate]).
  */
 COLI_API int coli_expert_group(coli_ctx *ctx, const void *x_rows, int x_dtype, int S,
                       const int32_t *idx, const float *w, const int32_t *n_sel, int K,
