@@ -38,7 +38,8 @@ namespace coli {
 #ifndef COLI_PF_CONV_WARPS
 #define COLI_PF_CONV_WARPS 16
 #endif
-constexpr int kPfRows = COLI_PF_ROWS;  // tokens (GEMM N) per work entry
+constexpr int kPfRows = COLI_PF_ROWS;  // tokens (the MMA's M) per work entry
+static_assert(kPfRows == 128, "the epilogue reads the accumulator in the M = 128 layout: a token per lane");
 constexpr int kPfPad = 16;      // per-entry token blocks are padded to a multiple of 16
 constexpr int kPfKTile = 64;    // K columns per pipeline stage
 constexpr int kPfConvWarps = COLI_PF_CONV_WARPS;  // warps 3.. convert; warps 4..7 also drain the accumulator
@@ -443,6 +444,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) pf_gemm_kernel(PfGemmParams P, 
     constexpr int kParts = kPfConvWarps * 32 / (Lay::kT * kTcRows);
     constexpr int kW = 8 / kParts;  // words of a 64-column K tile (8 words per row) per thread
     static_assert(kParts * kW == 8 && kW >= 2, "converter split");
+    static_assert(kW <= 4, "a thread's columns of a K tile must lie in one 32-column part (one scale)");
     const int r = ct & (kTcRows - 1);
     const int x = ct / (kTcRows * kParts);   // weight tile of the block
     const int w0 = ((ct / kTcRows) % kParts) * kW;
