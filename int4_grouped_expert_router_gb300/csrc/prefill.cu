@@ -44,6 +44,7 @@ constexpr int kPfPad = 16;      // per-entry token blocks are padded to a multip
 constexpr int kPfKTile = 64;    // K columns per pipeline stage
 constexpr int kPfConvWarps = COLI_PF_CONV_WARPS;  // warps 3.. convert; warps 4..7 also drain the accumulator
 constexpr int kPfThreads = (3 + kPfConvWarps) * 32;  // + the two producer warps and the MMA warp
+static_assert(kPfThreads <= 1024, "one CTA holds every role");
 constexpr uint32_t kPfTileBytes = kTcRows * 128;       // one bf16 operand tile: 128 rows x 128 bytes
 constexpr uint32_t kPfPackedBytes = kTcRows * kTcWords * 4;  // one packed int4 weight tile (4 K tiles)
 constexpr int kPfSuper = kTcWords * 8 / kPfKTile;            // K tiles per packed tile
